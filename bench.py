@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Throughput of the linear-attention hot path on GB300, one JSON line on rank 0.
+
+Headline step: one causal forward (keeping Out) plus one causal backward on the
+training workload B=4, H=16, N=8192, D=M=64, bf16 storage, fp32 accumulation.
+tokens/s counts (b, n) positions across all heads: B*N tokens per step.
+
+Also measured in the same run (the "paths" object): the causal forward alone,
+the long-sequence forward (B=1, H=16, N=65536, D=M=128), the non-causal fp32
+forward (B=8, H=8, N=4096, D=M=64) and one decode step of 256 sequences x 16
+heads (D=M=64, fp32 state), each with its fraction of the HBM roofline.
+
+Timing: W untimed warm-up steps, then K steps between a barrier and a device
+synchronize, timed with CUDA events on the launching stream; max over ranks.
+The training inputs (4 x 64 MiB) exceed L2, so consecutive steps do not reuse
+L2; the decode state (64 MiB) fits in L2, so the decode path flushes L2 (a
+256 MiB write) before each timed step and times only the step itself.
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal linear-attn tokens/s (fwd, fwd+bwd, decode) and % of roofline"
+HEADLINE = "causal_train_bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _csrc_hash() -> str:
+    d = os.path.join(ROOT, "linear_attention_02_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(key: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if absent/stale."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(key)
+    if not e or e.get("csrc_hash") != _csrc_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads
+
+def _bytes_fwd(B, H, N, D, M, esz):
+    return B * H * N * (2 * D + 2 * M) * esz  # read Q, K, V; write Out
+
+
+def _bytes_bwd(B, H, N, D, M, esz, with_out=True):
+    # read Q, K, V, dOut (+ Out); write dQ, dK, dV
+    return B * H * N * (2 * D + 2 * M + (M if with_out else 0) + 2 * D + M) * esz
+
+
+def _bytes_decode(B, H, D, M, esz):
+    return B * H * (2 * D * M * 4 + 2 * D * 4 + (2 * D + M) * esz + M * 4)
+
+
+def _time_events(torch, fn, reps, stream, flush=None):
+    """Mean device ms of fn over reps, events on `stream`; optional untimed flush before each."""
+    total = 0.0
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        total += a.elapsed_time(b)
+    return total / reps
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import linear_attention_02_gb300 as la
+    from linear_attention_02_gb300 import synth
+
+    hbm, peak_src = _peaks()
+    stream = torch.cuda.current_stream()
+    w = synth.WORKLOADS[HEADLINE]
+    B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
+    seed = w.seed + 7919 * rank  # each rank its own batch (weak scaling)
+    x = synth.qkv(B, H, N, D, M, w.dtype, seed, w.scale, with_grad=True, device="cuda")
+    Q, K, V, G = x["Q"], x["K"], x["V"], x["G"]
+    O = torch.empty_like(V)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+
+    ev = []
+
+    def step(record=False):
+        if record:
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+        la.la_forward_causal(Q, K, V, out=O)
+        if record:
+            e1.record(stream)
+        la.la_backward_causal(Q, K, V, G, Out=O, dQ=dQ, dK=dK, dV=dV)
+        if record:
+            e2.record(stream)
+            ev.append((e0, e1, e2))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches0 = la.la_kernel_launch_count()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    launches = la.la_kernel_launch_count() - launches0
+    ms_total = t0.elapsed_time(t1)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens = B * N * world
+    value = tokens / (ms_step / 1e3)
+
+    # end to end: pinned host inputs -> device -> fwd + bwd -> host outputs
+    hx = {k: v.cpu().pin_memory() for k, v in x.items()}
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (O, dQ, dK, dV)]
+    dx = {k: torch.empty_like(v) for k, v in x.items()}
+
+    def e2e_step():
+        for k in dx:
+            dx[k].copy_(hx[k], non_blocking=True)
+        la.la_forward_causal(dx["Q"], dx["K"], dx["V"], out=O)
+        la.la_backward_causal(dx["Q"], dx["K"], dx["V"], dx["G"], Out=O, dQ=dQ, dK=dK, dV=dV)
+        for h, d in zip(hout, (O, dQ, dK, dV)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    b.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in hx.values())
+    d2h = sum(h.numel() * h.element_size() for h in hout)
+
+    esz = 2
+    fwd_bytes = _bytes_fwd(B, H, N, D, M, esz)
+    bwd_bytes = _bytes_bwd(B, H, N, D, M, esz, with_out=True)
+    dom, dom_ms, dom_bytes = ("la_backward_causal", bwd_ms, bwd_bytes) if bwd_ms >= fwd_ms else \
+        ("la_forward_causal", fwd_ms, fwd_bytes)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+                "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": _traffic(f"{HEADLINE}/{dom}"),
+                "algorithmic_bytes": dom_bytes, "avg_ms": round(dom_ms, 5)}
+
+    paths = None
+    if not args.no_paths:
+        paths = measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_bytes,
+                              B * N)
+
+    if world > 1:
+        dist.barrier()
+    out = None
+    if rank == 0:
+        clocks = clk.summary()
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{HEADLINE}: causal linear attention fwd+bwd, B={B} H={H} "
+                                   f"N={N} D=M={D}, bf16 storage, fp32 accumulation, "
+                                   "phi=elu+1, Out kept from the forward",
+                       "global_batch": B * world, "seq_len": N, "heads": H, "head_dim": D,
+                       "parallelism": f"replicas x{world} (independent batches, no collective)",
+                       "l2": "inputs larger than L2 (4 x 64 MiB resident per rank)"},
+            "roofline": roofline,
+            "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "paths": paths,
+        }
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(synth)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return out
+
+
+def measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_bytes, tok):
+    res = {}
+
+    def entry(ms, byts, tokens, extra=None):
+        gbs = byts / (ms / 1e3) / 1e9
+        d = {"ms": round(ms, 5), "tokens_per_s": round(tokens / (ms / 1e3), 1),
+             "algorithmic_bytes": byts, "achieved_gbs": round(gbs, 1),
+             "hbm_frac": round(gbs / hbm, 4)}
+        if extra:
+            d.update(extra)
+        return d
+
+    res["causal_train_bf16/fwd"] = entry(fwd_ms, fwd_bytes, tok)
+    res["causal_train_bf16/bwd"] = entry(bwd_ms, bwd_bytes, tok)
+    res["causal_train_bf16/fwd+bwd"] = entry(fwd_ms + bwd_ms, fwd_bytes + bwd_bytes, tok)
+
+    w = synth.WORKLOADS["causal_long_bf16"]
+    x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, device="cuda")
+    O = torch.empty_like(x["V"])
+    f = lambda: la.la_forward_causal(x["Q"], x["K"], x["V"], out=O)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 10, stream)
+    res["causal_long_bf16/fwd"] = entry(ms, _bytes_fwd(w.B, w.H, w.N, w.D, w.M, 2), w.B * w.N)
+    del x, O
+
+    w = synth.WORKLOADS["noncausal_f32"]
+    x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, device="cuda")
+    O = torch.empty_like(x["V"])
+    f = lambda: la.la_forward_noncausal(x["Q"], x["K"], x["V"], out=O)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 20, stream)
+    res["noncausal_f32/fwd"] = entry(ms, _bytes_fwd(w.B, w.H, w.N, w.D, w.M, 4), w.B * w.N)
+    del x, O
+
+    w = synth.WORKLOADS["decode_bf16"]
+    B, H, D, M = w.B, w.H, w.D, w.M
+    S = torch.randn(B, H, D, M, device="cuda").abs_()
+    Z = torch.rand(B, H, D, device="cuda").add_(1.0)
+    steps = [synth.decode_step_qkv(B, H, D, M, w.dtype, w.seed, t, device="cuda") for t in range(8)]
+    out = torch.empty(B, H, M, device="cuda")
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, device="cuda")
+    it = [0]
+
+    def dec():
+        s = steps[it[0] % len(steps)]
+        it[0] += 1
+        la.la_decode_step(s["q"], s["k"], s["v"], S, Z, out=out)
+
+    for _ in range(3):
+        dec()
+    ms = _time_events(torch, dec, 50, stream, flush=lambda: flush_buf.fill_(1.0))
+    ms_warm = _time_events(torch, dec, 50, stream)
+    res["decode_bf16/step"] = entry(ms, _bytes_decode(B, H, D, M, 2), B,
+                                    {"l2": "flushed before each step",
+                                     "ms_l2_warm": round(ms_warm, 5)})
+    return res
+
+
+def cpu_baseline(synth, steps: int = 1):
+    """The fp64 oracle on host cores over a bounded sample of the headline workload."""
+    import oracle
+    w = synth.WORKLOADS[HEADLINE]
+    cores = oracle.default_threads()
+    heads = max(1, min(w.B * w.H, 2 * cores))
+    x = synth.qkv(1, heads, w.N, w.D, w.M, w.dtype, w.seed, w.scale, with_grad=True)
+    Q, K, V, G = (x[n] for n in ("Q", "K", "V", "G"))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.causal_forward_recurrent(Q, K, V, nthreads=cores)
+        oracle.causal_backward_cumsum(Q, K, V, G, nthreads=cores)
+    dt = (time.perf_counter() - t0) / steps
+    # heads / H of the B*N tokens of a step are covered per sample
+    tokens = w.N * heads / w.H
+    return {"value": round(tokens / dt, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} heads x N={w.N} (D=M={w.D}) of the fwd+bwd step, fp64 recurrent "
+                      f"forward + cumulative-sum backward, {dt:.2f} s per sample"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from linear_attention_02_gb300 import synth  # noqa: F401 (inputs only)
+    w = synth.WORKLOADS[HEADLINE]
+    for _ in range(max(0, min(args.warmup, 1))):
+        cpu_baseline(synth)
+    t0 = time.perf_counter()
+    samples = [cpu_baseline(synth) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    v = statistics.mean(s["value"] for s in samples)
+    tokens_per_sample = v * (wall / max(args.steps, 1))
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "tokens/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(wall / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"{HEADLINE}: causal linear attention fwd+bwd, B={w.B} H={w.H} "
+                                  f"N={w.N} D=M={w.D}, bf16 inputs evaluated in fp64",
+                      "global_batch": w.B, "seq_len": w.N},
+           "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s", "kind": "oracle",
+                            "cores": samples[0]["cores"], "sample": samples[0]["sample"]},
+           "e2e": {"value": round(v, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    del tokens_per_sample
+    print(json.dumps(out), flush=True)
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-paths", action="store_true", help="headline step only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,133 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) kernelized linear-attention library.
+ *
+ * The method ("Transformers are RNNs", as explained on wkq9411.github.io,
+ * "【论文解读】Transformers are RNNs"): with phi(x) = elu(x) + 1 (section
+ * 特征映射, eq. elu, alpha = 1),
+ *
+ *     V'_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i,                       (eq. output)
+ *     S_i  = sum_{j<=i} phi(K_j) V_j^T,   Z_i = sum_{j<=i} phi(K_j)   (section 三)
+ *
+ * in the causal case (diagonal included, eq. mask) and with full sums in the
+ * non-causal case (section 二, eq. linear).  No scaling is applied to Q or K.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are contiguous, row-major, in DEVICE memory of the current CUDA
+ *   device: Q, K are [B][H][N][D]; V, Out, dOut are [B][H][N][M]; states S are
+ *   [B][H][D][M] and Z are [B][H][D], always fp32.  Every non-empty tensor
+ *   pointer must be 16-byte aligned.
+ * - dtype: LA_DTYPE_F32 (fp32 storage) or LA_DTYPE_BF16 (bf16 storage).
+ *   Outputs have the input dtype, except decode `out` and all states (fp32).
+ *   All accumulation is fp32.
+ * - Supported head sizes: D, M in {32, 64, 128}.  B, H, N >= 0; a call with
+ *   B*H*N == 0 does no work and succeeds.  B*H*N*max(D,M) < 2^40.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *   asynchronous on that stream; arguments are validated on the host before
+ *   anything is enqueued, and an invalid call enqueues nothing.
+ * - Ownership: the caller owns every buffer it passes.  The library never
+ *   frees caller memory.  Per-call scratch (span states, gradient rows) is
+ *   taken stream-ordered from a library-owned CUDA memory pool of the current
+ *   device and given back on the same stream.
+ * - Errors: a status code; no exception or abort crosses the ABI.  On error,
+ *   la_last_error_message() gives a one-line reason (per host thread).
+ *
+ * Library scratch is stream-ordered, so calls on different streams may run
+ * concurrently.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, overflow */
+    LA_ERR_UNSUPPORTED = 2, /* D or M not in {32, 64, 128}, unknown dtype */
+    LA_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has details) */
+    LA_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see la_check_device_status) */
+} la_status;
+
+typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
+
+/*
+ * Causal forward V' = phi(Q) S_i / phi(Q) Z_i ("Transformers are RNNs",
+ * section 三, eq. mask and eq. output).
+ *   Q, K    [B][H][N][D] dtype          (read)
+ *   V       [B][H][N][M] dtype          (read)
+ *   Out     [B][H][N][M] dtype          (written)
+ *   S_init  [B][H][D][M] fp32, nullable (read)  state before token 0 (0 if NULL)
+ *   Z_init  [B][H][D]    fp32, nullable (read)  must be NULL iff S_init is NULL
+ *   S_final [B][H][D][M] fp32, nullable (written) state after token N-1
+ *   Z_final [B][H][D]    fp32, nullable (written) must be NULL iff S_final is NULL
+ * With S_init/Z_init a sequence can be processed in pieces; S_final/Z_final
+ * hand a prefill's state to la_decode_step (section 三（二）: the state phi(K)V^T
+ * is kept as an internal RNN state).  Out may not alias any input.
+ */
+la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out,
+                            int B, int H, int N, int D, int M, la_dtype dtype,
+                            const float* S_init, const float* Z_init,
+                            float* S_final, float* Z_final, void* stream);
+
+/*
+ * Causal backward of L(Out) given dOut = dL/dOut: the numerator gradients of
+ * section 三（一）4 (eqs. gq-gv: a prefix state for phi(Q), a suffix state for
+ * phi(K) and V), the denominator by the quotient rule, then the chain rule
+ * through phi.
+ *   Q, K [B][H][N][D]; V, dOut [B][H][N][M] dtype        (read)
+ *   Out  [B][H][N][M] dtype, nullable                    (read) the forward's
+ *        output; when NULL it is recomputed.
+ *   dQ, dK [B][H][N][D]; dV [B][H][N][M] dtype           (written)
+ * Outputs may not alias inputs or each other.
+ */
+la_status la_backward_causal(const void* Q, const void* K, const void* V, const void* Out,
+                             const void* dOut, void* dQ, void* dK, void* dV,
+                             int B, int H, int N, int D, int M, la_dtype dtype, void* stream);
+
+/*
+ * Non-causal forward V' = phi(Q)(phi(K)^T V) / phi(Q) sum_j phi(K_j)
+ * ("Transformers are RNNs", section 二, eq. linear and the matrix form
+ * (phi(Q)phi(K)^T)V = phi(Q)(phi(K)^T V)).
+ *   Q, K [B][H][N][D]; V [B][H][N][M] dtype (read);  Out [B][H][N][M] dtype (written).
+ */
+la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void* Out,
+                               int B, int H, int N, int D, int M, la_dtype dtype,
+                               void* stream);
+
+/*
+ * One recurrent decode step for B*H independent heads ("Transformers are
+ * RNNs" section 四, the RNN form; "Transformer与RNN的深层联结" section 2,
+ * RNN-mode inference): first S += phi(k) v^T and Z += phi(k), then
+ * out = phi(q)^T S / phi(q)^T Z.
+ *   q, k [B][H][D]; v [B][H][M] dtype     (read)
+ *   S [B][H][D][M], Z [B][H][D] fp32      (read and updated in place)
+ *   out [B][H][M] fp32                    (written)
+ * The caller owns S and Z (a session's state can be saved, restored or moved
+ * by copying them).  out may not alias S, Z or the inputs.
+ */
+la_status la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
+                         float* out, int B, int H, int D, int M, la_dtype dtype, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word set by bounded device-side waits.  LA_ERR_TIMEOUT if one gave up since
+ * the last check, LA_ERR_CUDA if the stream reported an error, else LA_OK. */
+la_status la_check_device_status(void* stream);
+
+/* Static text of a status code. */
+const char* la_status_string(la_status status);
+
+/* One-line reason for the last non-LA_OK status returned on this host thread. */
+const char* la_last_error_message(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t la_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LINATTN_H */

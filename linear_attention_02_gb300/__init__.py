@@ -1,0 +1,170 @@
+"""GB300 (sm_103a) kernelized linear attention, phi(x) = elu(x) + 1.
+
+Thin Python binding over the C ABI of include/linattn.h.  The functions carry
+the C names and only marshal arguments: torch supplies device memory and the
+current CUDA stream; every step of the computation runs in liblinattn.so.
+
+    la_forward_causal(Q, K, V, ...)      V'_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i, j <= i
+    la_backward_causal(Q, K, V, dOut, ...)
+    la_forward_noncausal(Q, K, V, ...)   phi(Q)(phi(K)^T V) / phi(Q) sum phi(K)
+    la_decode_step(q, k, v, S, Z, ...)   S += phi(k)v^T, Z += phi(k); read with q
+
+Shapes: Q, K [B,H,N,D]; V [B,H,N,M]; S [B,H,D,M] fp32; Z [B,H,D] fp32.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+
+_lib = _native.lib
+
+_DT = {torch.float32: _native.LA_DTYPE_F32, torch.bfloat16: _native.LA_DTYPE_BF16}
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_lib.la_status_string(status).decode()}: {msg}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != _native.LA_OK:
+        raise LinAttnError(status, (_lib.la_last_error_message() or b"").decode())
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _dims(Q, V):
+    if Q.dim() != 4 or V.dim() != 4:
+        raise ValueError("Q/K must be [B,H,N,D] and V [B,H,N,M]")
+    B, H, N, D = Q.shape
+    if tuple(V.shape[:3]) != (B, H, N):
+        raise ValueError(f"V shape {tuple(V.shape)} does not match Q {tuple(Q.shape)}")
+    return B, H, N, D, V.shape[3]
+
+
+def _dtype(t):
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    return _DT[t.dtype]
+
+
+def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=False,
+                      stream=None):
+    """Causal forward.  Returns Out, or (Out, S_final, Z_final) with return_state."""
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, Q.dtype, dev)
+    if K.shape != Q.shape:
+        raise ValueError("K must have the shape of Q")
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=Q.dtype, device=dev)
+    _need(out, "out", Q.dtype, dev)
+    if (S_init is None) != (Z_init is None):
+        raise ValueError("give both S_init and Z_init, or neither")
+    if S_init is not None:
+        _need(S_init, "S_init", torch.float32, dev)
+        _need(Z_init, "Z_init", torch.float32, dev)
+    S_f = Z_f = None
+    if return_state:
+        S_f = torch.empty((B, H, D, M), dtype=torch.float32, device=dev)
+        Z_f = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_forward_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D, M,
+                                      _dtype(Q), _ptr(S_init), _ptr(Z_init), _ptr(S_f), _ptr(Z_f),
+                                      _stream_handle(stream)))
+    return (out, S_f, Z_f) if return_state else out
+
+
+def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, stream=None):
+    """Causal backward; returns (dQ, dK, dV).  Out (the forward output) is optional."""
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (dOut, "dOut")):
+        _need(t, n, Q.dtype, dev)
+    if Out is not None:
+        _need(Out, "Out", Q.dtype, dev)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        _need(t, n, Q.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_backward_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Out), _ptr(dOut), _ptr(dQ),
+                                       _ptr(dK), _ptr(dV), B, H, N, D, M, _dtype(Q),
+                                       _stream_handle(stream)))
+    return dQ, dK, dV
+
+
+def la_forward_noncausal(Q, K, V, out=None, stream=None):
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, Q.dtype, dev)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=Q.dtype, device=dev)
+    _need(out, "out", Q.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_forward_noncausal(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D, M,
+                                         _dtype(Q), _stream_handle(stream)))
+    return out
+
+
+def la_decode_step(q, k, v, S, Z, out=None, stream=None):
+    """One decode step; updates S, Z in place and returns out [B,H,M] fp32."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q/k must be [B,H,D] and v [B,H,M]")
+    B, H, D = q.shape
+    M = v.shape[2]
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(S, "S", torch.float32, dev)
+    _need(Z, "Z", torch.float32, dev)
+    if tuple(S.shape) != (B, H, D, M) or tuple(Z.shape) != (B, H, D):
+        raise ValueError("S must be [B,H,D,M] and Z [B,H,D]")
+    if out is None:
+        out = torch.empty((B, H, M), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(Z), _ptr(out), B, H, D,
+                                   M, _dtype(q), _stream_handle(stream)))
+    return out
+
+
+def la_check_device_status(stream=None):
+    _check(_lib.la_check_device_status(_stream_handle(stream)))
+
+
+def la_kernel_launch_count() -> int:
+    return int(_lib.la_kernel_launch_count())
+
+
+def la_status_string(status: int) -> str:
+    return _lib.la_status_string(int(status)).decode()
+
+
+def la_last_error_message() -> str:
+    return (_lib.la_last_error_message() or b"").decode()

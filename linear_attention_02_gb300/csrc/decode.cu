@@ -1,0 +1,122 @@
+// decode.cu -- one recurrent decode step per head, bandwidth-bound.
+//
+// RNN form of "Transformers are RNNs" (section 四) in the order of RNN-mode
+// inference ("Transformer与RNN的深层联结", section 2): update first,
+//   S += phi(k) v^T,  Z += phi(k),
+// then read
+//   out = phi(q)^T S / phi(q)^T Z.
+// The fp32 state S [D][M] is streamed once in and once out with 128-bit
+// accesses; the read-out is fused into the same pass over S (each thread
+// forms phi(q)_d * S_new[d][e] for its rows and the partial sums are reduced
+// with warp shuffles, then across warps in shared memory).
+#include "la_common.cuh"
+#include "la_launch.h"
+
+namespace la {
+
+namespace {
+
+constexpr int kDecThreads = 256;
+
+template <typename T, int D, int M>
+__global__ void __launch_bounds__(kDecThreads)
+decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   float* __restrict__ S, float* __restrict__ Z, float* __restrict__ out, int BH) {
+    constexpr int CG = M / 4;                 // float4 column groups of a row of S
+    constexpr int RG = kDecThreads / CG;      // row groups
+    constexpr int RPT = D / RG;               // rows per thread
+    constexpr int WARPS = kDecThreads / 32;
+    static_assert(RPT >= 1 && D % RG == 0, "shape");
+    __shared__ float fq[D], fk[D], vv[M];
+    __shared__ float4 red[WARPS][CG < 32 ? CG : 32];
+    __shared__ float den_s;
+    const int bh = blockIdx.x;
+    const int t = threadIdx.x;
+    for (int i = t; i < D; i += kDecThreads) {
+        fq[i] = phi(to_f(q[(size_t)bh * D + i]));
+        fk[i] = phi(to_f(k[(size_t)bh * D + i]));
+    }
+    for (int i = t; i < M; i += kDecThreads) vv[i] = to_f(v[(size_t)bh * M + i]);
+    __syncthreads();
+
+    const int cg = t % CG, rg = t / CG;
+    float4* S4 = reinterpret_cast<float4*>(S + (size_t)bh * D * M);
+    const float4 v4 = make_float4(vv[4 * cg], vv[4 * cg + 1], vv[4 * cg + 2], vv[4 * cg + 3]);
+    float4 s[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) s[r] = (S4[(size_t)(rg + r * RG) * CG + cg]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int d = rg + r * RG;
+        const float a = fk[d], b = fq[d];
+        s[r].x = fmaf(a, v4.x, s[r].x);
+        s[r].y = fmaf(a, v4.y, s[r].y);
+        s[r].z = fmaf(a, v4.z, s[r].z);
+        s[r].w = fmaf(a, v4.w, s[r].w);
+        S4[(size_t)d * CG + cg] = s[r];
+        acc.x = fmaf(b, s[r].x, acc.x);
+        acc.y = fmaf(b, s[r].y, acc.y);
+        acc.z = fmaf(b, s[r].z, acc.z);
+        acc.w = fmaf(b, s[r].w, acc.w);
+    }
+    // reduce over the row groups held by this warp (lanes cg, cg + CG, ...)
+#pragma unroll
+    for (int o = CG; o < 32; o <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+    }
+    const int warp = t >> 5, lane = t & 31;
+    if (lane < CG) red[warp][lane] = acc;
+    if (warp == 0) {
+        // Z update and denominator: phi(q) . (Z + phi(k))
+        float dsum = 0.f;
+        for (int d = lane; d < D; d += 32) {
+            const float z = Z[(size_t)bh * D + d] + fk[d];
+            Z[(size_t)bh * D + d] = z;
+            dsum = fmaf(fq[d], z, dsum);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+        if (lane == 0) den_s = dsum;
+    }
+    __syncthreads();
+    if (t < CG) {
+        // warps that hold distinct row groups: each warp covers 32 / CG row groups
+        float4 a = red[0][t];
+        for (int w = 1; w < WARPS; ++w) {
+            const float4 b = red[w][t];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        const float inv_den = 1.f / den_s;
+        float4 o4 = make_float4(a.x * inv_den, a.y * inv_den, a.z * inv_den, a.w * inv_den);
+        reinterpret_cast<float4*>(out + (size_t)bh * M)[t] = o4;
+    }
+}
+
+}  // namespace
+
+template <typename T, int D, int M>
+cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
+                        float* Z, float* out, int BH) {
+    decode_step_kernel<T, D, M><<<BH, kDecThreads, 0, c.stream>>>(q, k, v, S, Z, out, BH);
+    note_launch();
+    return cudaGetLastError();
+}
+
+#define LA_INST_DEC(T, D, M)                                                                      \
+    template cudaError_t decode_step<T, D, M>(const LaunchCtx&, const T*, const T*, const T*,    \
+                                              float*, float*, float*, int);
+#define LA_INST_DEC_T(T) \
+    LA_INST_DEC(T, 32, 32) LA_INST_DEC(T, 32, 64) LA_INST_DEC(T, 32, 128) \
+    LA_INST_DEC(T, 64, 32) LA_INST_DEC(T, 64, 64) LA_INST_DEC(T, 64, 128) \
+    LA_INST_DEC(T, 128, 32) LA_INST_DEC(T, 128, 64) LA_INST_DEC(T, 128, 128)
+LA_INST_DEC_T(float)
+LA_INST_DEC_T(__nv_bfloat16)
+
+}  // namespace la

@@ -1,0 +1,311 @@
+// la_api.cu -- the C ABI declared in include/linattn.h: argument validation,
+// per-device context (SM count, scratch pool, device error word) and dispatch
+// to the kernels for each (dtype, D, M).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "la_launch.h"
+#include "linattn.h"
+
+namespace la {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_msg[512] = "";
+
+la_status fail(la_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+la_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(LA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    cudaMemPool_t pool = nullptr;
+    unsigned int* status_word = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+la_status get_ctx(cudaStream_t stream, LaunchCtx* ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(LA_ERR_CUDA, "device ordinal %d out of range", dev);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!d.ready) {
+            int sms = 0;
+            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+                return cuda_fail(e, "cudaDeviceGetAttribute");
+            cudaMemPoolProps props;
+            memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t pool = nullptr;
+            if ((e = cudaMemPoolCreate(&pool, &props))) return cuda_fail(e, "cudaMemPoolCreate");
+            uint64_t keep = ~0ull;  // keep freed scratch in the pool between calls
+            if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)))
+                return cuda_fail(e, "cudaMemPoolSetAttribute");
+            unsigned int* word = nullptr;
+            if ((e = cudaMalloc(&word, 256))) return cuda_fail(e, "cudaMalloc(status word)");
+            if ((e = cudaMemset(word, 0, 256))) return cuda_fail(e, "cudaMemset(status word)");
+            d.num_sms = sms;
+            d.pool = pool;
+            d.status_word = word;
+            d.ready = true;
+        }
+    }
+    ctx->stream = stream;
+    ctx->num_sms = d.num_sms;
+    ctx->pool = d.pool;
+    ctx->status_word = d.status_word;
+    return LA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_ok(int x) { return x == 32 || x == 64 || x == 128; }
+
+// Common shape/pointer checks.  `ptrs` must be non-null and 16-byte aligned
+// whenever the work is non-empty.
+la_status check_common(const char* fn, int B, int H, int N, int D, int M, la_dtype dt,
+                       const void* const* ptrs, const char* const* names, int nptr,
+                       bool* empty) {
+    if (B < 0 || H < 0 || N < 0)
+        return fail(LA_ERR_INVALID_ARG, "%s: negative size B=%d H=%d N=%d", fn, B, H, N);
+    if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16)
+        return fail(LA_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dt);
+    if (!head_ok(D) || !head_ok(M))
+        return fail(LA_ERR_UNSUPPORTED, "%s: D=%d M=%d, supported head sizes are 32, 64, 128", fn,
+                    D, M);
+    const unsigned long long bhn = (unsigned long long)B * H * N;
+    if (bhn * (unsigned long long)(D > M ? D : M) >= (1ull << 40))
+        return fail(LA_ERR_INVALID_ARG, "%s: tensor too large", fn);
+    if ((unsigned long long)B * H >= (1ull << 31))
+        return fail(LA_ERR_INVALID_ARG, "%s: B*H too large", fn);
+    *empty = bhn == 0;
+    if (*empty) return LA_OK;
+    for (int i = 0; i < nptr; ++i) {
+        if (!ptrs[i]) return fail(LA_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
+        if (!aligned16(ptrs[i]))
+            return fail(LA_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, names[i]);
+    }
+    return LA_OK;
+}
+
+la_status check_optional(const char* fn, const void* p, const char* name) {
+    if (p && !aligned16(p)) return fail(LA_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, name);
+    return LA_OK;
+}
+
+la_status finish(cudaError_t e, const char* fn) {
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return LA_OK;
+}
+
+// Calls F::template run<T, D, M>(args...) for the runtime (dtype, D, M).
+template <class F, class... A>
+cudaError_t dispatch(la_dtype dt, int D, int M, A... a) {
+#define LA_CASE_DM(T, d, m) \
+    if (D == d && M == m) return F::template run<T, d, m>(a...);
+#define LA_CASE_T(T)                                                                  \
+    LA_CASE_DM(T, 32, 32) LA_CASE_DM(T, 32, 64) LA_CASE_DM(T, 32, 128)                \
+    LA_CASE_DM(T, 64, 32) LA_CASE_DM(T, 64, 64) LA_CASE_DM(T, 64, 128)                \
+    LA_CASE_DM(T, 128, 32) LA_CASE_DM(T, 128, 64) LA_CASE_DM(T, 128, 128)
+    if (dt == LA_DTYPE_F32) {
+        LA_CASE_T(float)
+    } else {
+        LA_CASE_T(__nv_bfloat16)
+    }
+#undef LA_CASE_T
+#undef LA_CASE_DM
+    return cudaErrorInvalidValue;
+}
+
+struct FwdCausal {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
+                           int BH, int N, const float* Si, const float* Zi, float* Sf, float* Zf) {
+        return causal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N, Si,
+                                       Zi, Sf, Zf);
+    }
+};
+struct BwdCausal {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V,
+                           const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N) {
+        return causal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
+                                        (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
+    }
+};
+struct FwdNoncausal {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
+                           int BH, int N) {
+        return noncausal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N);
+    }
+};
+struct Decode {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* q, const void* k, const void* v,
+                           float* S, float* Z, float* out, int BH) {
+        return decode_step<T, D, M>(*c, (const T*)q, (const T*)k, (const T*)v, S, Z, out, BH);
+    }
+};
+
+// Writes zeros (or the initial state) to S_final/Z_final for an N == 0 forward.
+cudaError_t empty_forward_state(cudaStream_t st, size_t bh, int D, int M, const float* Si,
+                                const float* Zi, float* Sf, float* Zf) {
+    if (!Sf || bh == 0) return cudaSuccess;
+    const size_t sb = bh * D * M * sizeof(float), zb = bh * D * sizeof(float);
+    cudaError_t e;
+    if (Si) {
+        if ((e = cudaMemcpyAsync(Sf, Si, sb, cudaMemcpyDeviceToDevice, st))) return e;
+        return cudaMemcpyAsync(Zf, Zi, zb, cudaMemcpyDeviceToDevice, st);
+    }
+    if ((e = cudaMemsetAsync(Sf, 0, sb, st))) return e;
+    return cudaMemsetAsync(Zf, 0, zb, st);
+}
+
+}  // namespace
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes) {
+    if (bytes == 0) bytes = 256;
+    return cudaMallocFromPoolAsync(p, bytes, c.pool, c.stream);
+}
+
+void scratch_free(const LaunchCtx& c, void* p) {
+    if (p) cudaFreeAsync(p, c.stream);
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out, int B, int H,
+                            int N, int D, int M, la_dtype dtype, const float* S_init,
+                            const float* Z_init, float* S_final, float* Z_final, void* stream) {
+    static const char* fn = "la_forward_causal";
+    const void* p[] = {Q, K, V, Out};
+    const char* nm[] = {"Q", "K", "V", "Out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 4, &empty);
+    if (s != LA_OK) return s;
+    if ((S_init == nullptr) != (Z_init == nullptr))
+        return fail(LA_ERR_INVALID_ARG, "%s: S_init and Z_init must both be given or both NULL", fn);
+    if ((S_final == nullptr) != (Z_final == nullptr))
+        return fail(LA_ERR_INVALID_ARG, "%s: S_final and Z_final must both be given or both NULL", fn);
+    if ((s = check_optional(fn, S_init, "S_init")) || (s = check_optional(fn, Z_init, "Z_init")) ||
+        (s = check_optional(fn, S_final, "S_final")) || (s = check_optional(fn, Z_final, "Z_final")))
+        return s;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    const size_t bh = (size_t)B * H;
+    if (empty) return finish(empty_forward_state(ctx.stream, bh, D, M, S_init, Z_init, S_final, Z_final), fn);
+    return finish(dispatch<FwdCausal>(dtype, D, M, &ctx, Q, K, V, Out, (int)bh, N, S_init, Z_init,
+                                      S_final, Z_final),
+                  fn);
+}
+
+la_status la_backward_causal(const void* Q, const void* K, const void* V, const void* Out,
+                             const void* dOut, void* dQ, void* dK, void* dV, int B, int H, int N,
+                             int D, int M, la_dtype dtype, void* stream) {
+    static const char* fn = "la_backward_causal";
+    const void* p[] = {Q, K, V, dOut, dQ, dK, dV};
+    const char* nm[] = {"Q", "K", "V", "dOut", "dQ", "dK", "dV"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 7, &empty);
+    if (s != LA_OK) return s;
+    if ((s = check_optional(fn, Out, "Out"))) return s;
+    if (empty) return LA_OK;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    return finish(dispatch<BwdCausal>(dtype, D, M, &ctx, Q, K, V, Out, dOut, dQ, dK, dV,
+                                      (int)((size_t)B * H), N),
+                  fn);
+}
+
+la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void* Out, int B,
+                               int H, int N, int D, int M, la_dtype dtype, void* stream) {
+    static const char* fn = "la_forward_noncausal";
+    const void* p[] = {Q, K, V, Out};
+    const char* nm[] = {"Q", "K", "V", "Out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 4, &empty);
+    if (s != LA_OK || empty) return s;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    return finish(dispatch<FwdNoncausal>(dtype, D, M, &ctx, Q, K, V, Out, (int)((size_t)B * H), N),
+                  fn);
+}
+
+la_status la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
+                         float* out, int B, int H, int D, int M, la_dtype dtype, void* stream) {
+    static const char* fn = "la_decode_step";
+    const void* p[] = {q, k, v, S, Z, out};
+    const char* nm[] = {"q", "k", "v", "S", "Z", "out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, 1, D, M, dtype, p, nm, 6, &empty);
+    if (s != LA_OK || empty) return s;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    return finish(dispatch<Decode>(dtype, D, M, &ctx, q, k, v, S, Z, out, (int)((size_t)B * H)), fn);
+}
+
+la_status la_check_device_status(void* stream) {
+    LaunchCtx ctx;
+    la_status s = get_ctx((cudaStream_t)stream, &ctx);
+    if (s != LA_OK) return s;
+    cudaError_t e = cudaStreamSynchronize(ctx.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status");
+    unsigned int word = 0;
+    if ((e = cudaMemcpy(&word, ctx.status_word, sizeof(word), cudaMemcpyDeviceToHost)))
+        return cuda_fail(e, "la_check_device_status");
+    if (word) {
+        const unsigned int zero = 0;
+        if ((e = cudaMemcpy(ctx.status_word, &zero, sizeof(zero), cudaMemcpyHostToDevice)))
+            return cuda_fail(e, "la_check_device_status");
+        return fail(LA_ERR_TIMEOUT, "a bounded device wait gave up (code 0x%x)", word);
+    }
+    return LA_OK;
+}
+
+const char* la_status_string(la_status status) {
+    switch (status) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+const char* la_last_error_message(void) { return g_msg; }
+
+uint64_t la_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// la_launch.h -- host-side launchers behind the C ABI (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace la {
+
+// Everything a launcher needs from the device it runs on.
+struct LaunchCtx {
+    cudaStream_t stream;
+    int num_sms;
+    cudaMemPool_t pool;          // library-owned pool for stream-ordered scratch
+    unsigned int* status_word;   // device error word for bounded waits
+};
+
+// Counts one kernel launch (la_kernel_launch_count).
+void note_launch(int n = 1);
+
+// Stream-ordered scratch from the library pool.  Returns cudaSuccess or the error.
+cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes);
+void scratch_free(const LaunchCtx& c, void* p);
+
+// Each launcher returns cudaSuccess or the first CUDA error it met.
+template <typename T, int D, int M>
+cudaError_t causal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O, int BH,
+                           int N, const float* S_init, const float* Z_init, float* S_final,
+                           float* Z_final);
+
+template <typename T, int D, int M>
+cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,
+                            const T* G, T* dQ, T* dK, T* dV, int BH, int N);
+
+template <typename T, int D, int M>
+cudaError_t noncausal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O,
+                              int BH, int N);
+
+template <typename T, int D, int M>
+cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
+                        float* Z, float* out, int BH);
+
+}  // namespace la
