@@ -113,6 +113,30 @@ la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void
 la_status la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
                          float* out, int B, int H, int D, int M, la_dtype dtype, void* stream);
 
+/*
+ * la_forward_noncausal with no device allocation.  The paper has no
+ * counterpart: this is a service for callers that may not allocate device
+ * memory inside an op -- a host framework that plans all device memory in
+ * advance and gives the op only its inputs and outputs, a plugin runtime that
+ * forbids allocation, or a latency-critical loop that cannot pay for an
+ * allocator call.  Arguments, layouts and results are those of
+ * la_forward_noncausal (up to the order of floating-point summation).
+ * Its scratch is one fixed 16 MiB file-scope device array per device, held
+ * from the moment the library's code is loaded on that device until the
+ * process exits; this call makes no cudaMalloc, cudaFree or other allocating
+ * call.  Limit: 2 * B * H * (D*M + D) * 4 bytes must fit in 16 MiB (B*H <= 127
+ * at D = M = 128, <= 504 at D = M = 64); larger calls return
+ * LA_ERR_INVALID_ARG with the sizes in the message.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current, so make the first call on each device before any stream
+ * capture.  Every call on a device shares the one array and leaves its
+ * contents behind; calls whose work overlaps on the GPU (e.g. on two streams)
+ * race on it and must be serialised by the caller.
+ */
+la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void* V, void* Out,
+                                       int B, int H, int N, int D, int M, la_dtype dtype,
+                                       void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word set by bounded device-side waits.  LA_ERR_TIMEOUT if one gave up since
  * the last check, LA_ERR_CUDA if the stream reported an error, else LA_OK. */

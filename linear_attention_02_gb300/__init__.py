@@ -132,6 +132,26 @@ def la_forward_noncausal(Q, K, V, out=None, stream=None):
     return out
 
 
+def la_forward_noncausal_noalloc(Q, K, V, out=None, stream=None):
+    """la_forward_noncausal for callers that may not allocate device memory.
+
+    The library side allocates nothing (its scratch is a fixed 16 MiB device
+    array); pass `out` to keep this Python wrapper from allocating the output.
+    Calls that overlap on the GPU share that array and must be serialised.
+    """
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, Q.dtype, dev)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=Q.dtype, device=dev)
+    _need(out, "out", Q.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_forward_noncausal_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D,
+                                                 M, _dtype(Q), _stream_handle(stream)))
+    return out
+
+
 def la_decode_step(q, k, v, S, Z, out=None, stream=None):
     """One decode step; updates S, Z in place and returns out [B,H,M] fp32."""
     if q.dim() != 3 or v.dim() != 3:

@@ -20,6 +20,7 @@ SIGNATURES = {
     "la_forward_causal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _P],
     "la_backward_causal": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_forward_noncausal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
+    "la_forward_noncausal_noalloc": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_decode_step": [_P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _P],
     "la_check_device_status": [_P],
     "la_status_string": [_I],

@@ -190,6 +190,8 @@ cudaError_t empty_forward_state(cudaStream_t st, size_t bh, int D, int M, const 
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+void set_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
 cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes) {
     if (bytes == 0) bytes = 256;
     return cudaMallocFromPoolAsync(p, bytes, c.pool, c.stream);

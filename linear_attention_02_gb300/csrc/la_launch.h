@@ -18,6 +18,9 @@ struct LaunchCtx {
 // Counts one kernel launch (la_kernel_launch_count).
 void note_launch(int n = 1);
 
+// Sets the text returned by la_last_error_message() on this host thread.
+void set_error_message(const char* msg);
+
 // Stream-ordered scratch from the library pool.  Returns cudaSuccess or the error.
 cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes);
 void scratch_free(const LaunchCtx& c, void* p);
