@@ -1,0 +1,563 @@
+// causal_tc.cu -- chunked causal linear-attention forward on the 5th-generation
+// tensor core (bf16 storage, fp32 accumulation), D = M in {64, 128}.
+//
+// Per head the sequence is cut into spans (one CTA each) and each span into
+// chunks of L = 128 tokens.  With phi(x) = elu(x) + 1 ("Transformers are RNNs",
+// section 特征映射) applied in shared memory, a chunk c needs
+//   P      = tril(phi(Q_c) phi(K_c)^T)                (intra-chunk scores, eq. mask)
+//   O_ext  = phi(Q_c) [S | Z]_{c-1} + P [V_c | 1]     (numerator and normaliser)
+//   S_ext += phi(K_c)^T [V_c | 1]                     (S_c and Z_c, the incremental update)
+// and V'_c = O_ext[:, :M] / O_ext[:, M] (eq. output).  Appending a block of
+// ones to V turns the normaliser sum phi(Q_i).Z_i into one more output column
+// of the same products, so numerator and denominator see the same rounding of
+// P and of the state.
+//
+// All four products run on tcgen05.mma (M = 128) with accumulators in TMEM:
+//   P     [128 x 128]  A = phi(Q_c) K-major,  B = phi(K_c) K-major
+//   S_ext [128 x NE]   A = phi(K_c)^T MN-major (D = 64 pads to 128 rows whose
+//                      extra rows are never read), B = [V_c | 1] MN-major
+//   O_ext [128 x NE]   A = phi(Q_c) K-major, B = [S | Z] (bf16 copy) MN-major
+//                      then A = P (bf16, masked) K-major, B = [V_c | 1]
+// Tiles arrive by TMA with the 128-byte swizzle; P, the bf16 state and the
+// output tile are written by the threads in the same swizzled layout.
+//
+// Spans: phase 1 of every span but the last accumulates its aggregate
+// (sum phi(K)^T V | sum phi(K)) and publishes it with a release flag; phase 2
+// sums the aggregates of the earlier spans of its head (bounded waits on the
+// flags) into its starting state, then runs the chunk loop.  Units are taken
+// from an atomic ticket after TMEM is allocated, so a CTA only ever waits for
+// CTAs that started (and hold their TMEM) before it.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "la_launch.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+namespace tcf {
+
+using bf16 = __nv_bfloat16;
+using namespace la::tc;
+
+constexpr int L = 128;                      // chunk length = MMA M
+constexpr int kThreads = 128;               // one thread per TMEM lane / tile row
+constexpr uint32_t kAtom = 16384;           // one 128-row atom column (128 x 128 B)
+constexpr uint32_t kWaitLimit = 1u << 24;   // mbarrier polls before giving up
+constexpr uint32_t kSpinLimit = 1u << 22;   // flag polls (256 ns apart) before giving up
+
+// Status bits written to the device error word.
+constexpr unsigned kErrWait = 1u;      // a TMA or MMA completion never arrived
+constexpr unsigned kErrLookback = 2u;  // an earlier span never published its state
+constexpr unsigned kErrAlign = 4u;     // dynamic shared memory not 1024-byte aligned
+
+template <int D, int M>
+struct Layout {
+    static constexpr int DA = D / 64;  // atom columns of a phi(Q)/phi(K) tile
+    static constexpr int MA = M / 64;  // atom columns of a V / output tile
+    static constexpr int NE = M + 16;  // M values + 16 copies of the normaliser column
+    static constexpr int W = D * M + D;  // words of a published (S | Z) state
+    // shared memory (byte offsets from a 1024-aligned base)
+    static constexpr uint32_t Q = 0;
+    static constexpr uint32_t K = Q + DA * kAtom;
+    static constexpr uint32_t V = K + DA * kAtom;      // V atoms, then the ones atom
+    static constexpr uint32_t ONES = V + MA * kAtom;
+    static constexpr uint32_t P = ONES + kAtom;        // 2 atoms; also the output staging tile
+    static constexpr uint32_t S = P + 2 * kAtom;       // (MA + 1) atoms of D rows
+    static constexpr uint32_t S_ATOM = D * 128;
+    static constexpr uint32_t BARS = S + (MA + 1) * S_ATOM;
+    static constexpr uint32_t BYTES = BARS + 64;
+    // tensor memory columns: P and O_ext share the first block, S_ext follows
+    static constexpr uint32_t T_P = 0;
+    static constexpr uint32_t T_O = 0;
+    static constexpr uint32_t T_S = NE > 128 ? 160 : 128;
+    static constexpr uint32_t T_COLS = T_S + NE <= 256 ? 256 : 512;
+    static constexpr uint32_t TX_QKV = (2 * DA + MA) * kAtom;
+    static constexpr uint32_t TX_KV = (DA + MA) * kAtom;
+    static constexpr int CTAS_PER_SM = (T_COLS <= 256 && BYTES <= 115712) ? 2 : 1;
+    static_assert(D == M && (D == 64 || D == 128), "tensor-core path covers D = M in {64, 128}");
+    static_assert(BYTES <= 227 * 1024, "shared memory");
+};
+
+struct FwdParams {
+    int N, spans, span_len;
+    float* agg;            // [units][W]
+    unsigned* flags;       // [units], zero before the launch
+    unsigned* ticket;      // zero before the launch
+    const float* S_init;   // [BH][D][M] or null
+    const float* Z_init;   // [BH][D] or null
+    float* S_final;        // [BH][D][M] or null
+    float* Z_final;        // [BH][D] or null
+    unsigned* status;      // device error word
+};
+
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// phi on two packed bf16 values.  __expf (ex2.approx based) has a relative
+// error far below the 2^-9 rounding of the bf16 result.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    float2 f = __bfloat1622float2(h);
+    f.x = f.x > 0.f ? f.x + 1.f : __expf(f.x);
+    f.y = f.y > 0.f ? f.y + 1.f : __expf(f.y);
+    return pack_bf16(f.x, f.y);
+}
+
+// phi in place over `atoms` swizzled atom columns; rows >= valid become 0 when
+// ZERO_TAIL (padding keys must not enter S or Z: phi(0) = 1).
+template <bool ZERO_TAIL>
+__device__ __forceinline__ void phi_tile(uint8_t* tile, int atoms, int valid) {
+    const int n = atoms * 1024;
+    for (int ch = threadIdx.x; ch < n; ch += kThreads) {
+        uint4* ptr = reinterpret_cast<uint4*>(tile + static_cast<size_t>(ch) * 16);
+        const int row = (ch & 1023) >> 3;
+        if (ZERO_TAIL && row >= valid) {
+            *ptr = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        uint4 u = *ptr;
+        u.x = phi_bf16x2(u.x);
+        u.y = phi_bf16x2(u.y);
+        u.z = phi_bf16x2(u.z);
+        u.w = phi_bf16x2(u.w);
+        *ptr = u;
+    }
+}
+
+// Stores 32 consecutive bf16 values (packed in pk[16]) of `row`, starting at
+// column j0, into a K-major 128-row swizzled tile.
+__device__ __forceinline__ void store_row32(uint8_t* tile, uint32_t atom_bytes, int row, int j0,
+                                            const uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int c = (j0 >> 3) + q;  // logical 16-byte chunk along the row
+        *reinterpret_cast<uint4*>(tile + (c >> 3) * atom_bytes + swz(row, c & 7)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+}
+
+template <int D, int M>
+__global__ void __launch_bounds__(kThreads, Layout<D, M>::CTAS_PER_SM)
+causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const FwdParams p) {
+    using Lay = Layout<D, M>;
+    constexpr int DA = Lay::DA, MA = Lay::MA, NE = Lay::NE, W = Lay::W;
+    constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);
+    constexpr uint32_t ID_O = idesc_bf16(128, NE, false, true);
+
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int t = threadIdx.x, warp = t >> 5;
+    if (smem_u32(sm) & 1023u) {  // the swizzled layouts need a 1024-aligned base
+        if (t == 0) atomicOr(p.status, kErrAlign);
+        return;
+    }
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+    uint64_t* mma_bar = tma_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
+    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);  // [0] unit, [1] abort
+
+    if (t == 0) {
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        fence_mbar_init();
+        sh[1] = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_relinquish();
+    }
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kThreads)  // bf16 1.0 everywhere
+        reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
+            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+    if (t == 0) sh[0] = static_cast<int>(atomicAdd(p.ticket, 1u));
+    __syncthreads();
+
+    const int unit = sh[0];
+    const int bh = unit / p.spans, s = unit - bh * p.spans;
+    const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
+    const int nch = (n1 - n0 + L - 1) / L;
+    const bool last = s == p.spans - 1;
+    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
+    const uint32_t sV = smem_u32(sm + Lay::V), sP = smem_u32(sm + Lay::P);
+    const uint32_t sS = smem_u32(sm + Lay::S);
+    uint32_t tma_phase = 0, mma_phase = 0;
+
+    auto fail = [&](unsigned code) {
+        atomicOr(p.status, code);
+        sh[1] = 1;
+    };
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
+        if (!mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        phase ^= 1u;
+    };
+    auto load = [&](int c0, bool with_q) {  // thread 0 only
+        mbar_arrive_expect_tx(tma_bar, with_q ? Lay::TX_QKV : Lay::TX_KV);
+        for (int a = 0; a < DA; ++a) {
+            if (with_q) tma_load_3d(sm + Lay::Q + a * kAtom, &tmQ, tma_bar, 64 * a, c0, bh);
+            tma_load_3d(sm + Lay::K + a * kAtom, &tmK, tma_bar, 64 * a, c0, bh);
+        }
+        for (int a = 0; a < MA; ++a)
+            tma_load_3d(sm + Lay::V + a * kAtom, &tmV, tma_bar, 64 * a, c0, bh);
+    };
+    auto mma_state_update = [&](bool accumulate_first) {  // S_ext (+)= phi(K)^T [V | 1]
+#pragma unroll
+        for (int k = 0; k < L / 16; ++k)
+            mma_bf16(tm + Lay::T_S, sdesc(sK + 2048 * k, kAtom, 1024),
+                     sdesc(sV + 2048 * k, kAtom, 1024), ID_S, (accumulate_first || k > 0) ? 1u : 0u);
+    };
+
+    // ---------------------------------------------- phase 1: span aggregate
+    if (!last) {
+        if (t == 0) load(n0, false);
+        for (int c = 0; c < nch; ++c) {
+            const int c0 = n0 + c * L;
+            wait_bar(tma_bar, tma_phase);
+            phi_tile<true>(sm + Lay::K, DA, min(L, n1 - c0));
+            fence_proxy_async();
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+            if (sh[1]) goto cleanup;
+            if (t == 0) {
+                mma_state_update(c > 0);
+                mma_commit(mma_bar);
+            }
+            wait_bar(mma_bar, mma_phase);
+            fence_after_sync();
+            if (t == 0 && c + 1 < nch) load(c0 + L, false);
+        }
+        if (warp < D / 32) {  // rows d < D of S_ext
+            float* out = p.agg + static_cast<size_t>(unit) * W;
+            const int d = t;
+            for (int j0 = 0; j0 < M; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_S + j0, v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(out + d * M + j0)[q] =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            float z[16];
+            tmem_ld16(tm + lane + Lay::T_S + M, z);
+            out[D * M + d] = z[0];
+        }
+        __threadfence();
+        fence_before_sync();
+        __syncthreads();
+        if (t == 0) st_release(p.flags + unit, 1u);
+    }
+
+    // ------------------------------ look-back: starting state of this span
+    if (t == 0) {
+        for (int sp = 0; sp < s && !sh[1]; ++sp) {
+            const unsigned* f = p.flags + (bh * p.spans + sp);
+            uint32_t n = 0;
+            while (ld_acquire(f) == 0u) {
+                if (++n > kSpinLimit) {
+                    fail(kErrLookback);
+                    break;
+                }
+                __nanosleep(256);
+            }
+        }
+    }
+    __syncthreads();
+    if (sh[1]) goto cleanup;
+    if (warp < D / 32) {
+        const int d = t;
+        const float* base = p.agg + static_cast<size_t>(bh) * p.spans * W;
+        for (int j0 = 0; j0 < M; j0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                v[i] = p.S_init ? p.S_init[(static_cast<size_t>(bh) * D + d) * M + j0 + i] : 0.f;
+            for (int sp = 0; sp < s; ++sp) {
+                const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W +
+                                                                  d * M + j0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = __ldcg(a + q);
+                    v[4 * q] += x.x;
+                    v[4 * q + 1] += x.y;
+                    v[4 * q + 2] += x.z;
+                    v[4 * q + 3] += x.w;
+                }
+            }
+            tmem_st16(tm + lane + Lay::T_S + j0, v);
+            uint4 lo = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                  pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+            uint4 hi = make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]),
+                                  pack_bf16(v[12], v[13]), pack_bf16(v[14], v[15]));
+            const int c = j0 >> 3;
+            *reinterpret_cast<uint4*>(sm + Lay::S + (c >> 3) * Lay::S_ATOM + swz(d, c & 7)) = lo;
+            *reinterpret_cast<uint4*>(sm + Lay::S + ((c + 1) >> 3) * Lay::S_ATOM +
+                                      swz(d, (c + 1) & 7)) = hi;
+        }
+        float z = p.Z_init ? p.Z_init[static_cast<size_t>(bh) * D + d] : 0.f;
+        for (int sp = 0; sp < s; ++sp) z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+        float zv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) zv[i] = z;
+        tmem_st16(tm + lane + Lay::T_S + M, zv);
+        const uint32_t zz = pack_bf16(z, z);
+        const uint4 z4 = make_uint4(zz, zz, zz, zz);
+        *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) = z4;
+        *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) = z4;
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ------------------------------------------------- phase 2: outputs
+    if (t == 0) load(n0, true);
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = n0 + c * L;
+        const int valid = min(L, n1 - c0);
+        wait_bar(tma_bar, tma_phase);
+        phi_tile<false>(sm + Lay::Q, DA, valid);
+        phi_tile<true>(sm + Lay::K, DA, valid);
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (sh[1]) goto cleanup;
+        if (t == 0) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kAtom + 32 * (k & 3);
+                mma_bf16(tm + Lay::T_P, sdesc(sQ + off, 16, 1024), sdesc(sK + off, 16, 1024), ID_P,
+                         k > 0 ? 1u : 0u);
+            }
+            mma_state_update(true);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0) tma_store_wait_read();  // the staging tile (P area) is free again
+        __syncthreads();
+        {   // P: mask j > i, round to bf16, store K-major into the P tile
+            const int i = t;
+            for (int j0 = 0; j0 < L; j0 += 32) {
+                uint32_t pk[16];
+                if (j0 > 32 * warp + 31) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) pk[q] = 0u;
+                } else {
+                    float v[32];
+                    tmem_ld32(tm + lane + Lay::T_P + j0, v);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int j = j0 + 2 * q;
+                        pk[q] = pack_bf16(j <= i ? v[2 * q] : 0.f, j + 1 <= i ? v[2 * q + 1] : 0.f);
+                    }
+                }
+                store_row32(sm + Lay::P, kAtom, i, j0, pk);
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (t == 0) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)  // O_ext = phi(Q) [S | Z]
+                mma_bf16(tm + Lay::T_O, sdesc(sQ + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
+                         sdesc(sS + 2048 * k, Lay::S_ATOM, 1024), ID_O, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)  // O_ext += P [V | 1]
+                mma_bf16(tm + Lay::T_O, sdesc(sP + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
+                         sdesc(sV + 2048 * k, kAtom, 1024), ID_O, 1u);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0 && c + 1 < nch) load(c0 + L, true);  // every input tile is consumed
+        if (warp < D / 32) {  // S_c -> bf16 copy for the next chunk's O_ext
+            const int d = t;
+            for (int j0 = 0; j0 < M; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
+                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, pk);
+            }
+            float z[16];
+            tmem_ld16(tm + lane + Lay::T_S + M, z);
+            uint32_t zk[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) zk[q] = pack_bf16(z[2 * q], z[2 * q + 1]);
+            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) =
+                make_uint4(zk[0], zk[1], zk[2], zk[3]);
+            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) =
+                make_uint4(zk[4], zk[5], zk[6], zk[7]);
+        }
+        {   // V' = O_ext[:, :M] / O_ext[:, M] -> bf16 staging tile (P area)
+            const int i = t;
+            float dv[16];
+            tmem_ld16(tm + lane + Lay::T_O + M, dv);
+            const float inv = 1.f / dv[0];
+            for (int j0 = 0; j0 < M; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_O + j0, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(v[2 * q] * inv, v[2 * q + 1] * inv);
+                store_row32(sm + Lay::P, kAtom, i, j0, pk);
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (t == 0) {
+            for (int a = 0; a < MA; ++a) tma_store_3d(&tmO, sm + Lay::P + a * kAtom, 64 * a, c0, bh);
+            tma_store_commit();
+        }
+    }
+
+    if (last && p.S_final && warp < D / 32) {
+        const int d = t;
+        float* so = p.S_final + (static_cast<size_t>(bh) * D + d) * M;
+        for (int j0 = 0; j0 < M; j0 += 32) {
+            float v[32];
+            tmem_ld32(tm + lane + Lay::T_S + j0, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(so + j0)[q] =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+        float z[16];
+        tmem_ld16(tm + lane + Lay::T_S + M, z);
+        p.Z_final[static_cast<size_t>(bh) * D + d] = z[0];
+    }
+
+cleanup:
+    if (t == 0) tma_store_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
+}
+
+// ------------------------------------------------------------------ host
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+    });
+    return fn;
+}
+
+// 3-D map over a [BH][N][C] bf16 tensor with a {64, 128, 1} box and the
+// 128-byte swizzle; rows past N read as zero and are not written.
+cudaError_t make_map(CUtensorMap* m, const void* base, int BH, int N, int C) {
+    EncodeTiled enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2, static_cast<cuuint64_t>(N) * C * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(L), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace tcf
+
+template <int D, int M>
+cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                              const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
+                              const float* S_init, const float* Z_init, float* S_final,
+                              float* Z_final) {
+    using namespace tcf;
+    using Lay = Layout<D, M>;
+    const int chunks = (N + L - 1) / L;
+    auto kern = causal_fwd_tc_kernel<D, M>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Lay::BYTES));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Lay::BYTES);
+    if (e != cudaSuccess) return e;
+    // one wave of (head, span) units: CTAs resident at once (at most two per SM, as TMEM allows)
+    const int slots = std::max(1, std::min(per_sm, Lay::CTAS_PER_SM)) * c.num_sms;
+    int spans = std::max(1, std::min(slots / std::max(BH, 1), chunks));
+    const int per = (chunks + spans - 1) / spans;
+    const int span_len = per * L;
+    spans = (N + span_len - 1) / span_len;
+    const int units = BH * spans;
+
+    const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * Lay::W;
+    const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
+    char* ws = nullptr;
+    e = scratch_alloc(c, reinterpret_cast<void**>(&ws), agg_bytes + flag_bytes + 256);
+    if (e != cudaSuccess) return e;
+    FwdParams p;
+    p.N = N;
+    p.spans = spans;
+    p.span_len = span_len;
+    p.agg = reinterpret_cast<float*>(ws);
+    p.flags = reinterpret_cast<unsigned*>(ws + agg_bytes);
+    p.ticket = p.flags + units;
+    p.S_init = S_init;
+    p.Z_init = Z_init;
+    p.S_final = S_final;
+    p.Z_final = Z_final;
+    p.status = c.status_word;
+    do {
+        if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
+        CUtensorMap mQ, mK, mV, mO;
+        if ((e = make_map(&mQ, Q, BH, N, D)) || (e = make_map(&mK, K, BH, N, D)) ||
+            (e = make_map(&mV, V, BH, N, M)) || (e = make_map(&mO, O, BH, N, M)))
+            break;
+        kern<<<units, kThreads, Lay::BYTES, c.stream>>>(mQ, mK, mV, mO, p);
+        note_launch();
+        e = cudaGetLastError();
+    } while (0);
+    scratch_free(c, ws);
+    return e;
+}
+
+template cudaError_t causal_forward_tc<64, 64>(const LaunchCtx&, const __nv_bfloat16*,
+                                               const __nv_bfloat16*, const __nv_bfloat16*,
+                                               __nv_bfloat16*, int, int, const float*, const float*,
+                                               float*, float*);
+template cudaError_t causal_forward_tc<128, 128>(const LaunchCtx&, const __nv_bfloat16*,
+                                                 const __nv_bfloat16*, const __nv_bfloat16*,
+                                                 __nv_bfloat16*, int, int, const float*,
+                                                 const float*, float*, float*);
+
+}  // namespace la

@@ -141,12 +141,31 @@ cudaError_t dispatch(la_dtype dt, int D, int M, A... a) {
     return cudaErrorInvalidValue;
 }
 
+// bf16 with D = M in {64, 128} runs on the tensor cores; every other shape
+// and fp32 storage runs the CUDA-core kernels.
+template <typename T, int D, int M>
+struct UseTensorCores {
+    static constexpr bool value = false;
+};
+template <>
+struct UseTensorCores<__nv_bfloat16, 64, 64> {
+    static constexpr bool value = true;
+};
+template <>
+struct UseTensorCores<__nv_bfloat16, 128, 128> {
+    static constexpr bool value = true;
+};
+
 struct FwdCausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
                            int BH, int N, const float* Si, const float* Zi, float* Sf, float* Zf) {
-        return causal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N, Si,
-                                       Zi, Sf, Zf);
+        if constexpr (UseTensorCores<T, D, M>::value)
+            return causal_forward_tc<D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N,
+                                           Si, Zi, Sf, Zf);
+        else
+            return causal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N,
+                                           Si, Zi, Sf, Zf);
     }
 };
 struct BwdCausal {

@@ -1,6 +1,7 @@
 // la_launch.h -- host-side launchers behind the C ABI (internal).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -30,6 +31,13 @@ template <typename T, int D, int M>
 cudaError_t causal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O, int BH,
                            int N, const float* S_init, const float* Z_init, float* S_final,
                            float* Z_final);
+
+// Tensor-core causal forward for bf16 storage with D = M in {64, 128}.
+template <int D, int M>
+cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                              const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
+                              const float* S_init, const float* Z_init, float* S_final,
+                              float* Z_final);
 
 template <typename T, int D, int M>
 cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,

@@ -67,6 +67,28 @@ def test_causal_forward_small(dt, shape):
     assert rel_err(Z, Rz) <= TOL[dt]
 
 
+@pytest.mark.parametrize("shape", [
+    (8, 64, 300, 64, 64),     # more heads than resident CTAs: several waves, one span per head
+    (1, 2, 5000, 128, 128),   # few heads: many spans per head, ragged last chunk
+    (1, 1, 128, 64, 64),      # exactly one chunk
+    (2, 3, 129, 64, 64),      # one full chunk and a single-token tail
+    (1, 4, 4096, 64, 64),
+])
+def test_causal_forward_bf16_span_shapes(shape):
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=13 + N)
+    g = _dev(x)
+    O, S, Z = la.la_forward_causal(g["Q"], g["K"], g["V"], return_state=True)
+    la.la_check_device_status()
+    idx = list(range(min(B * H, 6)))
+    hs = [x[n].reshape(B * H, N, -1)[idx] for n in ("Q", "K", "V")]
+    Ro, Rs, Rz = oracle.causal_forward_recurrent(*hs)
+    assert rel_err(O.reshape(B * H, N, M)[idx], Ro) <= TOL["bf16"]
+    assert rel_err(S.reshape(B * H, D, M)[idx], Rs) <= TOL["bf16"]
+    assert rel_err(Z.reshape(B * H, D)[idx], Rz) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_causal_forward_carried_state_and_empty(dt):
     la = _la()
