@@ -1,0 +1,731 @@
+// causal_bwd_tc.cu -- causal linear-attention backward on the 5th-generation
+// tensor core, bf16 storage with D = M = 64.
+//
+// With qf = phi(Q), kf = phi(K), den_i = qf_i.Z_i, the quotient rule gives
+//   gn_i = G_i / den_i,   gd_i = -(G_i . O_i) / den_i
+// and the numerator gradients of "Transformers are RNNs" section 三（一）4
+// (eqs. gq-gv: a prefix state for phi(Q), a suffix state for phi(K) and V)
+// become, per chunk c of L = 128 tokens with g = [gn | gd 0...0] (an M + 16
+// wide row, matching the ones block appended to V):
+//   dP     = tril(g [V | 1]^T)                 (= gn_i.V_j + gd_i for j <= i)
+//   dqf_c  = g [S | Z]_{c-1}^T + dP kf_c       (prefix state)
+//   dV_c   = P^T gn + kf_c R_{c+1}             (suffix state R = sum qf g^T)
+//   dkf_c  = dP^T qf_c + [V | 1] [R | r]_{c+1}^T
+// and dQ = dqf * phi'(Q), dK = dkf * phi'(K) with phi' = min(phi, 1).
+//
+// Two kernels, one CTA per (head, span):
+//   prefix kernel -- phase 1 / look-back exactly as the forward to get the
+//     span's starting S, Z; then per chunk: P and qf.Z by MMA, den, gn, gd
+//     (written to scratch), dP and dqf by MMA, dQ out, and the span's
+//     sum qf^T g (its share of R) published for the suffix kernel;
+//   suffix kernel -- starts from the sum of the later spans' shares (all
+//     complete, the prefix kernel has finished) and walks its chunks in
+//     reverse: P and dP again, dV and dkf by MMA, R += qf^T g.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "la_launch.h"
+#include "tc_common.cuh"
+
+namespace la {
+namespace tcb {
+
+using namespace la::tcf;
+
+constexpr int D = 64, M = 64;
+constexpr int NE = M + 16;
+constexpr int W = D * M + D;           // words of a published (S | Z) or (R | r) state
+constexpr uint32_t S_ATOM = D * 128;   // one atom column of a D-row state tile
+
+// prefix-kernel shared memory
+struct LayF {
+    static constexpr uint32_t Q = 0, K = kAtom, V = 2 * kAtom, ONES = 3 * kAtom;
+    static constexpr uint32_t G = 4 * kAtom, O = 5 * kAtom;
+    static constexpr uint32_t GH = 6 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
+    static constexpr uint32_t P = 8 * kAtom;     // dP (bf16), then the dQ staging tile
+    static constexpr uint32_t S = 10 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
+    static constexpr uint32_t BARS = S + 2 * S_ATOM;
+    static constexpr uint32_t BYTES = BARS + 64;
+    static constexpr uint32_t T_P = 0, T_DEN = 128, T_DQ = 160, T_S = 224, T_R = 304;
+    static constexpr uint32_t T_COLS = 512;
+};
+
+// suffix-kernel shared memory
+struct LayR {
+    static constexpr uint32_t Q = 0, K = kAtom, V = 2 * kAtom, ONES = 3 * kAtom;
+    static constexpr uint32_t GH = 4 * kAtom;
+    static constexpr uint32_t P = 6 * kAtom;     // P (bf16), then the dK staging tile
+    static constexpr uint32_t DP = 8 * kAtom;    // dP (bf16), then the dV staging tile
+    static constexpr uint32_t R = 10 * kAtom;    // [R | r 0..0] bf16, 2 atoms of D rows
+    static constexpr uint32_t BARS = R + 2 * S_ATOM;
+    static constexpr uint32_t BYTES = BARS + 64;
+    static constexpr uint32_t T_P = 0, T_DP = 128, T_DV = 256, T_DK = 320, T_R = 384;
+    static constexpr uint32_t T_COLS = 512;
+};
+
+struct BwdParams {
+    int N, spans, span_len;
+    float* sagg;          // [units][W] per-span (sum kf V^T | sum kf)
+    float* ragg;          // [units][W] per-span (sum qf gn^T | sum qf gd)
+    unsigned* flags;      // [units]
+    unsigned* ticket;
+    float* gd;            // [BH][N]
+    unsigned* status;
+};
+
+constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);     // K-major x K-major
+constexpr uint32_t ID_NE_MNMN = idesc_bf16(128, NE, true, true);  // state updates
+constexpr uint32_t ID_16_KMN = idesc_bf16(128, 16, false, true);  // qf . [Z block]
+constexpr uint32_t ID_D_KK = idesc_bf16(128, D, false, false);
+constexpr uint32_t ID_D_KMN = idesc_bf16(128, D, false, true);
+constexpr uint32_t ID_D_MNMN = idesc_bf16(128, D, true, true);
+constexpr uint32_t ID_M_MNMN = idesc_bf16(128, M, true, true);
+constexpr uint32_t ID_M_KMN = idesc_bf16(128, M, false, true);
+
+// K-major descriptor for K step k of a tile whose 64-column atoms are `atom` bytes apart.
+__device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t atom) {
+    return sdesc(base + (k >> 2) * atom + 32 * (k & 3), 16, 1024);
+}
+// MN-major descriptor for K step k (16 rows) of a tile whose atoms are `lbo` bytes apart.
+__device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t lbo) {
+    return sdesc(base + 2048 * k, lbo, 1024);
+}
+
+// Reads 64 bf16 values of `row` from a swizzled 128-row atom column into fp32.
+__device__ __forceinline__ void read_row64(const uint8_t* tile, int row, float (&v)[64]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + swz(row, c));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+            v[8 * c + 2 * q] = f.x;
+            v[8 * c + 2 * q + 1] = f.y;
+        }
+    }
+}
+
+// Masked (j <= i) rows of a 128 x 128 fp32 TMEM block -> bf16 K-major tile
+// (when STORE).  Returns the row sum of the masked fp32 values.
+template <bool STORE = true>
+__device__ __forceinline__ float masked_rows_to_tile(uint32_t taddr, uint8_t* tile, int i, int warp) {
+    float sum = 0.f;
+    for (int j0 = 0; j0 < L; j0 += 32) {
+        uint32_t pk[16];
+        if (j0 > 32 * warp + 31) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) pk[q] = 0u;
+        } else {
+            float v[32];
+            tmem_ld32(taddr + j0, v);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int j = j0 + 2 * q;
+                const float a = j <= i ? v[2 * q] : 0.f;
+                const float b = j + 1 <= i ? v[2 * q + 1] : 0.f;
+                sum += a + b;
+                pk[q] = pack_bf16(a, b);
+            }
+        }
+        if (STORE) store_row32(tile, kAtom, i, j0, pk);
+    }
+    return sum;
+}
+
+// TMEM row (64 columns, times phi'(x) = min(phi, 1) taken from `phi_tile` when
+// given) -> bf16 staging tile row.
+__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile, int row,
+                                                 const uint8_t* phi_tile) {
+    float f[64];
+    if (phi_tile) read_row64(phi_tile, row, f);
+    for (int j0 = 0; j0 < 64; j0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + j0, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            float a = v[2 * q], b = v[2 * q + 1];
+            if (phi_tile) {
+                a *= fminf(f[j0 + 2 * q], 1.f);
+                b *= fminf(f[j0 + 2 * q + 1], 1.f);
+            }
+            pk[q] = pack_bf16(a, b);
+        }
+        store_row32(tile, kAtom, row, j0, pk);
+    }
+}
+
+// TMEM state row d (M + 16 columns) -> bf16 state tile [D rows] (M columns and
+// the first 16 columns of the extension atom).
+__device__ __forceinline__ void state_row_to_tile(uint32_t taddr, uint8_t* tile, int d) {
+    for (int j0 = 0; j0 < M; j0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + j0, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
+        store_row32(tile, S_ATOM, d, j0, pk);
+    }
+    float z[16];
+    tmem_ld16(taddr + M, z);
+    uint32_t zk[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) zk[q] = pack_bf16(z[2 * q], z[2 * q + 1]);
+    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(zk[0], zk[1], zk[2], zk[3]);
+    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(zk[4], zk[5], zk[6], zk[7]);
+}
+
+// Writes a state row (M values, then `ext` in the first extension column and
+// `ext_rest` in the other 15) into TMEM and into the bf16 state tile.
+__device__ __forceinline__ void put_state_row(uint32_t taddr, uint8_t* tile, int d,
+                                              const float* row, float ext, float ext_rest) {
+    for (int j0 = 0; j0 < M; j0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = row[j0 + q];
+        tmem_st16(taddr + j0, v);
+        const int c = j0 >> 3;
+        *reinterpret_cast<uint4*>(tile + swz(d, c)) =
+            make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                       pack_bf16(v[6], v[7]));
+        *reinterpret_cast<uint4*>(tile + swz(d, c + 1)) =
+            make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
+                       pack_bf16(v[14], v[15]));
+    }
+    float e[16];
+    e[0] = ext;
+#pragma unroll
+    for (int q = 1; q < 16; ++q) e[q] = ext_rest;
+    tmem_st16(taddr + M, e);
+    const uint32_t e0 = pack_bf16(ext, ext_rest), er = pack_bf16(ext_rest, ext_rest);
+    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(e0, er, er, er);
+    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(er, er, er, er);
+}
+
+__device__ __forceinline__ void sync_tc() {
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+}
+
+// ------------------------------------------------------------ prefix kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmGn,
+                     const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
+    using Lay = LayF;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int t = threadIdx.x, warp = t >> 5;
+    if (smem_u32(sm) & 1023u) {
+        if (t == 0) atomicOr(p.status, kErrAlign);
+        return;
+    }
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+    uint64_t* mma_bar = tma_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
+    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    if (t == 0) {
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        fence_mbar_init();
+        sh[1] = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_relinquish();
+    }
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kThreads)
+        reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
+            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+    if (t == 0) sh[0] = static_cast<int>(atomicAdd(p.ticket, 1u));
+    __syncthreads();
+
+    const int unit = sh[0];
+    const int bh = unit / p.spans, s = unit - bh * p.spans;
+    const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
+    const int nch = (n1 - n0 + L - 1) / L;
+    const bool last = s == p.spans - 1;
+    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
+    const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
+    const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
+    uint32_t tma_phase = 0, mma_phase = 0;
+
+    auto fail = [&](unsigned code) {
+        atomicOr(p.status, code);
+        sh[1] = 1;
+    };
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
+        if (!mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        phase ^= 1u;
+    };
+    auto mma_state_update = [&](bool accumulate_first) {  // S_ext (+)= kf^T [V | 1]
+#pragma unroll
+        for (int k = 0; k < L / 16; ++k)
+            mma_bf16(tm + Lay::T_S, mnmaj(sK, k, kAtom), mnmaj(sV, k, kAtom), ID_NE_MNMN,
+                     (accumulate_first || k > 0) ? 1u : 0u);
+    };
+
+    // ---------------------------------------------- phase 1: span aggregate
+    if (!last) {
+        if (t == 0) {
+            mbar_arrive_expect_tx(tma_bar, 2 * kAtom);
+            tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, n0, bh);
+            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
+        }
+        for (int c = 0; c < nch; ++c) {
+            const int c0 = n0 + c * L;
+            wait_bar(tma_bar, tma_phase);
+            phi_tile<true>(sm + Lay::K, 1, min(L, n1 - c0));
+            sync_tc();
+            if (sh[1]) goto cleanup;
+            if (t == 0) {
+                mma_state_update(c > 0);
+                mma_commit(mma_bar);
+            }
+            wait_bar(mma_bar, mma_phase);
+            fence_after_sync();
+            if (t == 0 && c + 1 < nch) {
+                mbar_arrive_expect_tx(tma_bar, 2 * kAtom);
+                tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 + L, bh);
+                tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
+            }
+        }
+        if (warp < D / 32) {
+            float* out = p.sagg + static_cast<size_t>(unit) * W;
+            const int d = t;
+            for (int j0 = 0; j0 < M; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_S + j0, v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(out + d * M + j0)[q] =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            float z[16];
+            tmem_ld16(tm + lane + Lay::T_S + M, z);
+            out[D * M + d] = z[0];
+        }
+        __threadfence();
+        fence_before_sync();
+        __syncthreads();
+        if (t == 0) st_release(p.flags + unit, 1u);
+    }
+
+    // ------------------------------------------------------------ look-back
+    if (t == 0) {
+        for (int sp = 0; sp < s && !sh[1]; ++sp) {
+            const unsigned* f = p.flags + (bh * p.spans + sp);
+            uint32_t n = 0;
+            while (ld_acquire(f) == 0u) {
+                if (++n > kSpinLimit) {
+                    fail(kErrLookback);
+                    break;
+                }
+                __nanosleep(256);
+            }
+        }
+    }
+    __syncthreads();
+    if (sh[1]) goto cleanup;
+    if (warp < D / 32) {
+        const int d = t;
+        const float* base = p.sagg + static_cast<size_t>(bh) * p.spans * W;
+        float row[M];
+#pragma unroll
+        for (int e = 0; e < M; ++e) row[e] = 0.f;
+        float z = 0.f;
+        for (int sp = 0; sp < s; ++sp) {
+            const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W + d * M);
+#pragma unroll
+            for (int q = 0; q < M / 4; ++q) {
+                const float4 x = __ldcg(a + q);
+                row[4 * q] += x.x;
+                row[4 * q + 1] += x.y;
+                row[4 * q + 2] += x.z;
+                row[4 * q + 3] += x.w;
+            }
+            z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+        }
+        put_state_row(tm + lane + Lay::T_S, sm + Lay::S, d, row, z, z);
+    }
+    sync_tc();
+
+    // ------------------------------------------------- phase 2: dQ, gn, gd
+    if (t == 0) {
+        mbar_arrive_expect_tx(tma_bar, 5 * kAtom);
+        tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, n0, bh);
+        tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, n0, bh);
+        tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
+        tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, n0, bh);
+        tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, n0, bh);
+    }
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = n0 + c * L;
+        const int valid = min(L, n1 - c0);
+        wait_bar(tma_bar, tma_phase);
+        phi_tile<false>(sm + Lay::Q, 1, valid);
+        phi_tile<true>(sm + Lay::K, 1, valid);
+        sync_tc();
+        if (sh[1]) goto cleanup;
+        if (t == 0) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
+                mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
+                         ID_16_KMN, k > 0);
+            }
+            mma_state_update(true);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0) tma_store_wait_read();  // staging and g tiles are free again
+        __syncthreads();
+        {   // den, gn, gd -> g tile (bf16) and gd scratch
+            const int i = t;
+            const float rowsum = masked_rows_to_tile<false>(tm + lane + Lay::T_P, nullptr, i, warp);
+            float dz[16];
+            tmem_ld16(tm + lane + Lay::T_DEN, dz);
+            const float den = rowsum + dz[0];
+            float g[64], o[64];
+            read_row64(sm + Lay::G, i, g);
+            read_row64(sm + Lay::O, i, o);
+            float go = 0.f;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) go = fmaf(g[e], o[e], go);
+            const bool ok = i < valid;
+            const float inv = ok ? 1.f / den : 0.f;
+            const float gd = -go * inv;
+#pragma unroll
+            for (int j0 = 0; j0 < 64; j0 += 32) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    pk[q] = pack_bf16(g[j0 + 2 * q] * inv, g[j0 + 2 * q + 1] * inv);
+                store_row32(sm + Lay::GH, kAtom, i, j0, pk);
+            }
+            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 0)) =
+                make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 1)) = make_uint4(0u, 0u, 0u, 0u);
+            if (ok) p.gd[static_cast<size_t>(bh) * p.N + c0 + i] = gd;
+        }
+        sync_tc();
+        if (t == 0) {
+            tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
+            tma_store_commit();
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k) {
+                // dP = g [V | 1]^T  (the P block of TMEM is free again)
+                mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
+                // dqf = g [S | Z]^T
+                mma_bf16(tm + Lay::T_DQ, kmaj(sGh, k, kAtom), kmaj(sS, k, S_ATOM), ID_D_KK, k > 0);
+            }
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)  // span share of R: qf^T g
+                mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN,
+                         (c > 0 || k > 0) ? 1u : 0u);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        masked_rows_to_tile(tm + lane + Lay::T_P, sm + Lay::P, t, warp);  // dP, masked, bf16
+        sync_tc();
+        if (t == 0) {
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)  // dqf += dP kf
+                mma_bf16(tm + Lay::T_DQ, kmaj(sP, k, kAtom), mnmaj(sK, k, kAtom), ID_D_KMN, 1u);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0 && c + 1 < nch) {  // K, V, G, O are consumed; Q waits for dQ's phi'
+            mbar_arrive_expect_tx(tma_bar, 5 * kAtom);
+            tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 + L, bh);
+            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
+            tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
+            tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
+        }
+        if (warp < D / 32) state_row_to_tile(tm + lane + Lay::T_S, sm + Lay::S, t);  // S_c, Z_c
+        tmem_row_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, t, sm + Lay::Q);       // dQ
+        sync_tc();
+        if (t == 0) {
+            tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
+            tma_store_commit();
+            if (c + 1 < nch) tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0 + L, bh);
+        }
+    }
+    if (warp < D / 32) {  // publish the span's share of R
+        float* out = p.ragg + static_cast<size_t>(unit) * W;
+        const int d = t;
+        for (int j0 = 0; j0 < M; j0 += 32) {
+            float v[32];
+            tmem_ld32(tm + lane + Lay::T_R + j0, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(out + d * M + j0)[q] =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+        float r[16];
+        tmem_ld16(tm + lane + Lay::T_R + M, r);
+        out[D * M + d] = r[0];
+    }
+
+cleanup:
+    if (t == 0) tma_store_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
+}
+
+// ------------------------------------------------------------ suffix kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmGn,
+                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                     const BwdParams p) {
+    using Lay = LayR;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int t = threadIdx.x, warp = t >> 5;
+    if (smem_u32(sm) & 1023u) {
+        if (t == 0) atomicOr(p.status, kErrAlign);
+        return;
+    }
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+    uint64_t* mma_bar = tma_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
+    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    if (t == 0) {
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        fence_mbar_init();
+        sh[1] = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_relinquish();
+    }
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kThreads)
+        reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
+            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    const int unit = blockIdx.x;
+    const int bh = unit / p.spans, s = unit - bh * p.spans;
+    const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
+    const int nch = (n1 - n0 + L - 1) / L;
+    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
+    const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
+    const uint32_t sP = smem_u32(sm + Lay::P), sDP = smem_u32(sm + Lay::DP);
+    const uint32_t sR = smem_u32(sm + Lay::R);
+    uint32_t tma_phase = 0, mma_phase = 0;
+
+    auto fail = [&](unsigned code) {
+        atomicOr(p.status, code);
+        sh[1] = 1;
+    };
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
+        if (!mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        phase ^= 1u;
+    };
+
+    if (warp < D / 32) {  // R, r after this span: the later spans' shares, in span order
+        const int d = t;
+        const float* base = p.ragg + static_cast<size_t>(bh) * p.spans * W;
+        float row[M];
+#pragma unroll
+        for (int e = 0; e < M; ++e) row[e] = 0.f;
+        float r = 0.f;
+        for (int sp = s + 1; sp < p.spans; ++sp) {
+            const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W + d * M);
+#pragma unroll
+            for (int q = 0; q < M / 4; ++q) {
+                const float4 x = __ldcg(a + q);
+                row[4 * q] += x.x;
+                row[4 * q + 1] += x.y;
+                row[4 * q + 2] += x.z;
+                row[4 * q + 3] += x.w;
+            }
+            r += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+        }
+        put_state_row(tm + lane + Lay::T_R, sm + Lay::R, d, row, r, 0.f);
+    }
+    sync_tc();
+
+    if (t == 0) {
+        const int c0 = n0 + (nch - 1) * L;
+        mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
+        tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0, bh);
+        tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0, bh);
+        tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0, bh);
+        tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, c0, bh);
+    }
+    for (int c = nch - 1; c >= 0; --c) {
+        const int c0 = n0 + c * L;
+        const int valid = min(L, n1 - c0);
+        {   // gd into the extension atom of the g tile (zero for padding rows)
+            const int i = t;
+            const float gd = i < valid ? __ldcg(p.gd + static_cast<size_t>(bh) * p.N + c0 + i) : 0.f;
+            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 0)) =
+                make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 1)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        wait_bar(tma_bar, tma_phase);
+        phi_tile<false>(sm + Lay::Q, 1, valid);
+        phi_tile<true>(sm + Lay::K, 1, valid);
+        sync_tc();
+        if (sh[1]) goto cleanup;
+        if (t == 0) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)  // P = qf kf^T
+                mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
+                mma_bf16(tm + Lay::T_DP, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0) tma_store_wait_read();  // the staging tiles (P, dP areas) are free again
+        __syncthreads();
+        masked_rows_to_tile(tm + lane + Lay::T_P, sm + Lay::P, t, warp);
+        masked_rows_to_tile(tm + lane + Lay::T_DP, sm + Lay::DP, t, warp);
+        sync_tc();
+        if (t == 0) {
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)  // dV = P^T gn
+                mma_bf16(tm + Lay::T_DV, mnmaj(sP, k, kAtom), mnmaj(sGh, k, kAtom), ID_M_MNMN, k > 0);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)  // dV += kf R
+                mma_bf16(tm + Lay::T_DV, kmaj(sK, k, kAtom), mnmaj(sR, k, S_ATOM), ID_M_KMN, 1u);
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)  // dkf = dP^T qf
+                mma_bf16(tm + Lay::T_DK, mnmaj(sDP, k, kAtom), mnmaj(sQ, k, kAtom), ID_D_MNMN, k > 0);
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)  // dkf += [V | 1] [R | r]^T
+                mma_bf16(tm + Lay::T_DK, kmaj(sV, k, kAtom), kmaj(sR, k, S_ATOM), ID_D_KK, 1u);
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)  // R += qf^T g
+                mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN, 1u);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0 && c > 0) {  // Q, V, g are consumed; K waits for dK's phi'
+            const int cp = c0 - L;
+            mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
+            tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, cp, bh);
+            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, cp, bh);
+            tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, cp, bh);
+        }
+        if (warp < D / 32) state_row_to_tile(tm + lane + Lay::T_R, sm + Lay::R, t);  // R_c
+        tmem_row_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, t, sm + Lay::K);       // dK
+        tmem_row_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, t, nullptr);          // dV
+        sync_tc();
+        if (t == 0) {
+            tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
+            tma_store_3d(&tmdV, sm + Lay::DP, 0, c0, bh);
+            tma_store_commit();
+            if (c > 0) tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 - L, bh);
+        }
+    }
+
+cleanup:
+    if (t == 0) tma_store_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
+}
+
+}  // namespace tcb
+
+cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                 const __nv_bfloat16* V, const __nv_bfloat16* O,
+                                 const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
+                                 __nv_bfloat16* dV, int BH, int N) {
+    using namespace tcb;
+    auto kf = bwd_prefix_tc_kernel;
+    auto kr = bwd_suffix_tc_kernel;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, LayF::BYTES)) ||
+        (e = cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, LayR::BYTES)))
+        return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kThreads, LayF::BYTES)))
+        return e;
+    const int chunks = (N + L - 1) / L;
+    const int slots = std::max(1, per_sm) * c.num_sms;
+    int spans = std::max(1, std::min(slots / std::max(BH, 1), chunks));
+    const int per = (chunks + spans - 1) / spans;
+    const int span_len = per * L;
+    spans = (N + span_len - 1) / span_len;
+    const int units = BH * spans;
+
+    const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * W;
+    const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
+    const size_t gn_bytes = sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
+    const size_t gd_bytes = sizeof(float) * static_cast<size_t>(BH) * N;
+    const size_t o_bytes = O ? 0 : gn_bytes;
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gn_bytes) + up(gd_bytes) + up(o_bytes);
+    char* ws = nullptr;
+    if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), total)) != cudaSuccess) return e;
+    BwdParams p;
+    p.N = N;
+    p.spans = spans;
+    p.span_len = span_len;
+    char* q = ws;
+    p.sagg = reinterpret_cast<float*>(q);
+    q += up(agg_bytes);
+    p.ragg = reinterpret_cast<float*>(q);
+    q += up(agg_bytes);
+    p.flags = reinterpret_cast<unsigned*>(q);
+    p.ticket = p.flags + units;
+    q += up(flag_bytes);
+    __nv_bfloat16* gn = reinterpret_cast<__nv_bfloat16*>(q);
+    q += up(gn_bytes);
+    p.gd = reinterpret_cast<float*>(q);
+    q += up(gd_bytes);
+    __nv_bfloat16* Ow = O ? nullptr : reinterpret_cast<__nv_bfloat16*>(q);
+    p.status = c.status_word;
+    do {
+        if (!O) {  // the output is needed for gd: recompute it
+            if ((e = causal_forward_tc<64, 64>(c, Q, K, V, Ow, BH, N, nullptr, nullptr, nullptr,
+                                               nullptr)) != cudaSuccess)
+                break;
+            O = Ow;
+        }
+        if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
+        CUtensorMap mQ, mK, mV, mG, mO, mGn, mdQ, mdK, mdV;
+        if ((e = make_map(&mQ, Q, BH, N, D)) || (e = make_map(&mK, K, BH, N, D)) ||
+            (e = make_map(&mV, V, BH, N, M)) || (e = make_map(&mG, G, BH, N, M)) ||
+            (e = make_map(&mO, O, BH, N, M)) || (e = make_map(&mGn, gn, BH, N, M)) ||
+            (e = make_map(&mdQ, dQ, BH, N, D)) || (e = make_map(&mdK, dK, BH, N, D)) ||
+            (e = make_map(&mdV, dV, BH, N, M)))
+            break;
+        kf<<<units, kThreads, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mGn, mdQ, p);
+        kr<<<units, kThreads, LayR::BYTES, c.stream>>>(mQ, mK, mV, mGn, mdK, mdV, p);
+        note_launch(2);
+        e = cudaGetLastError();
+    } while (0);
+    scratch_free(c, ws);
+    return e;
+}
+
+}  // namespace la

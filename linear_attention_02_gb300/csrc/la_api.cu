@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "la_launch.h"
 #include "linattn.h"
@@ -172,8 +173,13 @@ struct BwdCausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V,
                            const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N) {
-        return causal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
+        if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 64 && M == 64)
+            return causal_backward_tc64(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
                                         (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
+        else
+            return causal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V,
+                                            (const T*)O, (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH,
+                                            N);
     }
 };
 struct FwdNoncausal {

@@ -39,6 +39,12 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
                               const float* S_init, const float* Z_init, float* S_final,
                               float* Z_final);
 
+// Tensor-core causal backward for bf16 storage with D = M = 64.
+cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                 const __nv_bfloat16* V, const __nv_bfloat16* O,
+                                 const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
+                                 __nv_bfloat16* dV, int BH, int N);
+
 template <typename T, int D, int M>
 cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,
                             const T* G, T* dQ, T* dK, T* dV, int BH, int N);

@@ -128,14 +128,37 @@ def test_causal_backward_small(dt, shape, pass_out):
     assert rel_err(dV, RdV) <= TOL[dt]
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [
+    (1, 2, 4096, 64, 64),     # few heads: several spans per head
+    (8, 40, 300, 64, 64),     # more heads than SMs: one span per head, ragged tail
+    (2, 3, 129, 64, 64),      # one chunk plus a single-token tail
+    (1, 1, 128, 64, 64),
+])
 @pytest.mark.parametrize("pass_out", [True, False])
-def test_causal_backward_single_token(dt, pass_out):
+def test_causal_backward_bf16_span_shapes(shape, pass_out):
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=23 + N, with_grad=True)
+    g = _dev(x)
+    O = la.la_forward_causal(g["Q"], g["K"], g["V"]) if pass_out else None
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O)
+    la.la_check_device_status()
+    idx = list(range(min(B * H, 6)))
+    hs = [x[n].reshape(B * H, N, -1)[idx] for n in ("Q", "K", "V", "G")]
+    RdQ, RdK, RdV = oracle.causal_backward_cumsum(*hs)
+    assert rel_err(dQ.reshape(B * H, N, D)[idx], RdQ) <= TOL["bf16"]
+    assert rel_err(dK.reshape(B * H, N, D)[idx], RdK) <= TOL["bf16"]
+    assert rel_err(dV.reshape(B * H, N, M)[idx], RdV) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dt,M", [("f32", 32), ("bf16", 32), ("bf16", 64)])
+@pytest.mark.parametrize("pass_out", [True, False])
+def test_causal_backward_single_token(dt, M, pass_out):
     # N = 1: O_1 = V_1 whatever Q and K are, so dQ = dK = 0 exactly and dV = G.
     # The max-normalised error is undefined for an all-zero reference, so dQ
     # and dK are bounded against the natural scale max|G| * max|V| instead.
     la = _la()
-    B, H, N, D, M = 2, 3, 1, 64, 32
+    B, H, N, D = 2, 3, 1, 64
     x = synth.qkv(B, H, N, D, M, dt, seed=3, with_grad=True)
     g = _dev(x)
     O = la.la_forward_causal(g["Q"], g["K"], g["V"]) if pass_out else None
