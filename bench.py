@@ -75,60 +75,95 @@ def _traffic(key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clocks and clock-event (throttle) reasons sampled during the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Polls NVML (read-only queries through ctypes) every 2 ms on the GPU the
+    process runs on, matched by PCI bus id; falls back to nvidia-smi at its
+    100 ms minimum interval when NVML cannot be loaded."""
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []  # (sm_mhz, max_mhz, reason_bits)
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return False
+        handle = ctypes.c_void_p()
+        bus = None
+        try:
+            pr = torch.cuda.get_device_properties(self.cuda_index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        except Exception:
+            bus = None
+        if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(handle)) != 0:
+            if lib.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(handle)) != 0:
+                return False
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._nvml, self._handle = lib, handle
+        return True
+
+    def _poll_nvml(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        cur, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(cur)) == 0 and
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0):
+                r = self._reasons_fn(h, ctypes.byref(rs))
+                self.samples.append((cur.value, mx.value, rs.value if r == 0 else 0))
+            time.sleep(0.002)
+
+    def _poll_smi(self):
+        cmd = ["nvidia-smi", "-i", str(self.cuda_index), "--query-gpu=clocks.sm,clocks.max.sm,"
+               "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"]
+        proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        while not self._stop.is_set():
+            line = proc.stdout.readline()
+            if not line:
+                break
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+            except (ValueError, IndexError):
+                pass
+        proc.terminate()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
+            use_nvml = self._open_nvml()
         except Exception:
-            self.proc = None
+            use_nvml = False
+        self._thread = threading.Thread(target=self._poll_nvml if use_nvml else self._poll_smi,
+                                        daemon=True)
+        self._thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        self._stop.set()
+        self._thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for _, _, bits in self.samples:
+            for b, name in self.REASONS.items():
+                if bits & b:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
+                "sm_max_mhz": max(x[1] for x in self.samples), "reasons": sorted(reasons),
+                "samples": len(self.samples)}
 
 
 # ------------------------------------------------------------- workloads
@@ -420,7 +455,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-paths", action="store_true", help="headline step only")

@@ -114,16 +114,17 @@ __device__ __forceinline__ void read_row64(const uint8_t* tile, int row, float (
 template <bool STORE = true>
 __device__ __forceinline__ float masked_rows_to_tile(uint32_t taddr, uint8_t* tile, int i, int warp) {
     float sum = 0.f;
-    for (int j0 = 0; j0 < L; j0 += 32) {
-        uint32_t pk[16];
+#pragma unroll
+    for (int j0 = 0; j0 < L; j0 += 64) {
+        uint32_t pk[32];
         if (j0 > 32 * warp + 31) {
 #pragma unroll
-            for (int q = 0; q < 16; ++q) pk[q] = 0u;
+            for (int q = 0; q < 32; ++q) pk[q] = 0u;
         } else {
-            float v[32];
-            tmem_ld32(taddr + j0, v);
+            float v[64];
+            tmem_ld64(taddr + j0, v);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
+            for (int q = 0; q < 32; ++q) {
                 const int j = j0 + 2 * q;
                 const float a = j <= i ? v[2 * q] : 0.f;
                 const float b = j + 1 <= i ? v[2 * q + 1] : 0.f;
@@ -131,7 +132,10 @@ __device__ __forceinline__ float masked_rows_to_tile(uint32_t taddr, uint8_t* ti
                 pk[q] = pack_bf16(a, b);
             }
         }
-        if (STORE) store_row32(tile, kAtom, i, j0, pk);
+        if (STORE) {
+            store_row32(tile, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+            store_row32(tile, kAtom, i, j0 + 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+        }
     }
     return sum;
 }
@@ -140,35 +144,32 @@ __device__ __forceinline__ float masked_rows_to_tile(uint32_t taddr, uint8_t* ti
 // given) -> bf16 staging tile row.
 __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile, int row,
                                                  const uint8_t* phi_tile) {
-    float f[64];
-    if (phi_tile) read_row64(phi_tile, row, f);
-    for (int j0 = 0; j0 < 64; j0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + j0, v);
-        uint32_t pk[16];
+    float v[64];
+    tmem_ld64(taddr, v);
+    if (phi_tile) {
+        float f[64];
+        read_row64(phi_tile, row, f);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            float a = v[2 * q], b = v[2 * q + 1];
-            if (phi_tile) {
-                a *= fminf(f[j0 + 2 * q], 1.f);
-                b *= fminf(f[j0 + 2 * q + 1], 1.f);
-            }
-            pk[q] = pack_bf16(a, b);
-        }
-        store_row32(tile, kAtom, row, j0, pk);
+        for (int j = 0; j < 64; ++j) v[j] *= fminf(f[j], 1.f);
     }
+    uint32_t pk[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
+    store_row32(tile, kAtom, row, 0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+    store_row32(tile, kAtom, row, 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
 }
 
 // TMEM state row d (M + 16 columns) -> bf16 state tile [D rows] (M columns and
 // the first 16 columns of the extension atom).
 __device__ __forceinline__ void state_row_to_tile(uint32_t taddr, uint8_t* tile, int d) {
-    for (int j0 = 0; j0 < M; j0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + j0, v);
-        uint32_t pk[16];
+    {
+        float v[64];
+        tmem_ld64(taddr, v);
+        uint32_t pk[32];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
-        store_row32(tile, S_ATOM, d, j0, pk);
+        for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
+        store_row32(tile, S_ATOM, d, 0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+        store_row32(tile, S_ATOM, d, 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
     }
     float z[16];
     tmem_ld16(taddr + M, z);
@@ -266,8 +267,12 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         atomicOr(p.status, code);
         sh[1] = 1;
     };
+    // One thread polls the barrier; the others wait at the CTA barrier, which
+    // wakes them as soon as it completes (a thread parked in try_wait can
+    // wake much later than the phase flips).
     auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
-        if (!mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        __syncthreads();
         phase ^= 1u;
     };
     auto mma_state_update = [&](bool accumulate_first) {  // S_ext (+)= kf^T [V | 1]
@@ -540,8 +545,12 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         atomicOr(p.status, code);
         sh[1] = 1;
     };
+    // One thread polls the barrier; the others wait at the CTA barrier, which
+    // wakes them as soon as it completes (a thread parked in try_wait can
+    // wake much later than the phase flips).
     auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
-        if (!mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        __syncthreads();
         phase ^= 1u;
     };
 
@@ -664,14 +673,18 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     auto kr = bwd_suffix_tc_kernel;
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, LayF::BYTES)) ||
-        (e = cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, LayR::BYTES)))
+        (e = cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, LayR::BYTES)) ||
+        (e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) ||
+        (e = cudaFuncSetAttribute(kr, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)))
         return e;
     int per_sm = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kThreads, LayF::BYTES)))
         return e;
     const int chunks = (N + L - 1) / L;
     const int slots = std::max(1, per_sm) * c.num_sms;
-    int spans = std::max(1, std::min(slots / std::max(BH, 1), chunks));
+    int spans = choose_spans(BH, chunks, slots, 12);
     const int per = (chunks + spans - 1) / spans;
     const int span_len = per * L;
     spans = (N + span_len - 1) / span_len;

@@ -137,8 +137,12 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         atomicOr(p.status, code);
         sh[1] = 1;
     };
+    // One thread polls the barrier; the others wait at the CTA barrier, which
+    // wakes them as soon as it completes (a thread parked in try_wait can
+    // wake much later than the phase flips).
     auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
-        if (!mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        __syncthreads();
         phase ^= 1u;
     };
     auto load = [&](int c0, bool with_q) {  // thread 0 only
@@ -289,21 +293,24 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncthreads();
         {   // P: mask j > i, round to bf16, store K-major into the P tile
             const int i = t;
-            for (int j0 = 0; j0 < L; j0 += 32) {
-                uint32_t pk[16];
+#pragma unroll
+            for (int j0 = 0; j0 < L; j0 += 64) {
+                uint32_t pk[32];
                 if (j0 > 32 * warp + 31) {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = 0u;
+                    for (int q = 0; q < 32; ++q) pk[q] = 0u;
                 } else {
-                    float v[32];
-                    tmem_ld32(tm + lane + Lay::T_P + j0, v);
+                    float v[64];
+                    tmem_ld64(tm + lane + Lay::T_P + j0, v);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                    for (int q = 0; q < 32; ++q) {
                         const int j = j0 + 2 * q;
                         pk[q] = pack_bf16(j <= i ? v[2 * q] : 0.f, j + 1 <= i ? v[2 * q + 1] : 0.f);
                     }
                 }
-                store_row32(sm + Lay::P, kAtom, i, j0, pk);
+                store_row32(sm + Lay::P, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+                store_row32(sm + Lay::P, kAtom, i, j0 + 32,
+                            *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
             }
         }
         fence_proxy_async();
@@ -326,13 +333,16 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (t == 0 && c + 1 < nch) load(c0 + L, true);  // every input tile is consumed
         if (warp < D / 32) {  // S_c -> bf16 copy for the next chunk's O_ext
             const int d = t;
-            for (int j0 = 0; j0 < M; j0 += 32) {
-                float v[32];
-                tmem_ld32(tm + lane + Lay::T_S + j0, v);
-                uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
-                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, pk);
+            for (int j0 = 0; j0 < M; j0 += 64) {
+                float v[64];
+                tmem_ld64(tm + lane + Lay::T_S + j0, v);
+                uint32_t pk[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
+                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0 + 32,
+                            *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
             }
             float z[16];
             tmem_ld16(tm + lane + Lay::T_S + M, z);
@@ -349,13 +359,16 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             float dv[16];
             tmem_ld16(tm + lane + Lay::T_O + M, dv);
             const float inv = 1.f / dv[0];
-            for (int j0 = 0; j0 < M; j0 += 32) {
-                float v[32];
-                tmem_ld32(tm + lane + Lay::T_O + j0, v);
-                uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(v[2 * q] * inv, v[2 * q + 1] * inv);
-                store_row32(sm + Lay::P, kAtom, i, j0, pk);
+            for (int j0 = 0; j0 < M; j0 += 64) {
+                float v[64];
+                tmem_ld64(tm + lane + Lay::T_O + j0, v);
+                uint32_t pk[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q] * inv, v[2 * q + 1] * inv);
+                store_row32(sm + Lay::P, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+                store_row32(sm + Lay::P, kAtom, i, j0 + 32,
+                            *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
             }
         }
         fence_proxy_async();
@@ -406,13 +419,16 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     auto kern = causal_fwd_tc_kernel<D, M>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Lay::BYTES));
+    if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Lay::BYTES);
     if (e != cudaSuccess) return e;
     // one wave of (head, span) units: CTAs resident at once (at most two per SM, as TMEM allows)
     const int slots = std::max(1, std::min(per_sm, Lay::CTAS_PER_SM)) * c.num_sms;
-    int spans = std::max(1, std::min(slots / std::max(BH, 1), chunks));
+    int spans = choose_spans(BH, chunks, slots, 12);
     const int per = (chunks + spans - 1) / spans;
     const int span_len = per * L;
     spans = (N + span_len - 1) / span_len;

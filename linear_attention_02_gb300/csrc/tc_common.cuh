@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -38,34 +39,54 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
-// phi on two packed bf16 values.  __expf (ex2.approx based) has a relative
-// error far below the 2^-9 rounding of the bf16 result.
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
-    float2 f = __bfloat1622float2(h);
-    f.x = f.x > 0.f ? f.x + 1.f : __expf(f.x);
-    f.y = f.y > 0.f ? f.y + 1.f : __expf(f.y);
-    return pack_bf16(f.x, f.y);
+// 2^x on the special-function unit (ex2.approx, flush-to-zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// phi in place over `atoms` swizzled atom columns; rows >= valid become 0 when
-// ZERO_TAIL (padding keys must not enter S or Z: phi(0) = 1).
-template <bool ZERO_TAIL>
+// phi(x) = elu(x) + 1 written without a branch: max(x, 0) + e^min(x, 0), with
+// e^u = 2^(u log2 e).  For x > 0 this is x + 1, for x <= 0 it is e^x.  The
+// approximate 2^u is far more accurate than the 2^-9 rounding of bf16.
+__device__ __forceinline__ float phi_fast(float x) {
+    return fmaxf(x, 0.f) + ex2_approx(fminf(x, 0.f) * 1.4426950408889634f);
+}
+
+// phi on two packed bf16 values (a bf16 is the high half of an fp32, so the
+// unpack is a shift and a mask).
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
+    return pack_bf16(phi_fast(__uint_as_float(w << 16)), phi_fast(__uint_as_float(w & 0xFFFF0000u)));
+}
+
+// phi in place over `atoms` swizzled atom columns (1024 16-byte chunks each);
+// rows >= valid become 0 when ZERO_TAIL (padding keys must not enter S or Z:
+// phi(0) = 1).  Each thread works on 8 independent chunks at a time so that
+// the loads, the exponentials and the stores of different chunks overlap.
+template <bool ZERO_TAIL, int NT = kThreads>
 __device__ __forceinline__ void phi_tile(uint8_t* tile, int atoms, int valid) {
+    constexpr int U = 1024 / NT < 8 ? 1024 / NT : 8;  // chunks per thread per batch
     const int n = atoms * 1024;
-    for (int ch = threadIdx.x; ch < n; ch += kThreads) {
-        uint4* ptr = reinterpret_cast<uint4*>(tile + static_cast<size_t>(ch) * 16);
-        const int row = (ch & 1023) >> 3;
-        if (ZERO_TAIL && row >= valid) {
-            *ptr = make_uint4(0u, 0u, 0u, 0u);
-            continue;
+    for (int base = threadIdx.x; base < n; base += NT * U) {
+        uint4 u[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            u[j] = *reinterpret_cast<const uint4*>(tile + static_cast<size_t>(base + j * NT) * 16);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int row = ((base + j * NT) & 1023) >> 3;
+            if (ZERO_TAIL && row >= valid) {
+                u[j] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                u[j].x = phi_bf16x2(u[j].x);
+                u[j].y = phi_bf16x2(u[j].y);
+                u[j].z = phi_bf16x2(u[j].z);
+                u[j].w = phi_bf16x2(u[j].w);
+            }
         }
-        uint4 u = *ptr;
-        u.x = phi_bf16x2(u.x);
-        u.y = phi_bf16x2(u.y);
-        u.z = phi_bf16x2(u.z);
-        u.w = phi_bf16x2(u.w);
-        *ptr = u;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            *reinterpret_cast<uint4*>(tile + static_cast<size_t>(base + j * NT) * 16) = u[j];
     }
 }
 
@@ -82,6 +103,26 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, uint32_t atom_bytes, 
 }
 
 // ------------------------------------------------------------------ host
+
+// Spans per head for a grid of (head, span) units over `slots` resident CTAs:
+// minimises waves x chunks-per-span, charging every span but the last for its
+// aggregate pass over K and V (about a third of a full chunk).
+inline int choose_spans(int BH, int chunks, int slots, int max_spans) {
+    int best = 1;
+    double best_cost = 1e300;
+    for (int s = 1; s <= std::min(chunks, max_spans); ++s) {
+        const int per = (chunks + s - 1) / s;
+        const int eff = (chunks + per - 1) / per;
+        const long units = static_cast<long>(BH) * eff;
+        const long waves = (units + slots - 1) / slots;
+        const double cost = static_cast<double>(waves) * per * (eff > 1 ? 1.35 : 1.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = eff;
+        }
+    }
+    return best;
+}
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
