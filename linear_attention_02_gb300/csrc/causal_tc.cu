@@ -46,6 +46,11 @@ struct Layout {
     static constexpr int MA = M / 64;  // atom columns of a V / output tile
     static constexpr int NE = M + 16;  // M values + 16 copies of the normaliser column
     static constexpr int W = D * M + D;  // words of a published (S | Z) state
+    // D = 64: one warpgroup and 112 KB, so two CTAs share an SM and overlap each
+    // other's waits; D = 128: one CTA per SM whose two warpgroups split the
+    // element-wise work by columns (both measured faster than the alternatives).
+    static constexpr int GROUPS = D == 64 ? 1 : 2;
+    static constexpr int THREADS = 128 * GROUPS;
     // shared memory (byte offsets from a 1024-aligned base)
     static constexpr uint32_t Q = 0;
     static constexpr uint32_t K = Q + DA * kAtom;
@@ -63,9 +68,14 @@ struct Layout {
     static constexpr uint32_t T_COLS = T_S + NE <= 256 ? 256 : 512;
     static constexpr uint32_t TX_QKV = (2 * DA + MA) * kAtom;
     static constexpr uint32_t TX_KV = (DA + MA) * kAtom;
-    static constexpr int CTAS_PER_SM = (T_COLS <= 256 && BYTES <= 115712) ? 2 : 1;
+    // CTAs that fit on one SM: 228 KB of shared memory (1 KB reserved per CTA)
+    // and 512 TMEM columns.
+    static constexpr int SMEM_FIT = static_cast<int>(233472u / (BYTES + 1024u));
+    static constexpr int TMEM_FIT = static_cast<int>(512u / T_COLS);
+    static constexpr int PER_SM = SMEM_FIT < TMEM_FIT ? SMEM_FIT : TMEM_FIT;
     static_assert(D == M && (D == 64 || D == 128), "tensor-core path covers D = M in {64, 128}");
     static_assert(BYTES <= 227 * 1024, "shared memory");
+    static_assert(PER_SM >= 1, "one CTA must fit");
 };
 
 struct FwdParams {
@@ -80,19 +90,30 @@ struct FwdParams {
     unsigned* status;      // device error word
 };
 
+// Stores 64 bf16 values (packed in pk[32]) of `row` from column j0 on.
+__device__ __forceinline__ void store_row64(uint8_t* tile, uint32_t atom_bytes, int row, int j0,
+                                            const uint32_t (&pk)[32]) {
+    store_row32(tile, atom_bytes, row, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+    store_row32(tile, atom_bytes, row, j0 + 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+}
+
 template <int D, int M>
-__global__ void __launch_bounds__(kThreads, Layout<D, M>::CTAS_PER_SM)
+__global__ void __launch_bounds__(Layout<D, M>::THREADS, Layout<D, M>::PER_SM)
 causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                      const FwdParams p) {
     using Lay = Layout<D, M>;
-    constexpr int DA = Lay::DA, MA = Lay::MA, NE = Lay::NE, W = Lay::W;
+    constexpr int DA = Lay::DA, MA = Lay::MA, NE = Lay::NE, W = Lay::W, NT = Lay::THREADS;
+    constexpr int HALF = M / Lay::GROUPS;   // columns of a state/output row per warpgroup
+    constexpr int PCOLS = L / Lay::GROUPS;  // columns of P per warpgroup
     constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);
     constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);
     constexpr uint32_t ID_O = idesc_bf16(128, NE, false, true);
 
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
+    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup
+    const int row = 32 * q + (t & 31);      // tile row / TMEM lane owned by this thread
     if (smem_u32(sm) & 1023u) {  // the swizzled layouts need a 1024-aligned base
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
@@ -112,7 +133,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tmem_alloc(tmem_slot, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += kThreads)  // bf16 1.0 everywhere
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += NT)  // bf16 1.0 everywhere
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_before_sync();
@@ -127,7 +148,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
     const bool last = s == p.spans - 1;
-    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V), sP = smem_u32(sm + Lay::P);
     const uint32_t sS = smem_u32(sm + Lay::S);
@@ -137,9 +158,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         atomicOr(p.status, code);
         sh[1] = 1;
     };
-    // One thread polls the barrier; the others wait at the CTA barrier, which
-    // wakes them as soon as it completes (a thread parked in try_wait can
-    // wake much later than the phase flips).
+    // One thread polls the barrier; the others wait at the CTA barrier.
     auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
         if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
         __syncthreads();
@@ -167,7 +186,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int c = 0; c < nch; ++c) {
             const int c0 = n0 + c * L;
             wait_bar(tma_bar, tma_phase);
-            phi_tile<true>(sm + Lay::K, DA, min(L, n1 - c0));
+            phi_tile<true, NT>(sm + Lay::K, DA, min(L, n1 - c0));
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
@@ -181,20 +200,22 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             fence_after_sync();
             if (t == 0 && c + 1 < nch) load(c0 + L, false);
         }
-        if (warp < D / 32) {  // rows d < D of S_ext
+        if (q < D / 32) {  // rows d < D of S_ext, this warpgroup's columns
             float* out = p.agg + static_cast<size_t>(unit) * W;
-            const int d = t;
-            for (int j0 = 0; j0 < M; j0 += 32) {
+            const int d = row;
+            for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                 float v[32];
                 tmem_ld32(tm + lane + Lay::T_S + j0, v);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4*>(out + d * M + j0)[q] =
-                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                for (int u = 0; u < 8; ++u)
+                    reinterpret_cast<float4*>(out + d * M + j0)[u] =
+                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
             }
-            float z[16];
-            tmem_ld16(tm + lane + Lay::T_S + M, z);
-            out[D * M + d] = z[0];
+            if (g == 0) {
+                float z[16];
+                tmem_ld16(tm + lane + Lay::T_S + M, z);
+                out[D * M + d] = z[0];
+            }
         }
         __threadfence();
         fence_before_sync();
@@ -218,10 +239,10 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     __syncthreads();
     if (sh[1]) goto cleanup;
-    if (warp < D / 32) {
-        const int d = t;
+    if (q < D / 32) {
+        const int d = row;
         const float* base = p.agg + static_cast<size_t>(bh) * p.spans * W;
-        for (int j0 = 0; j0 < M; j0 += 16) {
+        for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 16) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -230,34 +251,36 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W +
                                                                   d * M + j0);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 x = __ldcg(a + q);
-                    v[4 * q] += x.x;
-                    v[4 * q + 1] += x.y;
-                    v[4 * q + 2] += x.z;
-                    v[4 * q + 3] += x.w;
+                for (int u = 0; u < 4; ++u) {
+                    const float4 x = __ldcg(a + u);
+                    v[4 * u] += x.x;
+                    v[4 * u + 1] += x.y;
+                    v[4 * u + 2] += x.z;
+                    v[4 * u + 3] += x.w;
                 }
             }
             tmem_st16(tm + lane + Lay::T_S + j0, v);
-            uint4 lo = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
-                                  pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
-            uint4 hi = make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]),
-                                  pack_bf16(v[12], v[13]), pack_bf16(v[14], v[15]));
-            const int c = j0 >> 3;
-            *reinterpret_cast<uint4*>(sm + Lay::S + (c >> 3) * Lay::S_ATOM + swz(d, c & 7)) = lo;
-            *reinterpret_cast<uint4*>(sm + Lay::S + ((c + 1) >> 3) * Lay::S_ATOM +
-                                      swz(d, (c + 1) & 7)) = hi;
+            const int cc = j0 >> 3;
+            *reinterpret_cast<uint4*>(sm + Lay::S + (cc >> 3) * Lay::S_ATOM + swz(d, cc & 7)) =
+                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                           pack_bf16(v[6], v[7]));
+            *reinterpret_cast<uint4*>(sm + Lay::S + ((cc + 1) >> 3) * Lay::S_ATOM +
+                                      swz(d, (cc + 1) & 7)) =
+                make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
+                           pack_bf16(v[14], v[15]));
         }
-        float z = p.Z_init ? p.Z_init[static_cast<size_t>(bh) * D + d] : 0.f;
-        for (int sp = 0; sp < s; ++sp) z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
-        float zv[16];
+        if (g == 0) {
+            float z = p.Z_init ? p.Z_init[static_cast<size_t>(bh) * D + d] : 0.f;
+            for (int sp = 0; sp < s; ++sp) z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+            float zv[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) zv[i] = z;
-        tmem_st16(tm + lane + Lay::T_S + M, zv);
-        const uint32_t zz = pack_bf16(z, z);
-        const uint4 z4 = make_uint4(zz, zz, zz, zz);
-        *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) = z4;
-        *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) = z4;
+            for (int i = 0; i < 16; ++i) zv[i] = z;
+            tmem_st16(tm + lane + Lay::T_S + M, zv);
+            const uint32_t zz = pack_bf16(z, z);
+            const uint4 z4 = make_uint4(zz, zz, zz, zz);
+            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) = z4;
+            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) = z4;
+        }
     }
     fence_proxy_async();
     fence_before_sync();
@@ -270,8 +293,8 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
         wait_bar(tma_bar, tma_phase);
-        phi_tile<false>(sm + Lay::Q, DA, valid);
-        phi_tile<true>(sm + Lay::K, DA, valid);
+        phi_tile<false, NT>(sm + Lay::Q, DA, valid);
+        phi_tile<true, NT>(sm + Lay::K, DA, valid);
         fence_proxy_async();
         fence_before_sync();
         __syncthreads();
@@ -286,31 +309,28 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             mma_state_update(true);
             mma_commit(mma_bar);
+            tma_store_wait_read();  // the staging tile (P area) is free again
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0) tma_store_wait_read();  // the staging tile (P area) is free again
-        __syncthreads();
         {   // P: mask j > i, round to bf16, store K-major into the P tile
-            const int i = t;
 #pragma unroll
-            for (int j0 = 0; j0 < L; j0 += 64) {
+            for (int jb = 0; jb < PCOLS / 64; ++jb) {
+                const int j0 = g * PCOLS + jb * 64;
                 uint32_t pk[32];
-                if (j0 > 32 * warp + 31) {
+                if (j0 > 32 * q + 31) {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) pk[q] = 0u;
+                    for (int u = 0; u < 32; ++u) pk[u] = 0u;
                 } else {
                     float v[64];
                     tmem_ld64(tm + lane + Lay::T_P + j0, v);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int j = j0 + 2 * q;
-                        pk[q] = pack_bf16(j <= i ? v[2 * q] : 0.f, j + 1 <= i ? v[2 * q + 1] : 0.f);
+                    for (int u = 0; u < 32; ++u) {
+                        const int j = j0 + 2 * u;
+                        pk[u] = pack_bf16(j <= row ? v[2 * u] : 0.f, j + 1 <= row ? v[2 * u + 1] : 0.f);
                     }
                 }
-                store_row32(sm + Lay::P, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-                store_row32(sm + Lay::P, kAtom, i, j0 + 32,
-                            *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+                store_row64(sm + Lay::P, kAtom, row, j0, pk);
             }
         }
         fence_proxy_async();
@@ -331,44 +351,39 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
         if (t == 0 && c + 1 < nch) load(c0 + L, true);  // every input tile is consumed
-        if (warp < D / 32) {  // S_c -> bf16 copy for the next chunk's O_ext
-            const int d = t;
+        if (q < D / 32) {  // S_c -> bf16 copy for the next chunk's O_ext
+            const int d = row;
+            for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                uint32_t pk[16];
 #pragma unroll
-            for (int j0 = 0; j0 < M; j0 += 64) {
-                float v[64];
-                tmem_ld64(tm + lane + Lay::T_S + j0, v);
-                uint32_t pk[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
-                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0 + 32,
-                            *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+                for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, pk);
             }
-            float z[16];
-            tmem_ld16(tm + lane + Lay::T_S + M, z);
-            uint32_t zk[8];
+            if (g == 0) {
+                float z[16];
+                tmem_ld16(tm + lane + Lay::T_S + M, z);
+                uint32_t zk[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) zk[q] = pack_bf16(z[2 * q], z[2 * q + 1]);
-            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) =
-                make_uint4(zk[0], zk[1], zk[2], zk[3]);
-            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) =
-                make_uint4(zk[4], zk[5], zk[6], zk[7]);
+                for (int u = 0; u < 8; ++u) zk[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
+                *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) =
+                    make_uint4(zk[0], zk[1], zk[2], zk[3]);
+                *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) =
+                    make_uint4(zk[4], zk[5], zk[6], zk[7]);
+            }
         }
         {   // V' = O_ext[:, :M] / O_ext[:, M] -> bf16 staging tile (P area)
-            const int i = t;
             float dv[16];
             tmem_ld16(tm + lane + Lay::T_O + M, dv);
             const float inv = 1.f / dv[0];
+            for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_O + j0, v);
+                uint32_t pk[16];
 #pragma unroll
-            for (int j0 = 0; j0 < M; j0 += 64) {
-                float v[64];
-                tmem_ld64(tm + lane + Lay::T_O + j0, v);
-                uint32_t pk[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q] * inv, v[2 * q + 1] * inv);
-                store_row32(sm + Lay::P, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-                store_row32(sm + Lay::P, kAtom, i, j0 + 32,
-                            *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+                for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u] * inv, v[2 * u + 1] * inv);
+                store_row32(sm + Lay::P, kAtom, row, j0, pk);
             }
         }
         fence_proxy_async();
@@ -381,20 +396,22 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
     }
 
-    if (last && p.S_final && warp < D / 32) {
-        const int d = t;
+    if (last && p.S_final && q < D / 32) {
+        const int d = row;
         float* so = p.S_final + (static_cast<size_t>(bh) * D + d) * M;
-        for (int j0 = 0; j0 < M; j0 += 32) {
+        for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
             float v[32];
             tmem_ld32(tm + lane + Lay::T_S + j0, v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                reinterpret_cast<float4*>(so + j0)[q] =
-                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int u = 0; u < 8; ++u)
+                reinterpret_cast<float4*>(so + j0)[u] =
+                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         }
-        float z[16];
-        tmem_ld16(tm + lane + Lay::T_S + M, z);
-        p.Z_final[static_cast<size_t>(bh) * D + d] = z[0];
+        if (g == 0) {
+            float z[16];
+            tmem_ld16(tm + lane + Lay::T_S + M, z);
+            p.Z_final[static_cast<size_t>(bh) * D + d] = z[0];
+        }
     }
 
 cleanup:
@@ -403,8 +420,6 @@ cleanup:
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
 }
-
-// ------------------------------------------------------------------ host
 
 }  // namespace tcf
 
@@ -424,10 +439,13 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
                                  cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Lay::BYTES);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Lay::THREADS, Lay::BYTES);
     if (e != cudaSuccess) return e;
-    // one wave of (head, span) units: CTAs resident at once (at most two per SM, as TMEM allows)
-    const int slots = std::max(1, std::min(per_sm, Lay::CTAS_PER_SM)) * c.num_sms;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    // The occupancy query does not see the carve-out the driver picks at launch
+    // and can report one CTA where two fit: take the larger of it and the fit
+    // computed from shared memory and TMEM.
+    const int slots = std::max(per_sm, Lay::PER_SM) * c.num_sms;  // CTAs resident at once
     int spans = choose_spans(BH, chunks, slots, 12);
     const int per = (chunks + spans - 1) / spans;
     const int span_len = per * L;
@@ -457,7 +475,7 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
         if ((e = make_map(&mQ, Q, BH, N, D)) || (e = make_map(&mK, K, BH, N, D)) ||
             (e = make_map(&mV, V, BH, N, M)) || (e = make_map(&mO, O, BH, N, M)))
             break;
-        kern<<<units, kThreads, Lay::BYTES, c.stream>>>(mQ, mK, mV, mO, p);
+        kern<<<units, Lay::THREADS, Lay::BYTES, c.stream>>>(mQ, mK, mV, mO, p);
         note_launch();
         e = cudaGetLastError();
     } while (0);
