@@ -47,11 +47,15 @@ struct LayF {
     static constexpr uint32_t GH = 6 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
     static constexpr uint32_t P = 8 * kAtom;     // dP (bf16), then the dQ staging tile
     static constexpr uint32_t S = 10 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
-    static constexpr uint32_t BARS = S + 2 * S_ATOM;
+    static constexpr uint32_t XCH = S + 2 * S_ATOM;  // 2 x [2][128] fp32 partial row sums
+    static constexpr uint32_t BARS = XCH + 2048;
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_P = 0, T_DEN = 128, T_DQ = 160, T_S = 224, T_R = 304;
     static constexpr uint32_t T_COLS = 512;
 };
+
+constexpr int kBT = 256;  // two warpgroups: warp w reads TMEM lanes 32 (w % 4) ..., and the
+                          // two warps of a lane quarter split the columns of every row
 
 // suffix-kernel shared memory
 struct LayR {
@@ -94,102 +98,101 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t lbo) {
     return sdesc(base + 2048 * k, lbo, 1024);
 }
 
-// Reads 64 bf16 values of `row` from a swizzled 128-row atom column into fp32.
-__device__ __forceinline__ void read_row64(const uint8_t* tile, int row, float (&v)[64]) {
+// Reads 32 bf16 values of `row` (16-byte chunks c0 .. c0 + 3) of a swizzled
+// 128-row atom column into fp32 (a bf16 is the high half of an fp32).
+__device__ __forceinline__ void read_row32(const uint8_t* tile, int row, int c0, float (&v)[32]) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4*>(tile + swz(row, c));
+    for (int c = 0; c < 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + swz(row, c0 + c));
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-            v[8 * c + 2 * q] = f.x;
-            v[8 * c + 2 * q + 1] = f.y;
+        for (int k = 0; k < 4; ++k) {
+            v[8 * c + 2 * k] = __uint_as_float(w[k] << 16);
+            v[8 * c + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
         }
     }
 }
 
-// Masked (j <= i) rows of a 128 x 128 fp32 TMEM block -> bf16 K-major tile
-// (when STORE).  Returns the row sum of the masked fp32 values.
-template <bool STORE = true>
-__device__ __forceinline__ float masked_rows_to_tile(uint32_t taddr, uint8_t* tile, int i, int warp) {
+// This warpgroup's 64 columns [64 g, 64 g + 64) of row i of a 128 x 128 fp32
+// TMEM block, masked to j <= i and rounded to bf16 into a K-major tile (when
+// STORE).  Returns the sum of the masked fp32 values.
+template <bool STORE>
+__device__ __forceinline__ float masked_half(uint32_t taddr, uint8_t* tile, int i, int q, int g) {
+    const int j0 = 64 * g;
+    uint32_t pk[32];
     float sum = 0.f;
+    if (j0 > 32 * q + 31) {
 #pragma unroll
-    for (int j0 = 0; j0 < L; j0 += 64) {
-        uint32_t pk[32];
-        if (j0 > 32 * warp + 31) {
+        for (int u = 0; u < 32; ++u) pk[u] = 0u;
+    } else {
+        float v[64];
+        tmem_ld64(taddr + j0, v);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) pk[q] = 0u;
-        } else {
-            float v[64];
-            tmem_ld64(taddr + j0, v);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int j = j0 + 2 * q;
-                const float a = j <= i ? v[2 * q] : 0.f;
-                const float b = j + 1 <= i ? v[2 * q + 1] : 0.f;
-                sum += a + b;
-                pk[q] = pack_bf16(a, b);
-            }
+        for (int u = 0; u < 32; ++u) {
+            const int j = j0 + 2 * u;
+            const float a = j <= i ? v[2 * u] : 0.f;
+            const float b = j + 1 <= i ? v[2 * u + 1] : 0.f;
+            sum += a + b;
+            pk[u] = pack_bf16(a, b);
         }
-        if (STORE) {
-            store_row32(tile, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-            store_row32(tile, kAtom, i, j0 + 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
-        }
+    }
+    if (STORE) {
+        store_row32(tile, kAtom, i, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+        store_row32(tile, kAtom, i, j0 + 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
     }
     return sum;
 }
 
-// TMEM row (64 columns, times phi'(x) = min(phi, 1) taken from `phi_tile` when
-// given) -> bf16 staging tile row.
-__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile, int row,
-                                                 const uint8_t* phi_tile) {
-    float v[64];
-    tmem_ld64(taddr, v);
+// This warpgroup's 32 columns of a 64-column TMEM row -> bf16 tile row, times
+// phi'(x) = min(phi, 1) taken from `phi_tile` when given.
+__device__ __forceinline__ void tmem_half_to_tile(uint32_t taddr, uint8_t* tile, int row, int g,
+                                                  const uint8_t* phi_tile) {
+    float v[32];
+    tmem_ld32(taddr + 32 * g, v);
     if (phi_tile) {
-        float f[64];
-        read_row64(phi_tile, row, f);
+        float f[32];
+        read_row32(phi_tile, row, 4 * g, f);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] *= fminf(f[j], 1.f);
+        for (int j = 0; j < 32; ++j) v[j] *= fminf(f[j], 1.f);
     }
-    uint32_t pk[32];
+    uint32_t pk[16];
 #pragma unroll
-    for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
-    store_row32(tile, kAtom, row, 0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-    store_row32(tile, kAtom, row, 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+    for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+    store_row32(tile, kAtom, row, 32 * g, pk);
 }
 
-// TMEM state row d (M + 16 columns) -> bf16 state tile [D rows] (M columns and
-// the first 16 columns of the extension atom).
-__device__ __forceinline__ void state_row_to_tile(uint32_t taddr, uint8_t* tile, int d) {
-    {
-        float v[64];
-        tmem_ld64(taddr, v);
-        uint32_t pk[32];
+// State row d: this warpgroup's 32 of the M columns (and, for g == 0, the 16
+// extension columns) from TMEM -> bf16 state tile [D rows].
+__device__ __forceinline__ void state_half_to_tile(uint32_t taddr, uint8_t* tile, int d, int g) {
+    float v[32];
+    tmem_ld32(taddr + 32 * g, v);
+    uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) pk[q] = pack_bf16(v[2 * q], v[2 * q + 1]);
-        store_row32(tile, S_ATOM, d, 0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-        store_row32(tile, S_ATOM, d, 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+    for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+    store_row32(tile, S_ATOM, d, 32 * g, pk);
+    if (g == 0) {
+        float z[16];
+        tmem_ld16(taddr + M, z);
+        uint32_t zk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) zk[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
+        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(zk[0], zk[1], zk[2], zk[3]);
+        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(zk[4], zk[5], zk[6], zk[7]);
     }
-    float z[16];
-    tmem_ld16(taddr + M, z);
-    uint32_t zk[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) zk[q] = pack_bf16(z[2 * q], z[2 * q + 1]);
-    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(zk[0], zk[1], zk[2], zk[3]);
-    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(zk[4], zk[5], zk[6], zk[7]);
 }
 
-// Writes a state row (M values, then `ext` in the first extension column and
-// `ext_rest` in the other 15) into TMEM and into the bf16 state tile.
-__device__ __forceinline__ void put_state_row(uint32_t taddr, uint8_t* tile, int d,
-                                              const float* row, float ext, float ext_rest) {
-    for (int j0 = 0; j0 < M; j0 += 16) {
+// Writes this warpgroup's 32 values of a state row into TMEM and the bf16
+// state tile; g == 0 also writes the extension columns (`ext`, then
+// `ext_rest` fifteen times).
+__device__ __forceinline__ void put_state_half(uint32_t taddr, uint8_t* tile, int d, int g,
+                                               const float (&vals)[32], float ext, float ext_rest) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
         float v[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) v[q] = row[j0 + q];
-        tmem_st16(taddr + j0, v);
-        const int c = j0 >> 3;
+        for (int u = 0; u < 16; ++u) v[u] = vals[16 * h + u];
+        tmem_st16(taddr + 32 * g + 16 * h, v);
+        const int c = 4 * g + 2 * h;
         *reinterpret_cast<uint4*>(tile + swz(d, c)) =
             make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                        pack_bf16(v[6], v[7]));
@@ -197,14 +200,55 @@ __device__ __forceinline__ void put_state_row(uint32_t taddr, uint8_t* tile, int
             make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
                        pack_bf16(v[14], v[15]));
     }
-    float e[16];
-    e[0] = ext;
+    if (g == 0) {
+        float e[16];
+        e[0] = ext;
 #pragma unroll
-    for (int q = 1; q < 16; ++q) e[q] = ext_rest;
-    tmem_st16(taddr + M, e);
-    const uint32_t e0 = pack_bf16(ext, ext_rest), er = pack_bf16(ext_rest, ext_rest);
-    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(e0, er, er, er);
-    *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(er, er, er, er);
+        for (int u = 1; u < 16; ++u) e[u] = ext_rest;
+        tmem_st16(taddr + M, e);
+        const uint32_t e0 = pack_bf16(ext, ext_rest), er = pack_bf16(ext_rest, ext_rest);
+        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(e0, er, er, er);
+        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(er, er, er, er);
+    }
+}
+
+// Sum of the published [D*M | D] states sp0 <= sp < sp1 of a head: this
+// warpgroup's 32 columns of row d into `row`; returns the summed extension
+// word (meaningful for g == 0).
+__device__ __forceinline__ float sum_states(const float* base, int sp0, int sp1, int d, int g,
+                                            float (&row)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) row[e] = 0.f;
+    float x0 = 0.f;
+    for (int sp = sp0; sp < sp1; ++sp) {
+        const float4* a =
+            reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W + d * M + 32 * g);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float4 x = __ldcg(a + u);
+            row[4 * u] += x.x;
+            row[4 * u + 1] += x.y;
+            row[4 * u + 2] += x.z;
+            row[4 * u + 3] += x.w;
+        }
+        if (g == 0) x0 += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+    }
+    return x0;
+}
+
+// Publishes this warpgroup's part of TMEM state row d as fp32 [D*M | D].
+__device__ __forceinline__ void publish_half(uint32_t taddr, float* out, int d, int g) {
+    float v[32];
+    tmem_ld32(taddr + 32 * g, v);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        reinterpret_cast<float4*>(out + d * M + 32 * g)[u] =
+            make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    if (g == 0) {
+        float z[16];
+        tmem_ld16(taddr + M, z);
+        out[D * M + d] = z[0];
+    }
 }
 
 __device__ __forceinline__ void sync_tc() {
@@ -216,7 +260,7 @@ __device__ __forceinline__ void sync_tc() {
 
 // ------------------------------------------------------------ prefix kernel
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBT, 1)
 bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmGn,
@@ -224,6 +268,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     using Lay = LayF;
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
+    const int q = warp & 3, g = warp >> 2, row = 32 * q + (t & 31);
     if (smem_u32(sm) & 1023u) {
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
@@ -232,6 +277,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     uint64_t* mma_bar = tma_bar + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
     volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    float* xch = reinterpret_cast<float*>(sm + Lay::XCH);  // [2 sums][2 warpgroups][128 rows]
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
@@ -242,7 +288,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tmem_alloc(tmem_slot, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += kThreads)
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kBT)
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_before_sync();
@@ -257,7 +303,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
     const bool last = s == p.spans - 1;
-    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
@@ -267,9 +313,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         atomicOr(p.status, code);
         sh[1] = 1;
     };
-    // One thread polls the barrier; the others wait at the CTA barrier, which
-    // wakes them as soon as it completes (a thread parked in try_wait can
-    // wake much later than the phase flips).
+    // One thread polls the barrier; the others wait at the CTA barrier.
     auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
         if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
         __syncthreads();
@@ -292,7 +336,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int c = 0; c < nch; ++c) {
             const int c0 = n0 + c * L;
             wait_bar(tma_bar, tma_phase);
-            phi_tile<true>(sm + Lay::K, 1, min(L, n1 - c0));
+            phi_tile<true, kBT>(sm + Lay::K, 1, min(L, n1 - c0));
             sync_tc();
             if (sh[1]) goto cleanup;
             if (t == 0) {
@@ -307,21 +351,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
             }
         }
-        if (warp < D / 32) {
-            float* out = p.sagg + static_cast<size_t>(unit) * W;
-            const int d = t;
-            for (int j0 = 0; j0 < M; j0 += 32) {
-                float v[32];
-                tmem_ld32(tm + lane + Lay::T_S + j0, v);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4*>(out + d * M + j0)[q] =
-                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
-            float z[16];
-            tmem_ld16(tm + lane + Lay::T_S + M, z);
-            out[D * M + d] = z[0];
-        }
+        if (q < D / 32) publish_half(tm + lane + Lay::T_S, p.sagg + static_cast<size_t>(unit) * W, row, g);
         __threadfence();
         fence_before_sync();
         __syncthreads();
@@ -344,26 +374,10 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     __syncthreads();
     if (sh[1]) goto cleanup;
-    if (warp < D / 32) {
-        const int d = t;
-        const float* base = p.sagg + static_cast<size_t>(bh) * p.spans * W;
-        float row[M];
-#pragma unroll
-        for (int e = 0; e < M; ++e) row[e] = 0.f;
-        float z = 0.f;
-        for (int sp = 0; sp < s; ++sp) {
-            const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W + d * M);
-#pragma unroll
-            for (int q = 0; q < M / 4; ++q) {
-                const float4 x = __ldcg(a + q);
-                row[4 * q] += x.x;
-                row[4 * q + 1] += x.y;
-                row[4 * q + 2] += x.z;
-                row[4 * q + 3] += x.w;
-            }
-            z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
-        }
-        put_state_row(tm + lane + Lay::T_S, sm + Lay::S, d, row, z, z);
+    if (q < D / 32) {
+        float vals[32];
+        const float z = sum_states(p.sagg + static_cast<size_t>(bh) * p.spans * W, 0, s, row, g, vals);
+        put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, vals, z, z);
     }
     sync_tc();
 
@@ -380,8 +394,8 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
         wait_bar(tma_bar, tma_phase);
-        phi_tile<false>(sm + Lay::Q, 1, valid);
-        phi_tile<true>(sm + Lay::K, 1, valid);
+        phi_tile<false, kBT>(sm + Lay::Q, 1, valid);
+        phi_tile<true, kBT>(sm + Lay::K, 1, valid);
         sync_tc();
         if (sh[1]) goto cleanup;
         if (t == 0) {
@@ -393,38 +407,39 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             mma_state_update(true);
             mma_commit(mma_bar);
+            tma_store_wait_read();  // staging and g tiles are free again
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0) tma_store_wait_read();  // staging and g tiles are free again
-        __syncthreads();
         {   // den, gn, gd -> g tile (bf16) and gd scratch
-            const int i = t;
-            const float rowsum = masked_rows_to_tile<false>(tm + lane + Lay::T_P, nullptr, i, warp);
-            float dz[16];
-            tmem_ld16(tm + lane + Lay::T_DEN, dz);
-            const float den = rowsum + dz[0];
-            float g[64], o[64];
-            read_row64(sm + Lay::G, i, g);
-            read_row64(sm + Lay::O, i, o);
+            const float part = masked_half<false>(tm + lane + Lay::T_P, nullptr, row, q, g);
+            float gv[32], ov[32];
+            read_row32(sm + Lay::G, row, 4 * g, gv);
+            read_row32(sm + Lay::O, row, 4 * g, ov);
             float go = 0.f;
 #pragma unroll
-            for (int e = 0; e < 64; ++e) go = fmaf(g[e], o[e], go);
-            const bool ok = i < valid;
+            for (int e = 0; e < 32; ++e) go = fmaf(gv[e], ov[e], go);
+            xch[g * 128 + row] = part;
+            xch[256 + g * 128 + row] = go;
+            float dz[16];
+            tmem_ld16(tm + lane + Lay::T_DEN, dz);
+            __syncthreads();
+            const float den = xch[row] + xch[128 + row] + dz[0];
+            const float go_all = xch[256 + row] + xch[384 + row];
+            const bool ok = row < valid;
             const float inv = ok ? 1.f / den : 0.f;
-            const float gd = -go * inv;
+            const float gd = -go_all * inv;
+            uint32_t pk[16];
 #pragma unroll
-            for (int j0 = 0; j0 < 64; j0 += 32) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    pk[q] = pack_bf16(g[j0 + 2 * q] * inv, g[j0 + 2 * q + 1] * inv);
-                store_row32(sm + Lay::GH, kAtom, i, j0, pk);
+            for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(gv[2 * u] * inv, gv[2 * u + 1] * inv);
+            store_row32(sm + Lay::GH, kAtom, row, 32 * g, pk);
+            if (g == 0) {
+                *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
+                    make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+                if (ok) p.gd[static_cast<size_t>(bh) * p.N + c0 + row] = gd;
             }
-            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 0)) =
-                make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 1)) = make_uint4(0u, 0u, 0u, 0u);
-            if (ok) p.gd[static_cast<size_t>(bh) * p.N + c0 + i] = gd;
         }
         sync_tc();
         if (t == 0) {
@@ -445,7 +460,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        masked_rows_to_tile(tm + lane + Lay::T_P, sm + Lay::P, t, warp);  // dP, masked, bf16
+        masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);  // dP, masked, bf16
         sync_tc();
         if (t == 0) {
 #pragma unroll
@@ -462,8 +477,8 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
             tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
         }
-        if (warp < D / 32) state_row_to_tile(tm + lane + Lay::T_S, sm + Lay::S, t);  // S_c, Z_c
-        tmem_row_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, t, sm + Lay::Q);       // dQ
+        if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
+        tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, sm + Lay::Q);   // dQ
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
@@ -471,21 +486,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             if (c + 1 < nch) tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0 + L, bh);
         }
     }
-    if (warp < D / 32) {  // publish the span's share of R
-        float* out = p.ragg + static_cast<size_t>(unit) * W;
-        const int d = t;
-        for (int j0 = 0; j0 < M; j0 += 32) {
-            float v[32];
-            tmem_ld32(tm + lane + Lay::T_R + j0, v);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                reinterpret_cast<float4*>(out + d * M + j0)[q] =
-                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-        float r[16];
-        tmem_ld16(tm + lane + Lay::T_R + M, r);
-        out[D * M + d] = r[0];
-    }
+    if (q < D / 32) publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
 
 cleanup:
     if (t == 0) tma_store_wait_all();
@@ -496,7 +497,7 @@ cleanup:
 
 // ------------------------------------------------------------ suffix kernel
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBT, 1)
 bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmGn,
                      const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -504,6 +505,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     using Lay = LayR;
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
+    const int q = warp & 3, g = warp >> 2, row = 32 * q + (t & 31);
     if (smem_u32(sm) & 1023u) {
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
@@ -522,7 +524,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tmem_alloc(tmem_slot, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += kThreads)
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kBT)
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_before_sync();
@@ -534,7 +536,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int bh = unit / p.spans, s = unit - bh * p.spans;
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
-    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sDP = smem_u32(sm + Lay::DP);
@@ -545,35 +547,17 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         atomicOr(p.status, code);
         sh[1] = 1;
     };
-    // One thread polls the barrier; the others wait at the CTA barrier, which
-    // wakes them as soon as it completes (a thread parked in try_wait can
-    // wake much later than the phase flips).
     auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
         if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
         __syncthreads();
         phase ^= 1u;
     };
 
-    if (warp < D / 32) {  // R, r after this span: the later spans' shares, in span order
-        const int d = t;
-        const float* base = p.ragg + static_cast<size_t>(bh) * p.spans * W;
-        float row[M];
-#pragma unroll
-        for (int e = 0; e < M; ++e) row[e] = 0.f;
-        float r = 0.f;
-        for (int sp = s + 1; sp < p.spans; ++sp) {
-            const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W + d * M);
-#pragma unroll
-            for (int q = 0; q < M / 4; ++q) {
-                const float4 x = __ldcg(a + q);
-                row[4 * q] += x.x;
-                row[4 * q + 1] += x.y;
-                row[4 * q + 2] += x.z;
-                row[4 * q + 3] += x.w;
-            }
-            r += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
-        }
-        put_state_row(tm + lane + Lay::T_R, sm + Lay::R, d, row, r, 0.f);
+    if (q < D / 32) {  // R, r after this span: the later spans' shares, in span order
+        float vals[32];
+        const float r = sum_states(p.ragg + static_cast<size_t>(bh) * p.spans * W, s + 1, p.spans,
+                                   row, g, vals);
+        put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, vals, r, 0.f);
     }
     sync_tc();
 
@@ -588,16 +572,15 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     for (int c = nch - 1; c >= 0; --c) {
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
-        {   // gd into the extension atom of the g tile (zero for padding rows)
-            const int i = t;
-            const float gd = i < valid ? __ldcg(p.gd + static_cast<size_t>(bh) * p.N + c0 + i) : 0.f;
-            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 0)) =
+        if (g == 0) {  // gd into the extension atom of the g tile (zero for padding rows)
+            const float gd = row < valid ? __ldcg(p.gd + static_cast<size_t>(bh) * p.N + c0 + row) : 0.f;
+            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
                 make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(i, 1)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
         }
         wait_bar(tma_bar, tma_phase);
-        phi_tile<false>(sm + Lay::Q, 1, valid);
-        phi_tile<true>(sm + Lay::K, 1, valid);
+        phi_tile<false, kBT>(sm + Lay::Q, 1, valid);
+        phi_tile<true, kBT>(sm + Lay::K, 1, valid);
         sync_tc();
         if (sh[1]) goto cleanup;
         if (t == 0) {
@@ -608,13 +591,12 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
                 mma_bf16(tm + Lay::T_DP, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
             mma_commit(mma_bar);
+            tma_store_wait_read();  // the staging tiles (P, dP areas) are free again
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0) tma_store_wait_read();  // the staging tiles (P, dP areas) are free again
-        __syncthreads();
-        masked_rows_to_tile(tm + lane + Lay::T_P, sm + Lay::P, t, warp);
-        masked_rows_to_tile(tm + lane + Lay::T_DP, sm + Lay::DP, t, warp);
+        masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);
+        masked_half<true>(tm + lane + Lay::T_DP, sm + Lay::DP, row, q, g);
         sync_tc();
         if (t == 0) {
 #pragma unroll
@@ -643,9 +625,9 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, cp, bh);
             tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, cp, bh);
         }
-        if (warp < D / 32) state_row_to_tile(tm + lane + Lay::T_R, sm + Lay::R, t);  // R_c
-        tmem_row_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, t, sm + Lay::K);       // dK
-        tmem_row_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, t, nullptr);          // dV
+        if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
+        tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, sm + Lay::K);     // dK
+        tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);        // dV
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
@@ -680,7 +662,7 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
                                   cudaSharedmemCarveoutMaxShared)))
         return e;
     int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kThreads, LayF::BYTES)))
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kBT, LayF::BYTES)))
         return e;
     const int chunks = (N + L - 1) / L;
     const int slots = std::max(1, per_sm) * c.num_sms;
@@ -732,8 +714,8 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
             (e = make_map(&mdQ, dQ, BH, N, D)) || (e = make_map(&mdK, dK, BH, N, D)) ||
             (e = make_map(&mdV, dV, BH, N, M)))
             break;
-        kf<<<units, kThreads, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mGn, mdQ, p);
-        kr<<<units, kThreads, LayR::BYTES, c.stream>>>(mQ, mK, mV, mGn, mdK, mdV, p);
+        kf<<<units, kBT, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mGn, mdQ, p);
+        kr<<<units, kBT, LayR::BYTES, c.stream>>>(mQ, mK, mV, mGn, mdK, mdV, p);
         note_launch(2);
         e = cudaGetLastError();
     } while (0);
