@@ -186,7 +186,11 @@ struct FwdNoncausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
                            int BH, int N) {
-        return noncausal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N);
+        if constexpr (std::is_same<T, float>::value && D == 64 && M == 64)
+            return noncausal_forward_tc_f32(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N);
+        else
+            return noncausal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH,
+                                              N);
     }
 };
 struct Decode {

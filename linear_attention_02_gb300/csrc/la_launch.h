@@ -49,6 +49,11 @@ template <typename T, int D, int M>
 cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,
                             const T* G, T* dQ, T* dK, T* dV, int BH, int N);
 
+// Tensor-core non-causal forward for fp32 storage with D = M = 64 (fp32
+// operands split into two bf16 terms).
+cudaError_t noncausal_forward_tc_f32(const LaunchCtx& c, const float* Q, const float* K,
+                                     const float* V, float* O, int BH, int N);
+
 template <typename T, int D, int M>
 cudaError_t noncausal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O,
                               int BH, int N);

@@ -183,6 +183,26 @@ def test_noncausal_small(dt, shape):
     assert rel_err(O, Ro) <= TOL[dt]
 
 
+@pytest.mark.parametrize("shape", [
+    (1, 1, 1, 64, 64),        # a single token
+    (2, 3, 129, 64, 64),      # one chunk and a one-token tail
+    (8, 40, 300, 64, 64),     # more heads than resident CTAs
+    (1, 2, 4097, 64, 64),     # many spans per head, ragged tail
+])
+def test_noncausal_f32_tensor_core_shapes(shape):
+    # fp32 at D = M = 64 runs on the tensor cores with operands split into two bf16 terms
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "f32", seed=37 + N)
+    g = _dev(x)
+    O = la.la_forward_noncausal(g["Q"], g["K"], g["V"])
+    la.la_check_device_status()
+    idx = list(range(min(B * H, 6)))
+    hs = [x[n].reshape(B * H, N, -1)[idx] for n in ("Q", "K", "V")]
+    Ro = oracle.noncausal_forward_assoc(*hs)[0]
+    assert rel_err(O.reshape(B * H, N, M)[idx], Ro) <= TOL["f32"]
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("B,H,D,M", [(2, 3, 64, 64), (1, 4, 32, 128), (3, 2, 128, 32)])
 def test_decode_continues_prefill(dt, B, H, D, M):
