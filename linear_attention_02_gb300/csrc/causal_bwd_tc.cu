@@ -40,35 +40,42 @@ constexpr int NE = M + 16;
 constexpr int W = D * M + D;           // words of a published (S | Z) or (R | r) state
 constexpr uint32_t S_ATOM = D * 128;   // one atom column of a D-row state tile
 
-// prefix-kernel shared memory
+// prefix-kernel shared memory.  An MN-major operand of D = 64 rows is read by
+// an M = 128 MMA as two atoms (the second one's rows land in accumulator lanes
+// nobody reads), so the atom after Q, Q1 and K must be allocated memory.
 struct LayF {
-    static constexpr uint32_t Q = 0, K = kAtom, V = 2 * kAtom, ONES = 3 * kAtom;
-    static constexpr uint32_t G = 4 * kAtom, O = 5 * kAtom;
-    static constexpr uint32_t GH = 6 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
-    static constexpr uint32_t P = 8 * kAtom;     // dP (bf16), then the dQ staging tile
-    static constexpr uint32_t S = 10 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
+    static constexpr uint32_t Q = 0, Q1 = kAtom;  // Q alternates between two buffers
+    static constexpr uint32_t K = 2 * kAtom, V = 3 * kAtom, ONES = 4 * kAtom;
+    static constexpr uint32_t G = 5 * kAtom, O = 6 * kAtom;
+    static constexpr uint32_t GH = 7 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
+    static constexpr uint32_t P = 9 * kAtom;     // dP (bf16), then the dQ staging tile
+    static constexpr uint32_t S = 11 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
     static constexpr uint32_t XCH = S + 2 * S_ATOM;  // 2 x [2][128] fp32 partial row sums
     static constexpr uint32_t BARS = XCH + 2048;
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_P = 0, T_DEN = 128, T_DQ = 160, T_S = 224, T_R = 304;
     static constexpr uint32_t T_COLS = 512;
 };
+static_assert(LayF::Q1 + 2 * kAtom <= LayF::BYTES && LayF::K + 2 * kAtom <= LayF::BYTES, "padding atom");
+static_assert(LayF::ONES == LayF::V + kAtom, "[V | 1] is two adjacent atoms");
 
 constexpr int kBT = 256;  // two warpgroups: warp w reads TMEM lanes 32 (w % 4) ..., and the
                           // two warps of a lane quarter split the columns of every row
 
-// suffix-kernel shared memory
+// suffix-kernel shared memory (Q, read MN-major as two atoms, is followed by K)
 struct LayR {
     static constexpr uint32_t Q = 0, K = kAtom, V = 2 * kAtom, ONES = 3 * kAtom;
     static constexpr uint32_t GH = 4 * kAtom;
     static constexpr uint32_t P = 6 * kAtom;     // P (bf16), then the dK staging tile
     static constexpr uint32_t DP = 8 * kAtom;    // dP (bf16), then the dV staging tile
     static constexpr uint32_t R = 10 * kAtom;    // [R | r 0..0] bf16, 2 atoms of D rows
-    static constexpr uint32_t BARS = R + 2 * S_ATOM;
+    static constexpr uint32_t K1 = R + 2 * S_ATOM;  // second K buffer (odd chunks), read K-major only
+    static constexpr uint32_t BARS = K1 + kAtom;
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_P = 0, T_DP = 128, T_DV = 256, T_DK = 320, T_R = 384;
     static constexpr uint32_t T_COLS = 512;
 };
+static_assert(LayR::Q + 2 * kAtom <= LayR::BYTES && LayR::ONES == LayR::V + kAtom, "layout");
 
 struct BwdParams {
     int N, spans, span_len;
@@ -304,7 +311,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int nch = (n1 - n0 + L - 1) / L;
     const bool last = s == p.spans - 1;
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
+    const uint32_t sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
     uint32_t tma_phase = 0, mma_phase = 0;
@@ -393,8 +400,14 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     for (int c = 0; c < nch; ++c) {
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
+        uint8_t* const tQ = sm + ((c & 1) ? Lay::Q1 : Lay::Q);  // Q alternates between two buffers
+        const uint32_t sQ = smem_u32(tQ);
         wait_bar(tma_bar, tma_phase);
-        phi_tile<false, kBT>(sm + Lay::Q, 1, valid);
+        if (t == 0 && c + 1 < nch) {  // the next chunk's loads: Q now, the rest as tiles free up
+            mbar_arrive_expect_tx(tma_bar, 5 * kAtom);
+            tma_load_3d(sm + ((c & 1) ? Lay::Q : Lay::Q1), &tmQ, tma_bar, 0, c0 + L, bh);
+        }
+        phi_tile<false, kBT>(tQ, 1, valid);
         phi_tile<true, kBT>(sm + Lay::K, 1, valid);
         sync_tc();
         if (sh[1]) goto cleanup;
@@ -405,9 +418,9 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
                          ID_16_KMN, k > 0);
             }
-            mma_state_update(true);
             mma_commit(mma_bar);
-            tma_store_wait_read();  // staging and g tiles are free again
+            mma_state_update(true);  // tracked by the next commit
+            tma_store_wait_read();   // staging and g tiles are free again
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
@@ -443,23 +456,27 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         sync_tc();
         if (t == 0) {
+            if (c + 1 < nch) {  // G and O are consumed
+                tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
+                tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
+            }
             tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
             tma_store_commit();
 #pragma unroll
-            for (int k = 0; k < NE / 16; ++k) {
-                // dP = g [V | 1]^T  (the P block of TMEM is free again)
+            for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T  (the P block of TMEM is free again)
                 mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
-                // dqf = g [S | Z]^T
+            mma_commit(mma_bar);
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)  // dqf = g [S | Z]^T
                 mma_bf16(tm + Lay::T_DQ, kmaj(sGh, k, kAtom), kmaj(sS, k, S_ATOM), ID_D_KK, k > 0);
-            }
 #pragma unroll
             for (int k = 0; k < L / 16; ++k)  // span share of R: qf^T g
                 mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN,
                          (c > 0 || k > 0) ? 1u : 0u);
-            mma_commit(mma_bar);
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
+        if (t == 0 && c + 1 < nch) tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);  // V consumed
         masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);  // dP, masked, bf16
         sync_tc();
         if (t == 0) {
@@ -470,20 +487,14 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0 && c + 1 < nch) {  // K, V, G, O are consumed; Q waits for dQ's phi'
-            mbar_arrive_expect_tx(tma_bar, 5 * kAtom);
+        if (t == 0 && c + 1 < nch)  // K is consumed
             tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 + L, bh);
-            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
-            tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
-            tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
-        }
         if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
-        tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, sm + Lay::Q);   // dQ
+        tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);            // dQ
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
             tma_store_commit();
-            if (c + 1 < nch) tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0 + L, bh);
         }
     }
     if (q < D / 32) publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
@@ -537,7 +548,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
+    const uint32_t sQ = smem_u32(sm + Lay::Q);
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sDP = smem_u32(sm + Lay::DP);
     const uint32_t sR = smem_u32(sm + Lay::R);
@@ -565,13 +576,15 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int c0 = n0 + (nch - 1) * L;
         mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
         tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0, bh);
-        tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0, bh);
+        tma_load_3d(sm + (((nch - 1) & 1) ? Lay::K1 : Lay::K), &tmK, tma_bar, 0, c0, bh);
         tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0, bh);
         tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, c0, bh);
     }
     for (int c = nch - 1; c >= 0; --c) {
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
+        uint8_t* const tK = sm + ((c & 1) ? Lay::K1 : Lay::K);  // K alternates between two buffers
+        const uint32_t sK = smem_u32(tK);
         if (g == 0) {  // gd into the extension atom of the g tile (zero for padding rows)
             const float gd = row < valid ? __ldcg(p.gd + static_cast<size_t>(bh) * p.N + c0 + row) : 0.f;
             *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
@@ -579,8 +592,12 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
         }
         wait_bar(tma_bar, tma_phase);
+        if (t == 0 && c > 0) {  // the next chunk's loads: K now, the rest as tiles free up
+            mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
+            tma_load_3d(sm + ((c & 1) ? Lay::K : Lay::K1), &tmK, tma_bar, 0, c0 - L, bh);
+        }
         phi_tile<false, kBT>(sm + Lay::Q, 1, valid);
-        phi_tile<true, kBT>(sm + Lay::K, 1, valid);
+        phi_tile<true, kBT>(tK, 1, valid);
         sync_tc();
         if (sh[1]) goto cleanup;
         if (t == 0) {
@@ -591,6 +608,13 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
                 mma_bf16(tm + Lay::T_DP, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
             mma_commit(mma_bar);
+            // R += qf^T g: the R tile already holds R after chunk c + 1, so the TMEM sum can
+            // move on now; tracked by the next commit, not needed after chunk 0
+            if (c > 0) {
+#pragma unroll
+                for (int k = 0; k < L / 16; ++k)
+                    mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN, 1u);
+            }
             tma_store_wait_read();  // the staging tiles (P, dP areas) are free again
         }
         wait_bar(mma_bar, mma_phase);
@@ -611,29 +635,23 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
             for (int k = 0; k < NE / 16; ++k)  // dkf += [V | 1] [R | r]^T
                 mma_bf16(tm + Lay::T_DK, kmaj(sV, k, kAtom), kmaj(sR, k, S_ATOM), ID_D_KK, 1u);
-#pragma unroll
-            for (int k = 0; k < L / 16; ++k)  // R += qf^T g
-                mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN, 1u);
             mma_commit(mma_bar);
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0 && c > 0) {  // Q, V, g are consumed; K waits for dK's phi'
-            const int cp = c0 - L;
-            mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
-            tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, cp, bh);
-            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, cp, bh);
-            tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, cp, bh);
+        if (t == 0 && c > 0) {  // Q, V, g are consumed (the R update included)
+            tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0 - L, bh);
+            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 - L, bh);
+            tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, c0 - L, bh);
         }
-        if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
-        tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, sm + Lay::K);     // dK
-        tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);        // dV
+        if (c > 0 && q < D / 32) state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
+        tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, tK);        // dK
+        tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);  // dV
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
             tma_store_3d(&tmdV, sm + Lay::DP, 0, c0, bh);
             tma_store_commit();
-            if (c > 0) tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 - L, bh);
         }
     }
 
