@@ -42,40 +42,40 @@ constexpr uint32_t S_ATOM = D * 128;   // one atom column of a D-row state tile
 
 // prefix-kernel shared memory.  An MN-major operand of D = 64 rows is read by
 // an M = 128 MMA as two atoms (the second one's rows land in accumulator lanes
-// nobody reads), so the atom after Q, Q1 and K must be allocated memory.
+// nobody reads), so the atom after each Q and K buffer must be allocated.
 struct LayF {
-    static constexpr uint32_t Q = 0, Q1 = kAtom;  // Q alternates between two buffers
-    static constexpr uint32_t K = 2 * kAtom, V = 3 * kAtom, ONES = 4 * kAtom;
-    static constexpr uint32_t G = 5 * kAtom, O = 6 * kAtom;
-    static constexpr uint32_t GH = 7 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
-    static constexpr uint32_t P = 9 * kAtom;     // dP (bf16), then the dQ staging tile
-    static constexpr uint32_t S = 11 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
+    static constexpr uint32_t Q0 = 0, Q1 = kAtom, K0 = 2 * kAtom, K1 = 3 * kAtom;  // two buffers each
+    static constexpr uint32_t V = 4 * kAtom, ONES = 5 * kAtom;
+    static constexpr uint32_t G = 6 * kAtom, O = 7 * kAtom;
+    static constexpr uint32_t GH = 8 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
+    static constexpr uint32_t P = 10 * kAtom;    // dP (bf16), then the dQ staging tile
+    static constexpr uint32_t S = 12 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
     static constexpr uint32_t XCH = S + 2 * S_ATOM;  // 2 x [2][128] fp32 partial row sums
     static constexpr uint32_t BARS = XCH + 2048;
-    static constexpr uint32_t BYTES = BARS + 64;
+    static constexpr uint32_t BYTES = BARS + 128;
     static constexpr uint32_t T_P = 0, T_DEN = 128, T_DQ = 160, T_S = 224, T_R = 304;
     static constexpr uint32_t T_COLS = 512;
 };
-static_assert(LayF::Q1 + 2 * kAtom <= LayF::BYTES && LayF::K + 2 * kAtom <= LayF::BYTES, "padding atom");
+static_assert(LayF::K1 + 2 * kAtom <= LayF::BYTES && LayF::Q1 + kAtom == LayF::K0, "padding atoms");
 static_assert(LayF::ONES == LayF::V + kAtom, "[V | 1] is two adjacent atoms");
 
 constexpr int kBT = 256;  // two warpgroups: warp w reads TMEM lanes 32 (w % 4) ..., and the
                           // two warps of a lane quarter split the columns of every row
 
-// suffix-kernel shared memory (Q, read MN-major as two atoms, is followed by K)
+// suffix-kernel shared memory (Q, read MN-major as two atoms, is followed by allocated atoms)
 struct LayR {
-    static constexpr uint32_t Q = 0, K = kAtom, V = 2 * kAtom, ONES = 3 * kAtom;
-    static constexpr uint32_t GH = 4 * kAtom;
-    static constexpr uint32_t P = 6 * kAtom;     // P (bf16), then the dK staging tile
-    static constexpr uint32_t DP = 8 * kAtom;    // dP (bf16), then the dV staging tile
-    static constexpr uint32_t R = 10 * kAtom;    // [R | r 0..0] bf16, 2 atoms of D rows
-    static constexpr uint32_t K1 = R + 2 * S_ATOM;  // second K buffer (odd chunks), read K-major only
-    static constexpr uint32_t BARS = K1 + kAtom;
-    static constexpr uint32_t BYTES = BARS + 64;
+    static constexpr uint32_t Q0 = 0, Q1 = kAtom, K0 = 2 * kAtom, K1 = 3 * kAtom;  // two buffers each
+    static constexpr uint32_t V = 4 * kAtom, ONES = 5 * kAtom;
+    static constexpr uint32_t GH = 6 * kAtom;
+    static constexpr uint32_t P = 8 * kAtom;     // P (bf16), then the dK staging tile
+    static constexpr uint32_t DP = 10 * kAtom;   // dP (bf16), then the dV staging tile
+    static constexpr uint32_t R = 12 * kAtom;    // [R | r 0..0] bf16, 2 atoms of D rows
+    static constexpr uint32_t BARS = R + 2 * S_ATOM;
+    static constexpr uint32_t BYTES = BARS + 128;
     static constexpr uint32_t T_P = 0, T_DP = 128, T_DV = 256, T_DK = 320, T_R = 384;
     static constexpr uint32_t T_COLS = 512;
 };
-static_assert(LayR::Q + 2 * kAtom <= LayR::BYTES && LayR::ONES == LayR::V + kAtom, "layout");
+static_assert(LayR::Q1 + kAtom == LayR::K0 && LayR::ONES == LayR::V + kAtom, "layout");
 
 struct BwdParams {
     int N, spans, span_len;
@@ -258,16 +258,100 @@ __device__ __forceinline__ void publish_half(uint32_t taddr, float* out, int d, 
     }
 }
 
+constexpr int kTW = 4;                    // transform warps (8 .. 11, one per scheduler)
+constexpr int kTT = 32 * kTW;             // their threads
+constexpr int kCT = kBT + kTT;            // threads per CTA
+constexpr uint32_t kBarE = 1, kBarT = 2;  // named barriers of the compute and transform warps
+
+// Hand-over among the compute warps: their shared-memory writes become
+// visible to the tensor core and TMA, and tcgen05 work is ordered around it.
 __device__ __forceinline__ void sync_tc() {
     fence_proxy_async();
     fence_before_sync();
-    __syncthreads();
+    bar_sync(kBarE, kBT);
     fence_after_sync();
 }
 
+// Barriers and flags at the end of shared memory.
+struct Bars {
+    uint64_t tma, mma;   // compute warps' own copies; MMA completion
+    uint64_t full[2];    // Q, K copies of buffer b landed
+    uint64_t ready[2];   // phi(Q), phi(K) of buffer b are in place
+    uint64_t freeb[2];   // the compute warps are done with buffer b
+    uint32_t tmem, pad;
+    int unit, abort_e, abort_t, pad2;
+};
+static_assert(sizeof(Bars) <= 128, "barrier block");
+
+// Transform warps: for each chunk of [n0, n1) in processing order (reversed
+// for the suffix kernel), load Q and K into buffer (i & 1) once the compute
+// warps have released it, apply phi (zeroing K's rows past the end) and hand
+// the pair over.  Gives up when the compute warps have given up.
+__device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                                 uint8_t* q0, uint8_t* q1, uint8_t* k0, uint8_t* k1,
+                                                 Bars* bars, int n0, int n1, int nch, bool reverse,
+                                                 int bh, unsigned* status) {
+    const int tt = threadIdx.x - kBT;
+    const volatile int* abort_e = &bars->abort_e;
+    for (int i = 0; i < nch; ++i) {
+        const int c = reverse ? nch - 1 - i : i;
+        const int b = i & 1;
+        const uint32_t u = static_cast<uint32_t>(i) >> 1;
+        const int c0 = n0 + c * L;
+        uint8_t* const tq = b ? q1 : q0;
+        uint8_t* const tk = b ? k1 : k0;
+        bool bad = false;
+        if (tt == 0) {
+            const int r = i >= 2 ? mbar_wait_or(&bars->freeb[b], (u - 1) & 1u, kWaitLimit, abort_e) : 0;
+            if (r == 0) {
+                mbar_arrive_expect_tx(&bars->full[b], 2 * kAtom);
+                tma_load_3d(tq, tmQ, &bars->full[b], 0, c0, bh);
+                tma_load_3d(tk, tmK, &bars->full[b], 0, c0, bh);
+                if (!mbar_wait(&bars->full[b], u & 1u, kWaitLimit)) {
+                    atomicOr(status, kErrWait);
+                    bad = true;
+                }
+            } else {
+                if (r == 2) atomicOr(status, kErrWait);
+                bad = true;
+            }
+            if (bad) *reinterpret_cast<volatile int*>(&bars->abort_t) = 1;
+        }
+        if (bar_sync_or(kBarT, kTT, bad)) return;
+        const int valid = min(L, n1 - c0);
+        phi_atom<false, kTT>(tq, valid, tt);
+        phi_atom<true, kTT>(tk, valid, tt);
+        fence_proxy_async();
+        bar_sync(kBarT, kTT);
+        if (tt == 0) mbar_arrive(&bars->ready[b]);
+    }
+}
+
+// Per-thread bookkeeping of the compute warps' own TMA loads (thread 0): the
+// bytes expected on the pending phase of `tma` but not issued yet, so that a
+// kernel giving up early can still drain the copies it started.
+struct TmaBook {
+    bool pending = false;
+    uint32_t missing = 0;
+    __device__ void expect(uint64_t* bar, uint32_t bytes) {
+        mbar_arrive_expect_tx(bar, bytes);
+        pending = true;
+        missing = bytes;
+    }
+    __device__ void load(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+        tma_load_3d(dst, map, bar, x, y, z);
+        missing -= kAtom;
+    }
+    __device__ void drain(uint64_t* bar, uint32_t parity) {
+        if (!pending) return;
+        if (missing) mbar_complete_tx(bar, missing);
+        mbar_wait(bar, parity, kWaitLimit);
+    }
+};
+
 // ------------------------------------------------------------ prefix kernel
 
-__global__ void __launch_bounds__(kBT, 1)
+__global__ void __launch_bounds__(kCT, 1)
 bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmGn,
@@ -275,142 +359,169 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     using Lay = LayF;
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
-    const int q = warp & 3, g = warp >> 2, row = 32 * q + (t & 31);
+    const int q = warp & 3, g = (warp >> 2) & 1, row = 32 * q + (t & 31);
     if (smem_u32(sm) & 1023u) {
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
     }
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
-    uint64_t* mma_bar = tma_bar + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
-    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    Bars* bars = reinterpret_cast<Bars*>(sm + Lay::BARS);
+    volatile int* abort_e = &bars->abort_e;
+    const volatile int* abort_t = &bars->abort_t;
+    uint64_t* tma_bar = &bars->tma;
+    uint64_t* mma_bar = &bars->mma;
     float* xch = reinterpret_cast<float*>(sm + Lay::XCH);  // [2 sums][2 warpgroups][128 rows]
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->full[b], 1);
+            mbar_init(&bars->ready[b], 1);
+            mbar_init(&bars->freeb[b], 1);
+        }
         fence_mbar_init();
-        sh[1] = 0;
+        bars->abort_e = 0;
+        bars->abort_t = 0;
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_alloc(&bars->tmem, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += kBT)
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kCT)
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tm = *tmem_slot;
-    if (t == 0) sh[0] = static_cast<int>(atomicAdd(p.ticket, 1u));
+    const uint32_t tm = bars->tmem;
+    if (t == 0) bars->unit = static_cast<int>(atomicAdd(p.ticket, 1u));
     __syncthreads();
 
-    const int unit = sh[0];
+    const int unit = bars->unit;
     const int bh = unit / p.spans, s = unit - bh * p.spans;
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
     const bool last = s == p.spans - 1;
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
     uint32_t tma_phase = 0, mma_phase = 0;
+    TmaBook book;
 
-    auto fail = [&](unsigned code) {
-        atomicOr(p.status, code);
-        sh[1] = 1;
-    };
-    // One thread polls the barrier; the others wait at the CTA barrier.
-    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
-        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
-        __syncthreads();
+    // Compute warps: waits by thread 0, the outcome shared at the barrier.
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) -> bool {  // true: give up
+        bool bad = false;
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) {
+            atomicOr(p.status, kErrWait);
+            *abort_e = 1;
+            bad = true;
+        }
         phase ^= 1u;
+        return bar_sync_or(kBarE, kBT, bad);
     };
-    auto mma_state_update = [&](bool accumulate_first) {  // S_ext (+)= kf^T [V | 1]
+    auto mma_state_update = [&](uint32_t sK, bool accumulate_first) {  // S_ext (+)= kf^T [V | 1]
 #pragma unroll
         for (int k = 0; k < L / 16; ++k)
             mma_bf16(tm + Lay::T_S, mnmaj(sK, k, kAtom), mnmaj(sV, k, kAtom), ID_NE_MNMN,
                      (accumulate_first || k > 0) ? 1u : 0u);
     };
 
-    // ---------------------------------------------- phase 1: span aggregate
-    if (!last) {
-        if (t == 0) {
-            mbar_arrive_expect_tx(tma_bar, 2 * kAtom);
-            tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, n0, bh);
-            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
-        }
-        for (int c = 0; c < nch; ++c) {
-            const int c0 = n0 + c * L;
-            wait_bar(tma_bar, tma_phase);
-            phi_tile<true, kBT>(sm + Lay::K, 1, min(L, n1 - c0));
-            sync_tc();
-            if (sh[1]) goto cleanup;
+    // ------------------------- phase 1 (span aggregate) and look-back, compute warps
+    auto prelude = [&]() -> bool {  // false: give up
+        const uint32_t sK = smem_u32(sm + Lay::K0);
+        if (!last) {
             if (t == 0) {
-                mma_state_update(c > 0);
-                mma_commit(mma_bar);
+                book.expect(tma_bar, 2 * kAtom);
+                book.load(sm + Lay::K0, &tmK, tma_bar, 0, n0, bh);
+                book.load(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
             }
-            wait_bar(mma_bar, mma_phase);
-            fence_after_sync();
-            if (t == 0 && c + 1 < nch) {
-                mbar_arrive_expect_tx(tma_bar, 2 * kAtom);
-                tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 + L, bh);
-                tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
-            }
-        }
-        if (q < D / 32) publish_half(tm + lane + Lay::T_S, p.sagg + static_cast<size_t>(unit) * W, row, g);
-        __threadfence();
-        fence_before_sync();
-        __syncthreads();
-        if (t == 0) st_release(p.flags + unit, 1u);
-    }
-
-    // ------------------------------------------------------------ look-back
-    if (t == 0) {
-        for (int sp = 0; sp < s && !sh[1]; ++sp) {
-            const unsigned* f = p.flags + (bh * p.spans + sp);
-            uint32_t n = 0;
-            while (ld_acquire(f) == 0u) {
-                if (++n > kSpinLimit) {
-                    fail(kErrLookback);
-                    break;
+            for (int c = 0; c < nch; ++c) {
+                const int c0 = n0 + c * L;
+                if (wait_bar(tma_bar, tma_phase)) return false;
+                if (t == 0) book.pending = false;
+                phi_tile<true, kBT>(sm + Lay::K0, 1, min(L, n1 - c0));
+                sync_tc();
+                if (t == 0) {
+                    mma_state_update(sK, c > 0);
+                    mma_commit(mma_bar);
                 }
-                __nanosleep(256);
+                if (wait_bar(mma_bar, mma_phase)) return false;
+                if (t == 0 && c + 1 < nch) {
+                    book.expect(tma_bar, 2 * kAtom);
+                    book.load(sm + Lay::K0, &tmK, tma_bar, 0, c0 + L, bh);
+                    book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
+                }
+            }
+            if (q < D / 32) publish_half(tm + lane + Lay::T_S, p.sagg + static_cast<size_t>(unit) * W, row, g);
+            __threadfence();
+            fence_before_sync();
+            bar_sync(kBarE, kBT);
+            if (t == 0) st_release(p.flags + unit, 1u);
+        }
+        bool bad = false;
+        if (t == 0) {
+            for (int sp = 0; sp < s && !bad; ++sp) {
+                const unsigned* f = p.flags + (bh * p.spans + sp);
+                uint32_t n = 0;
+                while (ld_acquire(f) == 0u) {
+                    if (++n > kSpinLimit) {
+                        atomicOr(p.status, kErrLookback);
+                        *abort_e = 1;
+                        bad = true;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
             }
         }
-    }
-    __syncthreads();
-    if (sh[1]) goto cleanup;
-    if (q < D / 32) {
-        float vals[32];
-        const float z = sum_states(p.sagg + static_cast<size_t>(bh) * p.spans * W, 0, s, row, g, vals);
-        put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, vals, z, z);
-    }
-    sync_tc();
+        if (bar_sync_or(kBarE, kBT, bad)) return false;
+        if (q < D / 32) {
+            float vals[32];
+            const float z = sum_states(p.sagg + static_cast<size_t>(bh) * p.spans * W, 0, s, row, g, vals);
+            put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, vals, z, z);
+        }
+        sync_tc();
+        return true;
+    };
+    const bool bad_pre = warp < kBT / 32 && !prelude();
+    if (__syncthreads_or(bad_pre)) goto cleanup;
 
-    // ------------------------------------------------- phase 2: dQ, gn, gd
-    if (t == 0) {
-        mbar_arrive_expect_tx(tma_bar, 5 * kAtom);
-        tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, n0, bh);
-        tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, n0, bh);
-        tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
-        tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, n0, bh);
-        tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, n0, bh);
+    if (warp >= kBT / 32) {  // transform warps
+        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars, n0,
+                         n1, nch, false, bh, p.status);
+        goto cleanup;
+    }
+
+    // ------------------------------------------ phase 2: dQ, gn, gd (compute warps)
+    if (t == 0) {  // V, G, O of the first chunk; Q and K come from the transform warps
+        book.expect(tma_bar, 3 * kAtom);
+        book.load(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
+        book.load(sm + Lay::G, &tmG, tma_bar, 0, n0, bh);
+        book.load(sm + Lay::O, &tmO, tma_bar, 0, n0, bh);
     }
     for (int c = 0; c < nch; ++c) {
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
-        uint8_t* const tQ = sm + ((c & 1) ? Lay::Q1 : Lay::Q);  // Q alternates between two buffers
-        const uint32_t sQ = smem_u32(tQ);
-        wait_bar(tma_bar, tma_phase);
-        if (t == 0 && c + 1 < nch) {  // the next chunk's loads: Q now, the rest as tiles free up
-            mbar_arrive_expect_tx(tma_bar, 5 * kAtom);
-            tma_load_3d(sm + ((c & 1) ? Lay::Q : Lay::Q1), &tmQ, tma_bar, 0, c0 + L, bh);
+        const int b = c & 1;
+        const uint32_t u = static_cast<uint32_t>(c) >> 1;
+        uint8_t* const tQ = sm + (b ? Lay::Q1 : Lay::Q0);
+        const uint32_t sQ = smem_u32(tQ), sK = smem_u32(sm + (b ? Lay::K1 : Lay::K0));
+        {   // this chunk's phi(Q), phi(K) from the transform warps and V, G, O by TMA
+            bool bad = false;
+            if (t == 0) {
+                const int r = mbar_wait_or(&bars->ready[b], u & 1u, kWaitLimit, abort_t);
+                if (r == 0 && mbar_wait(tma_bar, tma_phase, kWaitLimit)) {
+                    tma_phase ^= 1u;
+                    book.pending = false;
+                    if (c + 1 < nch) book.expect(tma_bar, 3 * kAtom);  // the next chunk's V, G, O
+                } else {
+                    if (r != 1) atomicOr(p.status, kErrWait);
+                    *abort_e = 1;
+                    bad = true;
+                }
+            }
+            if (bar_sync_or(kBarE, kBT, bad)) goto cleanup;
+            fence_after_sync();
         }
-        phi_tile<false, kBT>(tQ, 1, valid);
-        phi_tile<true, kBT>(sm + Lay::K, 1, valid);
-        sync_tc();
-        if (sh[1]) goto cleanup;
         if (t == 0) {
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
@@ -419,10 +530,10 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                          ID_16_KMN, k > 0);
             }
             mma_commit(mma_bar);
-            mma_state_update(true);  // tracked by the next commit
-            tma_store_wait_read();   // staging and g tiles are free again
+            mma_state_update(sK, true);  // tracked by the next commit
+            tma_store_wait_read();       // staging and g tiles are free again
         }
-        wait_bar(mma_bar, mma_phase);
+        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
         {   // den, gn, gd -> g tile (bf16) and gd scratch
             const float part = masked_half<false>(tm + lane + Lay::T_P, nullptr, row, q, g);
@@ -436,7 +547,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             xch[256 + g * 128 + row] = go;
             float dz[16];
             tmem_ld16(tm + lane + Lay::T_DEN, dz);
-            __syncthreads();
+            bar_sync(kBarE, kBT);
             const float den = xch[row] + xch[128 + row] + dz[0];
             const float go_all = xch[256 + row] + xch[384 + row];
             const bool ok = row < valid;
@@ -444,7 +555,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const float gd = -go_all * inv;
             uint32_t pk[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(gv[2 * u] * inv, gv[2 * u + 1] * inv);
+            for (int u2 = 0; u2 < 16; ++u2) pk[u2] = pack_bf16(gv[2 * u2] * inv, gv[2 * u2 + 1] * inv);
             store_row32(sm + Lay::GH, kAtom, row, 32 * g, pk);
             if (g == 0) {
                 *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
@@ -457,8 +568,8 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         sync_tc();
         if (t == 0) {
             if (c + 1 < nch) {  // G and O are consumed
-                tma_load_3d(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
-                tma_load_3d(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
+                book.load(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
+                book.load(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
             }
             tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
             tma_store_commit();
@@ -474,9 +585,9 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN,
                          (c > 0 || k > 0) ? 1u : 0u);
         }
-        wait_bar(mma_bar, mma_phase);
+        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
-        if (t == 0 && c + 1 < nch) tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);  // V consumed
+        if (t == 0 && c + 1 < nch) book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);  // V consumed
         masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);  // dP, masked, bf16
         sync_tc();
         if (t == 0) {
@@ -485,22 +596,24 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_DQ, kmaj(sP, k, kAtom), mnmaj(sK, k, kAtom), ID_D_KMN, 1u);
             mma_commit(mma_bar);
         }
-        wait_bar(mma_bar, mma_phase);
+        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
-        if (t == 0 && c + 1 < nch)  // K is consumed
-            tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0 + L, bh);
         if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
         tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);            // dQ
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
             tma_store_commit();
+            mbar_arrive(&bars->freeb[b]);  // this chunk's Q and K buffers
         }
     }
     if (q < D / 32) publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
 
 cleanup:
-    if (t == 0) tma_store_wait_all();
+    if (t == 0) {
+        book.drain(tma_bar, tma_phase);
+        tma_store_wait_all();
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
@@ -508,7 +621,7 @@ cleanup:
 
 // ------------------------------------------------------------ suffix kernel
 
-__global__ void __launch_bounds__(kBT, 1)
+__global__ void __launch_bounds__(kCT, 1)
 bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmGn,
                      const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -516,90 +629,119 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     using Lay = LayR;
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
-    const int q = warp & 3, g = warp >> 2, row = 32 * q + (t & 31);
+    const int q = warp & 3, g = (warp >> 2) & 1, row = 32 * q + (t & 31);
     if (smem_u32(sm) & 1023u) {
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
     }
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
-    uint64_t* mma_bar = tma_bar + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
-    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    Bars* bars = reinterpret_cast<Bars*>(sm + Lay::BARS);
+    volatile int* abort_e = &bars->abort_e;
+    const volatile int* abort_t = &bars->abort_t;
+    uint64_t* tma_bar = &bars->tma;
+    uint64_t* mma_bar = &bars->mma;
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->full[b], 1);
+            mbar_init(&bars->ready[b], 1);
+            mbar_init(&bars->freeb[b], 1);
+        }
         fence_mbar_init();
-        sh[1] = 0;
+        bars->abort_e = 0;
+        bars->abort_t = 0;
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_alloc(&bars->tmem, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += kBT)
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += kCT)
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tm = *tmem_slot;
+    const uint32_t tm = bars->tmem;
 
     const int unit = blockIdx.x;
     const int bh = unit / p.spans, s = unit - bh * p.spans;
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t sQ = smem_u32(sm + Lay::Q);
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sDP = smem_u32(sm + Lay::DP);
     const uint32_t sR = smem_u32(sm + Lay::R);
+    const float* gd_head = p.gd + static_cast<size_t>(bh) * p.N;
     uint32_t tma_phase = 0, mma_phase = 0;
+    TmaBook book;
+    float gd_next = 0.f;
 
-    auto fail = [&](unsigned code) {
-        atomicOr(p.status, code);
-        sh[1] = 1;
-    };
-    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
-        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
-        __syncthreads();
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) -> bool {  // true: give up
+        bool bad = false;
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) {
+            atomicOr(p.status, kErrWait);
+            *abort_e = 1;
+            bad = true;
+        }
         phase ^= 1u;
+        return bar_sync_or(kBarE, kBT, bad);
     };
 
-    if (q < D / 32) {  // R, r after this span: the later spans' shares, in span order
-        float vals[32];
-        const float r = sum_states(p.ragg + static_cast<size_t>(bh) * p.spans * W, s + 1, p.spans,
-                                   row, g, vals);
-        put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, vals, r, 0.f);
+    if (warp < kBT / 32) {
+        if (q < D / 32) {  // R, r after this span: the later spans' shares, in span order
+            float vals[32];
+            const float r = sum_states(p.ragg + static_cast<size_t>(bh) * p.spans * W, s + 1, p.spans,
+                                       row, g, vals);
+            put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, vals, r, 0.f);
+        }
+        const int cl = nch - 1;
+        if (g == 0) gd_next = row < n1 - (n0 + cl * L) ? __ldcg(gd_head + n0 + cl * L + row) : 0.f;
+        if (t == 0) {  // V and g of the first chunk; Q and K come from the transform warps
+            book.expect(tma_bar, 2 * kAtom);
+            book.load(sm + Lay::V, &tmV, tma_bar, 0, n0 + cl * L, bh);
+            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, n0 + cl * L, bh);
+        }
+        sync_tc();
     }
-    sync_tc();
+    __syncthreads();
+    if (warp >= kBT / 32) {  // transform warps
+        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars, n0,
+                         n1, nch, true, bh, p.status);
+        goto cleanup;
+    }
 
-    if (t == 0) {
-        const int c0 = n0 + (nch - 1) * L;
-        mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
-        tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0, bh);
-        tma_load_3d(sm + (((nch - 1) & 1) ? Lay::K1 : Lay::K), &tmK, tma_bar, 0, c0, bh);
-        tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0, bh);
-        tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, c0, bh);
-    }
-    for (int c = nch - 1; c >= 0; --c) {
+    for (int i = 0; i < nch; ++i) {
+        const int c = nch - 1 - i;
         const int c0 = n0 + c * L;
-        const int valid = min(L, n1 - c0);
-        uint8_t* const tK = sm + ((c & 1) ? Lay::K1 : Lay::K);  // K alternates between two buffers
-        const uint32_t sK = smem_u32(tK);
+        const int b = i & 1;
+        const uint32_t u = static_cast<uint32_t>(i) >> 1;
+        uint8_t* const tK = sm + (b ? Lay::K1 : Lay::K0);
+        const uint32_t sQ = smem_u32(sm + (b ? Lay::Q1 : Lay::Q0)), sK = smem_u32(tK);
         if (g == 0) {  // gd into the extension atom of the g tile (zero for padding rows)
-            const float gd = row < valid ? __ldcg(p.gd + static_cast<size_t>(bh) * p.N + c0 + row) : 0.f;
+            const float gd = gd_next;
             *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
                 make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
+            if (c > 0) gd_next = __ldcg(gd_head + c0 - L + row);  // earlier chunks are full
+            fence_proxy_async();
         }
-        wait_bar(tma_bar, tma_phase);
-        if (t == 0 && c > 0) {  // the next chunk's loads: K now, the rest as tiles free up
-            mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
-            tma_load_3d(sm + ((c & 1) ? Lay::K : Lay::K1), &tmK, tma_bar, 0, c0 - L, bh);
+        {   // this chunk's phi(Q), phi(K) from the transform warps and V, g by TMA
+            bool bad = false;
+            if (t == 0) {
+                const int r = mbar_wait_or(&bars->ready[b], u & 1u, kWaitLimit, abort_t);
+                if (r == 0 && mbar_wait(tma_bar, tma_phase, kWaitLimit)) {
+                    tma_phase ^= 1u;
+                    book.pending = false;
+                    if (c > 0) book.expect(tma_bar, 2 * kAtom);  // the next chunk's V, g
+                } else {
+                    if (r != 1) atomicOr(p.status, kErrWait);
+                    *abort_e = 1;
+                    bad = true;
+                }
+            }
+            if (bar_sync_or(kBarE, kBT, bad)) goto cleanup;
+            fence_after_sync();
         }
-        phi_tile<false, kBT>(sm + Lay::Q, 1, valid);
-        phi_tile<true, kBT>(tK, 1, valid);
-        sync_tc();
-        if (sh[1]) goto cleanup;
         if (t == 0) {
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)  // P = qf kf^T
@@ -617,7 +759,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             tma_store_wait_read();  // the staging tiles (P, dP areas) are free again
         }
-        wait_bar(mma_bar, mma_phase);
+        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
         masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);
         masked_half<true>(tm + lane + Lay::T_DP, sm + Lay::DP, row, q, g);
@@ -637,12 +779,11 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_DK, kmaj(sV, k, kAtom), kmaj(sR, k, S_ATOM), ID_D_KK, 1u);
             mma_commit(mma_bar);
         }
-        wait_bar(mma_bar, mma_phase);
+        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
-        if (t == 0 && c > 0) {  // Q, V, g are consumed (the R update included)
-            tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0 - L, bh);
-            tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0 - L, bh);
-            tma_load_3d(sm + Lay::GH, &tmGn, tma_bar, 0, c0 - L, bh);
+        if (t == 0 && c > 0) {  // V and g are consumed (the R update included)
+            book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 - L, bh);
+            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, c0 - L, bh);
         }
         if (c > 0 && q < D / 32) state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
         tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, tK);        // dK
@@ -652,11 +793,15 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
             tma_store_3d(&tmdV, sm + Lay::DP, 0, c0, bh);
             tma_store_commit();
+            mbar_arrive(&bars->freeb[b]);  // this chunk's Q and K buffers
         }
     }
 
 cleanup:
-    if (t == 0) tma_store_wait_all();
+    if (t == 0) {
+        book.drain(tma_bar, tma_phase);
+        tma_store_wait_all();
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
@@ -680,7 +825,7 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
                                   cudaSharedmemCarveoutMaxShared)))
         return e;
     int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kBT, LayF::BYTES)))
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kCT, LayF::BYTES)))
         return e;
     const int chunks = (N + L - 1) / L;
     const int slots = std::max(1, per_sm) * c.num_sms;
@@ -732,8 +877,8 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
             (e = make_map(&mdQ, dQ, BH, N, D)) || (e = make_map(&mdK, dK, BH, N, D)) ||
             (e = make_map(&mdV, dV, BH, N, M)))
             break;
-        kf<<<units, kBT, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mGn, mdQ, p);
-        kr<<<units, kBT, LayR::BYTES, c.stream>>>(mQ, mK, mV, mGn, mdK, mdV, p);
+        kf<<<units, kCT, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mGn, mdQ, p);
+        kr<<<units, kCT, LayR::BYTES, c.stream>>>(mQ, mK, mV, mGn, mdK, mdV, p);
         note_launch(2);
         e = cudaGetLastError();
     } while (0);

@@ -53,10 +53,22 @@ __device__ __forceinline__ float phi_fast(float x) {
     return fmaxf(x, 0.f) + ex2_approx(fminf(x, 0.f) * 1.4426950408889634f);
 }
 
-// phi on two packed bf16 values (a bf16 is the high half of an fp32, so the
-// unpack is a shift and a mask).
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-    return pack_bf16(phi_fast(__uint_as_float(w << 16)), phi_fast(__uint_as_float(w & 0xFFFF0000u)));
+// phi on two packed bf16 values in packed bf16 arithmetic: max(x, 0) +
+// 2^(min(x, 0) * log2 e), one exponential per pair.  For x > 0 the exponent
+// is 0 and the sum is x + 1 rounded once; for x <= 0 it is e^x.  The product
+// and the approximate 2^u are each within about one bf16 rounding, the size
+// of the rounding the result gets anyway when stored as bf16.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
+    uint32_t r;
+    asm("{\n\t.reg .b32 n, p, y, e;\n\t"
+        "min.bf16x2 n, %1, %2;\n\t"
+        "max.bf16x2 p, %1, %2;\n\t"
+        "fma.rn.bf16x2 y, n, %3, %2;\n\t"
+        "ex2.approx.ftz.bf16x2 e, y;\n\t"
+        "fma.rn.bf16x2 %0, p, %4, e;\n\t}"
+        : "=r"(r)
+        : "r"(x), "r"(0u), "r"(0x3FB93FB9u), "r"(0x3F803F80u));  // 0, log2 e, 1 (bf16 pairs)
+    return r;
 }
 
 // phi in place over `atoms` swizzled atom columns (1024 16-byte chunks each);
@@ -87,6 +99,31 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int atoms, int valid) {
 #pragma unroll
         for (int j = 0; j < U; ++j)
             *reinterpret_cast<uint4*>(tile + static_cast<size_t>(base + j * NT) * 16) = u[j];
+    }
+}
+
+// phi_tile for one atom, worked by NT threads numbered `tid` = 0 .. NT - 1.
+template <bool ZERO_TAIL, int NT>
+__device__ __forceinline__ void phi_atom(uint8_t* tile, int valid, int tid) {
+    constexpr int U = 1024 / NT < 8 ? 1024 / NT : 8;
+#pragma unroll 1
+    for (int base = tid; base < 1024; base += NT * U) {
+        uint4 u[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) u[j] = *reinterpret_cast<const uint4*>(tile + (base + j * NT) * 16);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            if (ZERO_TAIL && ((base + j * NT) >> 3) >= valid) {
+                u[j] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                u[j].x = phi_bf16x2(u[j].x);
+                u[j].y = phi_bf16x2(u[j].y);
+                u[j].z = phi_bf16x2(u[j].z);
+                u[j].w = phi_bf16x2(u[j].w);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) *reinterpret_cast<uint4*>(tile + (base + j * NT) * 16) = u[j];
     }
 }
 

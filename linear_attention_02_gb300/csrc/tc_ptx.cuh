@@ -56,12 +56,54 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Counts `bytes` of the current phase's expected transaction bytes as arrived
+// (for copies that were expected but never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Named barrier `id` over `n` threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also returns the OR of `pred` over its `n` threads, so a
+// decision taken by one thread reaches all of them at the same point.
+__device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
 // Waits for the phase of `bar` with the given parity; gives up after `limit`
 // polls (each try_wait itself blocks for a bounded, hardware-chosen time).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// As mbar_wait, but also gives up as soon as `*abort` is set.  Returns 0 when
+// the phase completed, 1 on abort, 2 on timeout.
+__device__ __forceinline__ int mbar_wait_or(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                            const volatile int* abort) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return 0;
+        if (*abort) return 1;
+    }
+    return 2;
 }
 
 // ----------------------------------------------------------------------- TMA
