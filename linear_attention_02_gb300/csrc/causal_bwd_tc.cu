@@ -13,14 +13,21 @@
 //   dkf_c  = dP^T qf_c + [V | 1] [R | r]_{c+1}^T
 // and dQ = dqf * phi'(Q), dK = dkf * phi'(K) with phi' = min(phi, 1).
 //
-// Two kernels, one CTA per (head, span):
+// Two kernels over the same work split as the forward (the chunks of all heads,
+// head-major, cut into equal ranges, one per CTA; a range's pieces in
+// successive heads are its segments):
 //   prefix kernel -- phase 1 / look-back exactly as the forward to get the
-//     span's starting S, Z; then per chunk: P and qf.Z by MMA, den, gn, gd
-//     (written to scratch), dP and dqf by MMA, dQ out, and the span's
-//     sum qf^T g (its share of R) published for the suffix kernel;
-//   suffix kernel -- starts from the sum of the later spans' shares (all
-//     complete, the prefix kernel has finished) and walks its chunks in
-//     reverse: P and dP again, dV and dkf by MMA, R += qf^T g.
+//     first piece's starting S, Z (later pieces start a head from zero); then
+//     per chunk: P and qf.Z by MMA, den, gn, gd (written to scratch), dP and
+//     dqf by MMA, dQ out; the first piece's sum qf^T g (its share of R) is
+//     published for the suffix kernel;
+//   suffix kernel -- walks its chunks in reverse; the last piece starts from
+//     the shares of the later units of its head (all complete, the prefix
+//     kernel has finished), earlier pieces from zero: P and dP again, dV and
+//     dkf by MMA, R += qf^T g.
+// Each CTA has eight compute warps and four transform warps: the transform
+// warps load the next chunk's Q and K into the free one of two buffers and
+// apply phi there, so that work leaves the compute warps' chain.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -78,9 +85,9 @@ struct LayR {
 static_assert(LayR::Q1 + kAtom == LayR::K0 && LayR::ONES == LayR::V + kAtom, "layout");
 
 struct BwdParams {
-    int N, spans, span_len;
-    float* sagg;          // [units][W] per-span (sum kf V^T | sum kf)
-    float* ragg;          // [units][W] per-span (sum qf gn^T | sum qf gd)
+    int N, BH, CH, per;   // tokens, heads, chunks per head, chunks per unit
+    float* sagg;          // [units][W] last piece's (sum kf V^T | sum kf), pieces stopping mid-head
+    float* ragg;          // [units][W] first piece's (sum qf gn^T | sum qf gd)
     unsigned* flags;      // [units]
     unsigned* ticket;
     float* gd;            // [BH][N]
@@ -283,21 +290,23 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 128, "barrier block");
 
-// Transform warps: for each chunk of [n0, n1) in processing order (reversed
-// for the suffix kernel), load Q and K into buffer (i & 1) once the compute
-// warps have released it, apply phi (zeroing K's rows past the end) and hand
-// the pair over.  Gives up when the compute warps have given up.
+// Transform warps: for each global chunk of the unit's range [start, end) in
+// processing order (reversed for the suffix kernel), load Q and K into buffer
+// (i & 1) once the compute warps have released it, apply phi (zeroing K's
+// rows past the end of the head) and hand the pair over.  Gives up when the
+// compute warps have given up.
 __device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                                  uint8_t* q0, uint8_t* q1, uint8_t* k0, uint8_t* k1,
-                                                 Bars* bars, int n0, int n1, int nch, bool reverse,
-                                                 int bh, unsigned* status) {
+                                                 Bars* bars, int start, int end, int CH, int N,
+                                                 bool reverse, unsigned* status) {
     const int tt = threadIdx.x - kBT;
     const volatile int* abort_e = &bars->abort_e;
-    for (int i = 0; i < nch; ++i) {
-        const int c = reverse ? nch - 1 - i : i;
+    for (int i = 0; i < end - start; ++i) {
+        const int gc = reverse ? end - 1 - i : start + i;
+        const int bh = gc / CH;
+        const int c0 = (gc - bh * CH) * L;
         const int b = i & 1;
         const uint32_t u = static_cast<uint32_t>(i) >> 1;
-        const int c0 = n0 + c * L;
         uint8_t* const tq = b ? q1 : q0;
         uint8_t* const tk = b ? k1 : k0;
         bool bad = false;
@@ -318,7 +327,7 @@ __device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const C
             if (bad) *reinterpret_cast<volatile int*>(&bars->abort_t) = 1;
         }
         if (bar_sync_or(kBarT, kTT, bad)) return;
-        const int valid = min(L, n1 - c0);
+        const int valid = min(L, N - c0);
         phi_atom<false, kTT>(tq, valid, tt);
         phi_atom<true, kTT>(tk, valid, tt);
         fence_proxy_async();
@@ -397,10 +406,8 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     __syncthreads();
 
     const int unit = bars->unit;
-    const int bh = unit / p.spans, s = unit - bh * p.spans;
-    const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
-    const int nch = (n1 - n0 + L - 1) / L;
-    const bool last = s == p.spans - 1;
+    const UnitRange ur(unit, p.per, p.CH, p.BH);
+    const int first_end = min(ur.end, (ur.hA + 1) * p.CH);  // end of the first piece
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
@@ -425,30 +432,31 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                      (accumulate_first || k > 0) ? 1u : 0u);
     };
 
-    // ------------------------- phase 1 (span aggregate) and look-back, compute warps
+    // ------ phase 1 (aggregate of a last piece that stops mid-head) and look-back, compute warps
     auto prelude = [&]() -> bool {  // false: give up
         const uint32_t sK = smem_u32(sm + Lay::K0);
-        if (!last) {
+        if (ur.publish) {
+            const int h = ur.hB, g0 = max(ur.start, h * p.CH);
             if (t == 0) {
                 book.expect(tma_bar, 2 * kAtom);
-                book.load(sm + Lay::K0, &tmK, tma_bar, 0, n0, bh);
-                book.load(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
+                book.load(sm + Lay::K0, &tmK, tma_bar, 0, (g0 - h * p.CH) * L, h);
+                book.load(sm + Lay::V, &tmV, tma_bar, 0, (g0 - h * p.CH) * L, h);
             }
-            for (int c = 0; c < nch; ++c) {
-                const int c0 = n0 + c * L;
+            for (int gc = g0; gc < ur.end; ++gc) {
+                const int c0 = (gc - h * p.CH) * L;
                 if (wait_bar(tma_bar, tma_phase)) return false;
                 if (t == 0) book.pending = false;
-                phi_tile<true, kBT>(sm + Lay::K0, 1, min(L, n1 - c0));
+                phi_tile<true, kBT>(sm + Lay::K0, 1, min(L, p.N - c0));
                 sync_tc();
                 if (t == 0) {
-                    mma_state_update(sK, c > 0);
+                    mma_state_update(sK, gc > g0);
                     mma_commit(mma_bar);
                 }
                 if (wait_bar(mma_bar, mma_phase)) return false;
-                if (t == 0 && c + 1 < nch) {
+                if (t == 0 && gc + 1 < ur.end) {
                     book.expect(tma_bar, 2 * kAtom);
-                    book.load(sm + Lay::K0, &tmK, tma_bar, 0, c0 + L, bh);
-                    book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);
+                    book.load(sm + Lay::K0, &tmK, tma_bar, 0, c0 + L, h);
+                    book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, h);
                 }
             }
             if (q < D / 32) publish_half(tm + lane + Lay::T_S, p.sagg + static_cast<size_t>(unit) * W, row, g);
@@ -458,11 +466,10 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             if (t == 0) st_release(p.flags + unit, 1u);
         }
         bool bad = false;
-        if (t == 0) {
-            for (int sp = 0; sp < s && !bad; ++sp) {
-                const unsigned* f = p.flags + (bh * p.spans + sp);
+        if (t == 0 && ur.look) {
+            for (int sp = ur.u_first; sp < unit && !bad; ++sp) {
                 uint32_t n = 0;
-                while (ld_acquire(f) == 0u) {
+                while (ld_acquire(p.flags + sp) == 0u) {
                     if (++n > kSpinLimit) {
                         atomicOr(p.status, kErrLookback);
                         *abort_e = 1;
@@ -476,7 +483,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (bar_sync_or(kBarE, kBT, bad)) return false;
         if (q < D / 32) {
             float vals[32];
-            const float z = sum_states(p.sagg + static_cast<size_t>(bh) * p.spans * W, 0, s, row, g, vals);
+            const float z = sum_states(p.sagg, ur.look ? ur.u_first : unit, unit, row, g, vals);
             put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, vals, z, z);
         }
         sync_tc();
@@ -486,23 +493,28 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     if (__syncthreads_or(bad_pre)) goto cleanup;
 
     if (warp >= kBT / 32) {  // transform warps
-        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars, n0,
-                         n1, nch, false, bh, p.status);
+        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars,
+                         ur.start, ur.end, p.CH, p.N, false, p.status);
         goto cleanup;
     }
 
     // ------------------------------------------ phase 2: dQ, gn, gd (compute warps)
     if (t == 0) {  // V, G, O of the first chunk; Q and K come from the transform warps
+        const int c0 = (ur.start - ur.hA * p.CH) * L;
         book.expect(tma_bar, 3 * kAtom);
-        book.load(sm + Lay::V, &tmV, tma_bar, 0, n0, bh);
-        book.load(sm + Lay::G, &tmG, tma_bar, 0, n0, bh);
-        book.load(sm + Lay::O, &tmO, tma_bar, 0, n0, bh);
+        book.load(sm + Lay::V, &tmV, tma_bar, 0, c0, ur.hA);
+        book.load(sm + Lay::G, &tmG, tma_bar, 0, c0, ur.hA);
+        book.load(sm + Lay::O, &tmO, tma_bar, 0, c0, ur.hA);
     }
-    for (int c = 0; c < nch; ++c) {
-        const int c0 = n0 + c * L;
-        const int valid = min(L, n1 - c0);
-        const int b = c & 1;
-        const uint32_t u = static_cast<uint32_t>(c) >> 1;
+    for (int gc = ur.start; gc < ur.end; ++gc) {
+        const int bh = gc / p.CH, cc = gc - bh * p.CH;
+        const int c0 = cc * L;
+        const int valid = min(L, p.N - c0);
+        const int hn = (gc + 1) / p.CH, cn0 = (gc + 1 - hn * p.CH) * L;  // the next chunk
+        const bool more = gc + 1 < ur.end;
+        const bool in_first = gc < first_end;  // this chunk's qf^T g enters the published R share
+        const int b = (gc - ur.start) & 1;
+        const uint32_t u = static_cast<uint32_t>(gc - ur.start) >> 1;
         uint8_t* const tQ = sm + (b ? Lay::Q1 : Lay::Q0);
         const uint32_t sQ = smem_u32(tQ), sK = smem_u32(sm + (b ? Lay::K1 : Lay::K0));
         {   // this chunk's phi(Q), phi(K) from the transform warps and V, G, O by TMA
@@ -512,7 +524,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (r == 0 && mbar_wait(tma_bar, tma_phase, kWaitLimit)) {
                     tma_phase ^= 1u;
                     book.pending = false;
-                    if (c + 1 < nch) book.expect(tma_bar, 3 * kAtom);  // the next chunk's V, G, O
+                    if (more) book.expect(tma_bar, 3 * kAtom);  // the next chunk's V, G, O
                 } else {
                     if (r != 1) atomicOr(p.status, kErrWait);
                     *abort_e = 1;
@@ -567,9 +579,9 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         sync_tc();
         if (t == 0) {
-            if (c + 1 < nch) {  // G and O are consumed
-                book.load(sm + Lay::G, &tmG, tma_bar, 0, c0 + L, bh);
-                book.load(sm + Lay::O, &tmO, tma_bar, 0, c0 + L, bh);
+            if (more) {  // G and O are consumed
+                book.load(sm + Lay::G, &tmG, tma_bar, 0, cn0, hn);
+                book.load(sm + Lay::O, &tmO, tma_bar, 0, cn0, hn);
             }
             tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
             tma_store_commit();
@@ -580,14 +592,16 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
             for (int k = 0; k < NE / 16; ++k)  // dqf = g [S | Z]^T
                 mma_bf16(tm + Lay::T_DQ, kmaj(sGh, k, kAtom), kmaj(sS, k, S_ATOM), ID_D_KK, k > 0);
+            if (in_first) {
 #pragma unroll
-            for (int k = 0; k < L / 16; ++k)  // span share of R: qf^T g
-                mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN,
-                         (c > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < L / 16; ++k)  // the first piece's share of R: qf^T g
+                    mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN,
+                             (gc > ur.start || k > 0) ? 1u : 0u);
+            }
         }
         if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
-        if (t == 0 && c + 1 < nch) book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, bh);  // V consumed
+        if (t == 0 && more) book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);  // V consumed
         masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);  // dP, masked, bf16
         sync_tc();
         if (t == 0) {
@@ -598,8 +612,19 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
-        if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
-        tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);            // dQ
+        if (q < D / 32) {
+            if (gc == first_end - 1)  // the first piece is complete: publish its share of R
+                publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
+            if (more && hn != bh) {  // the next chunk starts a head: zero state
+                float zero[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) zero[e] = 0.f;
+                put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, zero, 0.f, 0.f);
+            } else {
+                state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
+            }
+        }
+        tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);  // dQ
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
@@ -607,7 +632,6 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             mbar_arrive(&bars->freeb[b]);  // this chunk's Q and K buffers
         }
     }
-    if (q < D / 32) publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
 
 cleanup:
     if (t == 0) {
@@ -664,14 +688,11 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t tm = bars->tmem;
 
     const int unit = blockIdx.x;
-    const int bh = unit / p.spans, s = unit - bh * p.spans;
-    const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
-    const int nch = (n1 - n0 + L - 1) / L;
+    const UnitRange ur(unit, p.per, p.CH, p.BH);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sDP = smem_u32(sm + Lay::DP);
     const uint32_t sR = smem_u32(sm + Lay::R);
-    const float* gd_head = p.gd + static_cast<size_t>(bh) * p.N;
     uint32_t tma_phase = 0, mma_phase = 0;
     TmaBook book;
     float gd_next = 0.f;
@@ -686,33 +707,41 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         phase ^= 1u;
         return bar_sync_or(kBarE, kBT, bad);
     };
+    // gd of rows 0 .. 127 of global chunk gc (zero past the end of its head)
+    auto gd_rows = [&](int gc) {
+        const int h = gc / p.CH, c0 = (gc - h * p.CH) * L;
+        return row < p.N - c0 ? __ldcg(p.gd + static_cast<size_t>(h) * p.N + c0 + row) : 0.f;
+    };
 
     if (warp < kBT / 32) {
-        if (q < D / 32) {  // R, r after this span: the later spans' shares, in span order
+        if (q < D / 32) {  // R, r after the last piece: the first-piece shares of the later units
             float vals[32];
-            const float r = sum_states(p.ragg + static_cast<size_t>(bh) * p.spans * W, s + 1, p.spans,
-                                       row, g, vals);
+            const int sp0 = ur.publish ? unit + 1 : 0, sp1 = ur.publish ? ur.u_last + 1 : 0;
+            const float r = sum_states(p.ragg, sp0, sp1, row, g, vals);
             put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, vals, r, 0.f);
         }
-        const int cl = nch - 1;
-        if (g == 0) gd_next = row < n1 - (n0 + cl * L) ? __ldcg(gd_head + n0 + cl * L + row) : 0.f;
+        if (g == 0) gd_next = gd_rows(ur.end - 1);
         if (t == 0) {  // V and g of the first chunk; Q and K come from the transform warps
+            const int c0 = (ur.end - 1 - ur.hB * p.CH) * L;
             book.expect(tma_bar, 2 * kAtom);
-            book.load(sm + Lay::V, &tmV, tma_bar, 0, n0 + cl * L, bh);
-            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, n0 + cl * L, bh);
+            book.load(sm + Lay::V, &tmV, tma_bar, 0, c0, ur.hB);
+            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, c0, ur.hB);
         }
         sync_tc();
     }
     __syncthreads();
     if (warp >= kBT / 32) {  // transform warps
-        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars, n0,
-                         n1, nch, true, bh, p.status);
+        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars,
+                         ur.start, ur.end, p.CH, p.N, true, p.status);
         goto cleanup;
     }
 
-    for (int i = 0; i < nch; ++i) {
-        const int c = nch - 1 - i;
-        const int c0 = n0 + c * L;
+    for (int gc = ur.end - 1; gc >= ur.start; --gc) {
+        const int bh = gc / p.CH, cc = gc - bh * p.CH;
+        const int c0 = cc * L;
+        const bool more = gc > ur.start;
+        const int hn = (gc - 1) / p.CH, cn0 = (gc - 1 - hn * p.CH) * L;  // the next chunk (if more)
+        const int i = ur.end - 1 - gc;
         const int b = i & 1;
         const uint32_t u = static_cast<uint32_t>(i) >> 1;
         uint8_t* const tK = sm + (b ? Lay::K1 : Lay::K0);
@@ -722,7 +751,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
                 make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
-            if (c > 0) gd_next = __ldcg(gd_head + c0 - L + row);  // earlier chunks are full
+            if (more) gd_next = gd_rows(gc - 1);
             fence_proxy_async();
         }
         {   // this chunk's phi(Q), phi(K) from the transform warps and V, g by TMA
@@ -732,7 +761,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (r == 0 && mbar_wait(tma_bar, tma_phase, kWaitLimit)) {
                     tma_phase ^= 1u;
                     book.pending = false;
-                    if (c > 0) book.expect(tma_bar, 2 * kAtom);  // the next chunk's V, g
+                    if (more) book.expect(tma_bar, 2 * kAtom);  // the next chunk's V, g
                 } else {
                     if (r != 1) atomicOr(p.status, kErrWait);
                     *abort_e = 1;
@@ -750,9 +779,9 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
                 mma_bf16(tm + Lay::T_DP, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
             mma_commit(mma_bar);
-            // R += qf^T g: the R tile already holds R after chunk c + 1, so the TMEM sum can
-            // move on now; tracked by the next commit, not needed after chunk 0
-            if (c > 0) {
+            // R += qf^T g: the R tile already holds R after chunk gc + 1, so the TMEM sum can
+            // move on now; tracked by the next commit, not needed before a head's first chunk
+            if (cc > 0) {
 #pragma unroll
                 for (int k = 0; k < L / 16; ++k)
                     mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN, 1u);
@@ -781,11 +810,20 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         if (wait_bar(mma_bar, mma_phase)) goto cleanup;
         fence_after_sync();
-        if (t == 0 && c > 0) {  // V and g are consumed (the R update included)
-            book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 - L, bh);
-            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, c0 - L, bh);
+        if (t == 0 && more) {  // V and g are consumed (the R update included)
+            book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
+            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, cn0, hn);
         }
-        if (c > 0 && q < D / 32) state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
+        if (q < D / 32) {
+            if (cc > 0) {
+                state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
+            } else if (more) {  // the next chunk ends the previous head: R starts from zero
+                float zero[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) zero[e] = 0.f;
+                put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, zero, 0.f, 0.f);
+            }
+        }
         tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, tK);        // dK
         tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);  // dV
         sync_tc();
@@ -829,11 +867,8 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
         return e;
     const int chunks = (N + L - 1) / L;
     const int slots = std::max(1, per_sm) * c.num_sms;
-    int spans = choose_spans(BH, chunks, slots, 12);
-    const int per = (chunks + spans - 1) / spans;
-    const int span_len = per * L;
-    spans = (N + span_len - 1) / span_len;
-    const int units = BH * spans;
+    const ChunkSplit split = split_chunks(BH, chunks, slots);
+    const int units = split.units;
 
     const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * W;
     const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
@@ -846,8 +881,9 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), total)) != cudaSuccess) return e;
     BwdParams p;
     p.N = N;
-    p.spans = spans;
-    p.span_len = span_len;
+    p.BH = BH;
+    p.CH = chunks;
+    p.per = split.per;
     char* q = ws;
     p.sagg = reinterpret_cast<float*>(q);
     q += up(agg_bytes);

@@ -1,8 +1,7 @@
 // causal_tc.cu -- chunked causal linear-attention forward on the 5th-generation
 // tensor core (bf16 storage, fp32 accumulation), D = M in {64, 128}.
 //
-// Per head the sequence is cut into spans (one CTA each) and each span into
-// chunks of L = 128 tokens.  With phi(x) = elu(x) + 1 ("Transformers are RNNs",
+// The sequence of every head is cut into chunks of L = 128 tokens.  With phi(x) = elu(x) + 1 ("Transformers are RNNs",
 // section 特征映射) applied in shared memory, a chunk c needs
 //   P      = tril(phi(Q_c) phi(K_c)^T)                (intra-chunk scores, eq. mask)
 //   O_ext  = phi(Q_c) [S | Z]_{c-1} + P [V_c | 1]     (numerator and normaliser)
@@ -21,12 +20,16 @@
 // Tiles arrive by TMA with the 128-byte swizzle; P, the bf16 state and the
 // output tile are written by the threads in the same swizzled layout.
 //
-// Spans: phase 1 of every span but the last accumulates its aggregate
-// (sum phi(K)^T V | sum phi(K)) and publishes it with a release flag; phase 2
-// sums the aggregates of the earlier spans of its head (bounded waits on the
-// flags) into its starting state, then runs the chunk loop.  Units are taken
-// from an atomic ticket after TMEM is allocated, so a CTA only ever waits for
-// CTAs that started (and hold their TMEM) before it.
+// Work split: the chunks of all heads, head-major, are cut into equal ranges,
+// one per resident CTA, so a range may end inside a head and the next range
+// continue it.  Phase 1 of a unit whose range stops inside a head accumulates
+// that last piece's aggregate (sum phi(K)^T V | sum phi(K)) and publishes it
+// with a release flag; phase 2 starts its first piece from the carried-in
+// state plus the aggregates of the earlier units of that head (bounded waits
+// on their flags), then runs the chunk loop, restarting the state at every
+// head boundary.  Units are taken from an atomic ticket after TMEM is
+// allocated, so a CTA only ever waits for CTAs that started (and hold their
+// TMEM) before it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -79,7 +82,7 @@ struct Layout {
 };
 
 struct FwdParams {
-    int N, spans, span_len;
+    int N, BH, CH, per;    // tokens, heads, chunks per head, chunks per unit
     float* agg;            // [units][W]
     unsigned* flags;       // [units], zero before the launch
     unsigned* ticket;      // zero before the launch
@@ -144,10 +147,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     __syncthreads();
 
     const int unit = sh[0];
-    const int bh = unit / p.spans, s = unit - bh * p.spans;
-    const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
-    const int nch = (n1 - n0 + L - 1) / L;
-    const bool last = s == p.spans - 1;
+    const UnitRange ur(unit, p.per, p.CH, p.BH);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V), sP = smem_u32(sm + Lay::P);
@@ -164,14 +164,14 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncthreads();
         phase ^= 1u;
     };
-    auto load = [&](int c0, bool with_q) {  // thread 0 only
+    auto load = [&](int h, int c0, bool with_q) {  // thread 0 only
         mbar_arrive_expect_tx(tma_bar, with_q ? Lay::TX_QKV : Lay::TX_KV);
         for (int a = 0; a < DA; ++a) {
-            if (with_q) tma_load_3d(sm + Lay::Q + a * kAtom, &tmQ, tma_bar, 64 * a, c0, bh);
-            tma_load_3d(sm + Lay::K + a * kAtom, &tmK, tma_bar, 64 * a, c0, bh);
+            if (with_q) tma_load_3d(sm + Lay::Q + a * kAtom, &tmQ, tma_bar, 64 * a, c0, h);
+            tma_load_3d(sm + Lay::K + a * kAtom, &tmK, tma_bar, 64 * a, c0, h);
         }
         for (int a = 0; a < MA; ++a)
-            tma_load_3d(sm + Lay::V + a * kAtom, &tmV, tma_bar, 64 * a, c0, bh);
+            tma_load_3d(sm + Lay::V + a * kAtom, &tmV, tma_bar, 64 * a, c0, h);
     };
     auto mma_state_update = [&](bool accumulate_first) {  // S_ext (+)= phi(K)^T [V | 1]
 #pragma unroll
@@ -179,26 +179,72 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             mma_bf16(tm + Lay::T_S, sdesc(sK + 2048 * k, kAtom, 1024),
                      sdesc(sV + 2048 * k, kAtom, 1024), ID_S, (accumulate_first || k > 0) ? 1u : 0u);
     };
+    // Starting state of a segment of head h: the carried-in state plus the
+    // published aggregates of units sp0 <= sp < sp1, into TMEM and the bf16
+    // S tile (threads with q < D / 32: state row d = row).
+    auto put_state = [&](int h, int sp0, int sp1) {
+        const int d = row;
+        for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                v[i] = p.S_init ? p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i] : 0.f;
+            for (int sp = sp0; sp < sp1; ++sp) {
+                const float4* a =
+                    reinterpret_cast<const float4*>(p.agg + static_cast<size_t>(sp) * W + d * M + j0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 x = __ldcg(a + u);
+                    v[4 * u] += x.x;
+                    v[4 * u + 1] += x.y;
+                    v[4 * u + 2] += x.z;
+                    v[4 * u + 3] += x.w;
+                }
+            }
+            tmem_st16(tm + lane + Lay::T_S + j0, v);
+            const int cc = j0 >> 3;
+            *reinterpret_cast<uint4*>(sm + Lay::S + (cc >> 3) * Lay::S_ATOM + swz(d, cc & 7)) =
+                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                           pack_bf16(v[6], v[7]));
+            *reinterpret_cast<uint4*>(sm + Lay::S + ((cc + 1) >> 3) * Lay::S_ATOM +
+                                      swz(d, (cc + 1) & 7)) =
+                make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
+                           pack_bf16(v[14], v[15]));
+        }
+        if (g == 0) {
+            float z = p.Z_init ? p.Z_init[static_cast<size_t>(h) * D + d] : 0.f;
+            for (int sp = sp0; sp < sp1; ++sp) z += __ldcg(p.agg + static_cast<size_t>(sp) * W + D * M + d);
+            float zv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zv[i] = z;
+            tmem_st16(tm + lane + Lay::T_S + M, zv);
+            const uint32_t zz = pack_bf16(z, z);
+            const uint4 z4 = make_uint4(zz, zz, zz, zz);
+            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) = z4;
+            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) = z4;
+        }
+    };
 
-    // ---------------------------------------------- phase 1: span aggregate
-    if (!last) {
-        if (t == 0) load(n0, false);
-        for (int c = 0; c < nch; ++c) {
-            const int c0 = n0 + c * L;
+    // ------------------------- phase 1: aggregate of a last segment that stops mid-head
+    if (ur.publish) {
+        const int h = ur.hB, g0 = max(ur.start, h * p.CH);
+        if (t == 0) load(h, (g0 - h * p.CH) * L, false);
+        for (int gc = g0; gc < ur.end; ++gc) {
+            const int c0 = (gc - h * p.CH) * L;
             wait_bar(tma_bar, tma_phase);
-            phi_tile<true, NT>(sm + Lay::K, DA, min(L, n1 - c0));
+            phi_tile<true, NT>(sm + Lay::K, DA, min(L, p.N - c0));
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
             fence_after_sync();
             if (sh[1]) goto cleanup;
             if (t == 0) {
-                mma_state_update(c > 0);
+                mma_state_update(gc > g0);
                 mma_commit(mma_bar);
             }
             wait_bar(mma_bar, mma_phase);
             fence_after_sync();
-            if (t == 0 && c + 1 < nch) load(c0 + L, false);
+            if (t == 0 && gc + 1 < ur.end) load(h, c0 + L, false);
         }
         if (q < D / 32) {  // rows d < D of S_ext, this warpgroup's columns
             float* out = p.agg + static_cast<size_t>(unit) * W;
@@ -223,12 +269,11 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (t == 0) st_release(p.flags + unit, 1u);
     }
 
-    // ------------------------------ look-back: starting state of this span
-    if (t == 0) {
-        for (int sp = 0; sp < s && !sh[1]; ++sp) {
-            const unsigned* f = p.flags + (bh * p.spans + sp);
+    // ------------------ look-back: starting state of the first segment
+    if (t == 0 && ur.look) {
+        for (int sp = ur.u_first; sp < unit && !sh[1]; ++sp) {
             uint32_t n = 0;
-            while (ld_acquire(f) == 0u) {
+            while (ld_acquire(p.flags + sp) == 0u) {
                 if (++n > kSpinLimit) {
                     fail(kErrLookback);
                     break;
@@ -239,59 +284,18 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     __syncthreads();
     if (sh[1]) goto cleanup;
-    if (q < D / 32) {
-        const int d = row;
-        const float* base = p.agg + static_cast<size_t>(bh) * p.spans * W;
-        for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 16) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                v[i] = p.S_init ? p.S_init[(static_cast<size_t>(bh) * D + d) * M + j0 + i] : 0.f;
-            for (int sp = 0; sp < s; ++sp) {
-                const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W +
-                                                                  d * M + j0);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 x = __ldcg(a + u);
-                    v[4 * u] += x.x;
-                    v[4 * u + 1] += x.y;
-                    v[4 * u + 2] += x.z;
-                    v[4 * u + 3] += x.w;
-                }
-            }
-            tmem_st16(tm + lane + Lay::T_S + j0, v);
-            const int cc = j0 >> 3;
-            *reinterpret_cast<uint4*>(sm + Lay::S + (cc >> 3) * Lay::S_ATOM + swz(d, cc & 7)) =
-                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                           pack_bf16(v[6], v[7]));
-            *reinterpret_cast<uint4*>(sm + Lay::S + ((cc + 1) >> 3) * Lay::S_ATOM +
-                                      swz(d, (cc + 1) & 7)) =
-                make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
-                           pack_bf16(v[14], v[15]));
-        }
-        if (g == 0) {
-            float z = p.Z_init ? p.Z_init[static_cast<size_t>(bh) * D + d] : 0.f;
-            for (int sp = 0; sp < s; ++sp) z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
-            float zv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) zv[i] = z;
-            tmem_st16(tm + lane + Lay::T_S + M, zv);
-            const uint32_t zz = pack_bf16(z, z);
-            const uint4 z4 = make_uint4(zz, zz, zz, zz);
-            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) = z4;
-            *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) = z4;
-        }
-    }
+    if (q < D / 32) put_state(ur.hA, ur.look ? ur.u_first : unit, unit);
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
 
     // ------------------------------------------------- phase 2: outputs
-    if (t == 0) load(n0, true);
-    for (int c = 0; c < nch; ++c) {
-        const int c0 = n0 + c * L;
-        const int valid = min(L, n1 - c0);
+    if (t == 0) load(ur.hA, (ur.start - ur.hA * p.CH) * L, true);
+    for (int gc = ur.start; gc < ur.end; ++gc) {
+        const int h = gc / p.CH, cc = gc - h * p.CH;
+        const int c0 = cc * L;
+        const int valid = min(L, p.N - c0);
         wait_bar(tma_bar, tma_phase);
         phi_tile<false, NT>(sm + Lay::Q, DA, valid);
         phi_tile<true, NT>(sm + Lay::K, DA, valid);
@@ -350,27 +354,50 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0 && c + 1 < nch) load(c0 + L, true);  // every input tile is consumed
-        if (q < D / 32) {  // S_c -> bf16 copy for the next chunk's O_ext
+        if (t == 0 && gc + 1 < ur.end) {  // every input tile is consumed
+            const int hn = (gc + 1) / p.CH;
+            load(hn, (gc + 1 - hn * p.CH) * L, true);
+        }
+        if (q < D / 32) {
             const int d = row;
-            for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
-                float v[32];
-                tmem_ld32(tm + lane + Lay::T_S + j0, v);
-                uint32_t pk[16];
+            if (cc == p.CH - 1) {  // the head ends here: its final state, then the next head's start
+                if (p.S_final) {
+                    float* so = p.S_final + (static_cast<size_t>(h) * D + d) * M;
+                    for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
+                        float v[32];
+                        tmem_ld32(tm + lane + Lay::T_S + j0, v);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
-                store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, pk);
-            }
-            if (g == 0) {
-                float z[16];
-                tmem_ld16(tm + lane + Lay::T_S + M, z);
-                uint32_t zk[8];
+                        for (int u = 0; u < 8; ++u)
+                            reinterpret_cast<float4*>(so + j0)[u] =
+                                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                    }
+                    if (g == 0) {
+                        float z[16];
+                        tmem_ld16(tm + lane + Lay::T_S + M, z);
+                        p.Z_final[static_cast<size_t>(h) * D + d] = z[0];
+                    }
+                }
+                if (gc + 1 < ur.end) put_state(h + 1, 0, 0);
+            } else {  // S_c -> bf16 copy for the next chunk's O_ext
+                for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
+                    float v[32];
+                    tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) zk[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
-                *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) =
-                    make_uint4(zk[0], zk[1], zk[2], zk[3]);
-                *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) =
-                    make_uint4(zk[4], zk[5], zk[6], zk[7]);
+                    for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+                    store_row32(sm + Lay::S, Lay::S_ATOM, d, j0, pk);
+                }
+                if (g == 0) {
+                    float z[16];
+                    tmem_ld16(tm + lane + Lay::T_S + M, z);
+                    uint32_t zk[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) zk[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
+                    *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 0)) =
+                        make_uint4(zk[0], zk[1], zk[2], zk[3]);
+                    *reinterpret_cast<uint4*>(sm + Lay::S + MA * Lay::S_ATOM + swz(d, 1)) =
+                        make_uint4(zk[4], zk[5], zk[6], zk[7]);
+                }
             }
         }
         {   // V' = O_ext[:, :M] / O_ext[:, M] -> bf16 staging tile (P area)
@@ -391,26 +418,8 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncthreads();
         fence_after_sync();
         if (t == 0) {
-            for (int a = 0; a < MA; ++a) tma_store_3d(&tmO, sm + Lay::P + a * kAtom, 64 * a, c0, bh);
+            for (int a = 0; a < MA; ++a) tma_store_3d(&tmO, sm + Lay::P + a * kAtom, 64 * a, c0, h);
             tma_store_commit();
-        }
-    }
-
-    if (last && p.S_final && q < D / 32) {
-        const int d = row;
-        float* so = p.S_final + (static_cast<size_t>(bh) * D + d) * M;
-        for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
-            float v[32];
-            tmem_ld32(tm + lane + Lay::T_S + j0, v);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                reinterpret_cast<float4*>(so + j0)[u] =
-                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        }
-        if (g == 0) {
-            float z[16];
-            tmem_ld16(tm + lane + Lay::T_S + M, z);
-            p.Z_final[static_cast<size_t>(bh) * D + d] = z[0];
         }
     }
 
@@ -446,11 +455,8 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     // and can report one CTA where two fit: take the larger of it and the fit
     // computed from shared memory and TMEM.
     const int slots = std::max(per_sm, Lay::PER_SM) * c.num_sms;  // CTAs resident at once
-    int spans = choose_spans(BH, chunks, slots, 12);
-    const int per = (chunks + spans - 1) / spans;
-    const int span_len = per * L;
-    spans = (N + span_len - 1) / span_len;
-    const int units = BH * spans;
+    const ChunkSplit split = split_chunks(BH, chunks, slots);
+    const int units = split.units;
 
     const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * Lay::W;
     const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
@@ -459,8 +465,9 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.N = N;
-    p.spans = spans;
-    p.span_len = span_len;
+    p.BH = BH;
+    p.CH = chunks;
+    p.per = split.per;
     p.agg = reinterpret_cast<float*>(ws);
     p.flags = reinterpret_cast<unsigned*>(ws + agg_bytes);
     p.ticket = p.flags + units;

@@ -141,25 +141,41 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, uint32_t atom_bytes, 
 
 // ------------------------------------------------------------------ host
 
-// Spans per head for a grid of (head, span) units over `slots` resident CTAs:
-// minimises waves x chunks-per-span, charging every span but the last for its
-// aggregate pass over K and V (about a third of a full chunk).
-inline int choose_spans(int BH, int chunks, int slots, int max_spans) {
-    int best = 1;
-    double best_cost = 1e300;
-    for (int s = 1; s <= std::min(chunks, max_spans); ++s) {
-        const int per = (chunks + s - 1) / s;
-        const int eff = (chunks + per - 1) / per;
-        const long units = static_cast<long>(BH) * eff;
-        const long waves = (units + slots - 1) / slots;
-        const double cost = static_cast<double>(waves) * per * (eff > 1 ? 1.35 : 1.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = eff;
-        }
-    }
-    return best;
+// Work split of the causal kernels: the chunks of all heads, head-major, cut
+// into `units` equal ranges of `per` chunks, one per resident CTA (one wave,
+// every CTA busy for the same number of chunks whatever the head count).
+struct ChunkSplit {
+    int per, units;
+};
+inline ChunkSplit split_chunks(int BH, int chunks_per_head, int slots) {
+    const long long total = static_cast<long long>(BH) * chunks_per_head;
+    const long long per = std::max(1LL, (total + slots - 1) / std::max(1, slots));
+    return {static_cast<int>(per), static_cast<int>((total + per - 1) / per)};
 }
+
+// One unit's range [start, end) of global chunk indices (head h = index / CH)
+// and how it meets its neighbours.  Its pieces in successive heads are its
+// segments: only the first can continue a head begun by earlier units, and
+// only the last can stop inside a head that later units continue.
+struct UnitRange {
+    int start, end;  // global chunk indices
+    int hA, hB;      // heads of the first and the last segment
+    bool look;       // the first segment continues a head: earlier units hold its prefix
+    bool publish;    // the last segment stops inside its head: later units need its sum
+    int u_first;     // first unit holding a chunk of head hA
+    int u_last;      // last unit holding a chunk of head hB
+    __device__ UnitRange(int u, int per, int CH, int BH) {
+        const int total = BH * CH;
+        start = u * per;
+        end = min(total, start + per);
+        hA = start / CH;
+        hB = (end - 1) / CH;
+        look = start != hA * CH;
+        publish = end != (hB + 1) * CH;
+        u_first = hA * CH / per;
+        u_last = ((hB + 1) * CH - 1) / per;
+    }
+};
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -67,12 +67,16 @@ def test_causal_forward_small(dt, shape):
     assert rel_err(Z, Rz) <= TOL[dt]
 
 
+# The tensor-core kernels cut the chunks of all heads (head-major) into equal
+# ranges, one per resident CTA: a range can hold the tail of one head, whole
+# heads and the start of another, or a piece in the middle of a head.
 @pytest.mark.parametrize("shape", [
-    (8, 64, 300, 64, 64),     # more heads than resident CTAs: several waves, one span per head
-    (1, 2, 5000, 128, 128),   # few heads: many spans per head, ragged last chunk
+    (8, 64, 300, 64, 64),     # many short heads: ranges of several heads each, ragged tails
+    (1, 2, 5000, 128, 128),   # few heads: one chunk per range, ragged last chunk
     (1, 1, 128, 64, 64),      # exactly one chunk
     (2, 3, 129, 64, 64),      # one full chunk and a single-token tail
     (1, 4, 4096, 64, 64),
+    (2, 3, 8300, 64, 64),     # several chunks per range, ranges crossing heads, ragged last chunk
 ])
 def test_causal_forward_bf16_span_shapes(shape):
     la = _la()
@@ -129,10 +133,11 @@ def test_causal_backward_small(dt, shape, pass_out):
 
 
 @pytest.mark.parametrize("shape", [
-    (1, 2, 4096, 64, 64),     # few heads: several spans per head
-    (8, 40, 300, 64, 64),     # more heads than SMs: one span per head, ragged tail
+    (1, 2, 4096, 64, 64),     # few heads: one chunk per range
+    (8, 40, 300, 64, 64),     # many short heads: ranges of several heads each, ragged tails
     (2, 3, 129, 64, 64),      # one chunk plus a single-token tail
     (1, 1, 128, 64, 64),
+    (2, 3, 8300, 64, 64),     # several chunks per range, ranges crossing heads, ragged last chunk
 ])
 @pytest.mark.parametrize("pass_out", [True, False])
 def test_causal_backward_bf16_span_shapes(shape, pass_out):
