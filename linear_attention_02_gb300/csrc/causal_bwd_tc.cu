@@ -64,7 +64,7 @@ struct LayF {
     static constexpr uint32_t T_COLS = 512;
 };
 static_assert(LayF::K1 + 2 * kAtom <= LayF::BYTES && LayF::Q1 + kAtom == LayF::K0, "padding atoms");
-static_assert(LayF::ONES == LayF::V + kAtom, "[V | 1] is two adjacent atoms");
+static_assert(LayF::ONES == LayF::V + kAtom && LayF::O == LayF::G + kAtom, "[V | 1] is two adjacent atoms");
 
 constexpr int kBT = 256;  // two warpgroups: warp w reads TMEM lanes 32 (w % 4) ..., and the
                           // two warps of a lane quarter split the columns of every row
@@ -425,40 +425,50 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         phase ^= 1u;
         return bar_sync_or(kBarE, kBT, bad);
     };
-    auto mma_state_update = [&](uint32_t sK, bool accumulate_first) {  // S_ext (+)= kf^T [V | 1]
+    // S_ext (+)= kf^T [V | 1] from K at sK and V at sv (a ones atom right after it)
+    auto mma_state_update = [&](uint32_t sK, uint32_t sv, bool accumulate_first) {
 #pragma unroll
         for (int k = 0; k < L / 16; ++k)
-            mma_bf16(tm + Lay::T_S, mnmaj(sK, k, kAtom), mnmaj(sV, k, kAtom), ID_NE_MNMN,
+            mma_bf16(tm + Lay::T_S, mnmaj(sK, k, kAtom), mnmaj(sv, k, kAtom), ID_NE_MNMN,
                      (accumulate_first || k > 0) ? 1u : 0u);
     };
 
     // ------ phase 1 (aggregate of a last piece that stops mid-head) and look-back, compute warps
+    // Phase 1 alternates K and V between (K0, V) and (K1, G) -- a ones atom written into O,
+    // right after G -- so the next chunk's copy overlaps this chunk's phi and MMA.
     auto prelude = [&]() -> bool {  // false: give up
-        const uint32_t sK = smem_u32(sm + Lay::K0);
         if (ur.publish) {
             const int h = ur.hB, g0 = max(ur.start, h * p.CH);
-            if (t == 0) {
+            auto load_kv = [&](int c0, int b) {  // thread 0 only
                 book.expect(tma_bar, 2 * kAtom);
-                book.load(sm + Lay::K0, &tmK, tma_bar, 0, (g0 - h * p.CH) * L, h);
-                book.load(sm + Lay::V, &tmV, tma_bar, 0, (g0 - h * p.CH) * L, h);
-            }
+                book.load(sm + (b ? Lay::K1 : Lay::K0), &tmK, tma_bar, 0, c0, h);
+                book.load(sm + (b ? Lay::G : Lay::V), &tmV, tma_bar, 0, c0, h);
+            };
+            for (int i = t; i < static_cast<int>(kAtom / 16); i += kBT)
+                reinterpret_cast<uint4*>(sm + Lay::O)[i] =
+                    make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+            fence_proxy_async();
+            if (t == 0) load_kv((g0 - h * p.CH) * L, 0);
             for (int gc = g0; gc < ur.end; ++gc) {
                 const int c0 = (gc - h * p.CH) * L;
+                const int b = (gc - g0) & 1;
                 if (wait_bar(tma_bar, tma_phase)) return false;
                 if (t == 0) book.pending = false;
-                phi_tile<true, kBT>(sm + Lay::K0, 1, min(L, p.N - c0));
+                if (gc > g0) {  // the previous chunk's MMA has released the other buffer
+                    if (wait_bar(mma_bar, mma_phase)) return false;
+                    fence_after_sync();
+                }
+                if (t == 0 && gc + 1 < ur.end) load_kv(c0 + L, b ^ 1);
+                phi_tile<true, kBT>(sm + (b ? Lay::K1 : Lay::K0), 1, min(L, p.N - c0));
                 sync_tc();
                 if (t == 0) {
-                    mma_state_update(sK, gc > g0);
+                    mma_state_update(smem_u32(sm + (b ? Lay::K1 : Lay::K0)), b ? smem_u32(sm + Lay::G) : sV,
+                                     gc > g0);
                     mma_commit(mma_bar);
                 }
-                if (wait_bar(mma_bar, mma_phase)) return false;
-                if (t == 0 && gc + 1 < ur.end) {
-                    book.expect(tma_bar, 2 * kAtom);
-                    book.load(sm + Lay::K0, &tmK, tma_bar, 0, c0 + L, h);
-                    book.load(sm + Lay::V, &tmV, tma_bar, 0, c0 + L, h);
-                }
             }
+            if (wait_bar(mma_bar, mma_phase)) return false;
+            fence_after_sync();
             if (q < D / 32) publish_half(tm + lane + Lay::T_S, p.sagg + static_cast<size_t>(unit) * W, row, g);
             __threadfence();
             fence_before_sync();
@@ -542,7 +552,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                          ID_16_KMN, k > 0);
             }
             mma_commit(mma_bar);
-            mma_state_update(sK, true);  // tracked by the next commit
+            mma_state_update(sK, sV, true);  // tracked by the next commit
             tma_store_wait_read();       // staging and g tiles are free again
         }
         if (wait_bar(mma_bar, mma_phase)) goto cleanup;

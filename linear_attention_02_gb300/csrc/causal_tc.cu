@@ -173,11 +173,12 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int a = 0; a < MA; ++a)
             tma_load_3d(sm + Lay::V + a * kAtom, &tmV, tma_bar, 64 * a, c0, h);
     };
-    auto mma_state_update = [&](bool accumulate_first) {  // S_ext (+)= phi(K)^T [V | 1]
+    // S_ext (+)= phi(K)^T [V | 1] from K at sk and V at sv (the ones atom kAtom * MA after it)
+    auto mma_state_update = [&](uint32_t sk, uint32_t sv, bool accumulate_first) {
 #pragma unroll
         for (int k = 0; k < L / 16; ++k)
-            mma_bf16(tm + Lay::T_S, sdesc(sK + 2048 * k, kAtom, 1024),
-                     sdesc(sV + 2048 * k, kAtom, 1024), ID_S, (accumulate_first || k > 0) ? 1u : 0u);
+            mma_bf16(tm + Lay::T_S, sdesc(sk + 2048 * k, kAtom, 1024),
+                     sdesc(sv + 2048 * k, kAtom, 1024), ID_S, (accumulate_first || k > 0) ? 1u : 0u);
     };
     // Starting state of a segment of head h: the carried-in state plus the
     // published aggregates of units sp0 <= sp < sp1, into TMEM and the bf16
@@ -226,26 +227,45 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     };
 
     // ------------------------- phase 1: aggregate of a last segment that stops mid-head
+    // K and V alternate between their own tiles and a second buffer in the idle Q and P
+    // areas (a ones atom written after the second V), so the next chunk's copy overlaps
+    // this chunk's phi and MMA.
     if (ur.publish) {
         const int h = ur.hB, g0 = max(ur.start, h * p.CH);
-        if (t == 0) load(h, (g0 - h * p.CH) * L, false);
+        auto load_kv = [&](int c0, int b) {  // thread 0 only
+            mbar_arrive_expect_tx(tma_bar, Lay::TX_KV);
+            for (int a = 0; a < DA; ++a)
+                tma_load_3d(sm + (b ? Lay::Q : Lay::K) + a * kAtom, &tmK, tma_bar, 64 * a, c0, h);
+            for (int a = 0; a < MA; ++a)
+                tma_load_3d(sm + (b ? Lay::P : Lay::V) + a * kAtom, &tmV, tma_bar, 64 * a, c0, h);
+        };
+        for (int i = t; i < static_cast<int>(kAtom / 16); i += NT)
+            reinterpret_cast<uint4*>(sm + Lay::P + MA * kAtom)[i] =
+                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        fence_proxy_async();
+        if (t == 0) load_kv((g0 - h * p.CH) * L, 0);
         for (int gc = g0; gc < ur.end; ++gc) {
             const int c0 = (gc - h * p.CH) * L;
+            const int b = (gc - g0) & 1;
             wait_bar(tma_bar, tma_phase);
-            phi_tile<true, NT>(sm + Lay::K, DA, min(L, p.N - c0));
+            if (gc > g0) {  // the previous chunk's MMA has released the other buffer
+                wait_bar(mma_bar, mma_phase);
+                fence_after_sync();
+            }
+            if (t == 0 && gc + 1 < ur.end) load_kv(c0 + L, b ^ 1);
+            phi_tile<true, NT>(sm + (b ? Lay::Q : Lay::K), DA, min(L, p.N - c0));
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
             fence_after_sync();
             if (sh[1]) goto cleanup;
             if (t == 0) {
-                mma_state_update(gc > g0);
+                mma_state_update(b ? sQ : sK, b ? sP : sV, gc > g0);
                 mma_commit(mma_bar);
             }
-            wait_bar(mma_bar, mma_phase);
-            fence_after_sync();
-            if (t == 0 && gc + 1 < ur.end) load(h, c0 + L, false);
         }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
         if (q < D / 32) {  // rows d < D of S_ext, this warpgroup's columns
             float* out = p.agg + static_cast<size_t>(unit) * W;
             const int d = row;
@@ -311,7 +331,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_P, sdesc(sQ + off, 16, 1024), sdesc(sK + off, 16, 1024), ID_P,
                          k > 0 ? 1u : 0u);
             }
-            mma_state_update(true);
+            mma_state_update(sK, sV, true);
             mma_commit(mma_bar);
             tma_store_wait_read();  // the staging tile (P area) is free again
         }
