@@ -168,13 +168,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------- workloads
 
-def _bytes_fwd(B, H, N, D, M, esz):
-    return B * H * N * (2 * D + 2 * M) * esz  # read Q, K, V; write Out
+def _bytes_fwd(B, H, N, D, M, esz, den=False):
+    # read Q, K, V; write Out (+ the fp32 normaliser per token)
+    return B * H * N * ((2 * D + 2 * M) * esz + (4 if den else 0))
 
 
-def _bytes_bwd(B, H, N, D, M, esz, with_out=True):
-    # read Q, K, V, dOut (+ Out); write dQ, dK, dV
-    return B * H * N * (2 * D + 2 * M + (M if with_out else 0) + 2 * D + M) * esz
+def _bytes_bwd(B, H, N, D, M, esz, with_out=True, den=False):
+    # read Q, K, V, dOut (+ Out, + the fp32 normaliser per token); write dQ, dK, dV
+    return B * H * N * ((2 * D + 2 * M + (M if with_out else 0) + 2 * D + M) * esz + (4 if den else 0))
 
 
 def _bytes_decode(B, H, D, M, esz):
@@ -220,6 +221,7 @@ def run_ours(args):
     x = synth.qkv(B, H, N, D, M, w.dtype, seed, w.scale, with_grad=True, device="cuda")
     Q, K, V, G = x["Q"], x["K"], x["V"], x["G"]
     O = torch.empty_like(V)
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda")  # normaliser kept for the backward
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
 
     ev = []
@@ -228,10 +230,10 @@ def run_ours(args):
         if record:
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
-        la.la_forward_causal(Q, K, V, out=O)
+        la.la_forward_causal(Q, K, V, out=O, den=den)
         if record:
             e1.record(stream)
-        la.la_backward_causal(Q, K, V, G, Out=O, dQ=dQ, dK=dK, dV=dV)
+        la.la_backward_causal(Q, K, V, G, Out=O, dQ=dQ, dK=dK, dV=dV, Den=den)
         if record:
             e2.record(stream)
             ev.append((e0, e1, e2))
@@ -271,8 +273,8 @@ def run_ours(args):
     def e2e_step():
         for k in dx:
             dx[k].copy_(hx[k], non_blocking=True)
-        la.la_forward_causal(dx["Q"], dx["K"], dx["V"], out=O)
-        la.la_backward_causal(dx["Q"], dx["K"], dx["V"], dx["G"], Out=O, dQ=dQ, dK=dK, dV=dV)
+        la.la_forward_causal(dx["Q"], dx["K"], dx["V"], out=O, den=den)
+        la.la_backward_causal(dx["Q"], dx["K"], dx["V"], dx["G"], Out=O, dQ=dQ, dK=dK, dV=dV, Den=den)
         for h, d in zip(hout, (O, dQ, dK, dV)):
             h.copy_(d, non_blocking=True)
 
@@ -296,8 +298,8 @@ def run_ours(args):
     d2h = sum(h.numel() * h.element_size() for h in hout)
 
     esz = 2
-    fwd_bytes = _bytes_fwd(B, H, N, D, M, esz)
-    bwd_bytes = _bytes_bwd(B, H, N, D, M, esz, with_out=True)
+    fwd_bytes = _bytes_fwd(B, H, N, D, M, esz, den=True)
+    bwd_bytes = _bytes_bwd(B, H, N, D, M, esz, with_out=True, den=True)
     dom, dom_ms, dom_bytes = ("la_backward_causal", bwd_ms, bwd_bytes) if bwd_ms >= fwd_ms else \
         ("la_forward_causal", fwd_ms, fwd_bytes)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -323,7 +325,7 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": f"{HEADLINE}: causal linear attention fwd+bwd, B={B} H={H} "
                                    f"N={N} D=M={D}, bf16 storage, fp32 accumulation, "
-                                   "phi=elu+1, Out kept from the forward",
+                                   "phi=elu+1, Out and the normaliser kept from the forward",
                        "global_batch": B * world, "seq_len": N, "heads": H, "head_dim": D,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": "inputs larger than L2 (4 x 64 MiB resident per rank)"},

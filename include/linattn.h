@@ -65,14 +65,16 @@ typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
  *   Z_init  [B][H][D]    fp32, nullable (read)  must be NULL iff S_init is NULL
  *   S_final [B][H][D][M] fp32, nullable (written) state after token N-1
  *   Z_final [B][H][D]    fp32, nullable (written) must be NULL iff S_final is NULL
+ *   Den     [B][H][N]    fp32, nullable (written) the normaliser phi(Q_i).Z_i
+ *           of every token (the denominator of eq. output), for the backward
  * With S_init/Z_init a sequence can be processed in pieces; S_final/Z_final
  * hand a prefill's state to la_decode_step (section 三（二）: the state phi(K)V^T
- * is kept as an internal RNN state).  Out may not alias any input.
+ * is kept as an internal RNN state).  Out and Den may not alias any input.
  */
 la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out,
                             int B, int H, int N, int D, int M, la_dtype dtype,
                             const float* S_init, const float* Z_init,
-                            float* S_final, float* Z_final, void* stream);
+                            float* S_final, float* Z_final, float* Den, void* stream);
 
 /*
  * Causal backward of L(Out) given dOut = dL/dOut: the numerator gradients of
@@ -82,12 +84,17 @@ la_status la_forward_causal(const void* Q, const void* K, const void* V, void* O
  *   Q, K [B][H][N][D]; V, dOut [B][H][N][M] dtype        (read)
  *   Out  [B][H][N][M] dtype, nullable                    (read) the forward's
  *        output; when NULL it is recomputed.
+ *   Den  [B][H][N] fp32, nullable                        (read) the forward's
+ *        normaliser per token (la_forward_causal's Den, from the same inputs);
+ *        the bf16 D = M = 64 path then skips recomputing it, the other paths
+ *        ignore it.  The results agree within the bf16 tolerance either way.
  *   dQ, dK [B][H][N][D]; dV [B][H][N][M] dtype           (written)
  * Outputs may not alias inputs or each other.
  */
 la_status la_backward_causal(const void* Q, const void* K, const void* V, const void* Out,
                              const void* dOut, void* dQ, void* dK, void* dV,
-                             int B, int H, int N, int D, int M, la_dtype dtype, void* stream);
+                             int B, int H, int N, int D, int M, la_dtype dtype,
+                             const float* Den, void* stream);
 
 /*
  * Non-causal forward V' = phi(Q)(phi(K)^T V) / phi(Q) sum_j phi(K_j)

@@ -71,8 +71,11 @@ def _dtype(t):
 
 
 def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=False,
-                      stream=None):
-    """Causal forward.  Returns Out, or (Out, S_final, Z_final) with return_state."""
+                      den=None, stream=None):
+    """Causal forward.  Returns Out, or (Out, S_final, Z_final) with return_state.
+
+    den: optional fp32 [B, H, N] tensor that receives the normaliser
+    phi(Q_i).Z_i of every token, to hand to la_backward_causal(Den=...)."""
     B, H, N, D, M = _dims(Q, V)
     dev = Q.device
     for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
@@ -87,6 +90,10 @@ def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=
     if S_init is not None:
         _need(S_init, "S_init", torch.float32, dev)
         _need(Z_init, "Z_init", torch.float32, dev)
+    if den is not None:
+        _need(den, "den", torch.float32, dev)
+        if tuple(den.shape) != (B, H, N):
+            raise ValueError(f"den must be [B, H, N] = {(B, H, N)}, got {tuple(den.shape)}")
     S_f = Z_f = None
     if return_state:
         S_f = torch.empty((B, H, D, M), dtype=torch.float32, device=dev)
@@ -94,18 +101,24 @@ def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=
     with torch.cuda.device(dev):
         _check(_lib.la_forward_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D, M,
                                       _dtype(Q), _ptr(S_init), _ptr(Z_init), _ptr(S_f), _ptr(Z_f),
-                                      _stream_handle(stream)))
+                                      _ptr(den), _stream_handle(stream)))
     return (out, S_f, Z_f) if return_state else out
 
 
-def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, stream=None):
-    """Causal backward; returns (dQ, dK, dV).  Out (the forward output) is optional."""
+def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, Den=None,
+                       stream=None):
+    """Causal backward; returns (dQ, dK, dV).  Out (the forward output) and Den
+    (the forward's normaliser, fp32 [B, H, N]) are optional."""
     B, H, N, D, M = _dims(Q, V)
     dev = Q.device
     for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (dOut, "dOut")):
         _need(t, n, Q.dtype, dev)
     if Out is not None:
         _need(Out, "Out", Q.dtype, dev)
+    if Den is not None:
+        _need(Den, "Den", torch.float32, dev)
+        if tuple(Den.shape) != (B, H, N):
+            raise ValueError(f"Den must be [B, H, N] = {(B, H, N)}, got {tuple(Den.shape)}")
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -113,7 +126,7 @@ def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, strea
         _need(t, n, Q.dtype, dev)
     with torch.cuda.device(dev):
         _check(_lib.la_backward_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Out), _ptr(dOut), _ptr(dQ),
-                                       _ptr(dK), _ptr(dV), B, H, N, D, M, _dtype(Q),
+                                       _ptr(dK), _ptr(dV), B, H, N, D, M, _dtype(Q), _ptr(Den),
                                        _stream_handle(stream)))
     return dQ, dK, dV
 

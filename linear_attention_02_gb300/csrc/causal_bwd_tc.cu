@@ -91,6 +91,7 @@ struct BwdParams {
     unsigned* flags;      // [units]
     unsigned* ticket;
     float* gd;            // [BH][N]
+    const float* den;     // [BH][N] the forward's normaliser per token, or null (recomputed)
     unsigned* status;
 };
 
@@ -408,6 +409,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int unit = bars->unit;
     const UnitRange ur(unit, p.per, p.CH, p.BH);
     const int first_end = min(ur.end, (ur.hA + 1) * p.CH);  // end of the first piece
+    const bool have_den = p.den != nullptr;
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
@@ -527,6 +529,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const uint32_t u = static_cast<uint32_t>(gc - ur.start) >> 1;
         uint8_t* const tQ = sm + (b ? Lay::Q1 : Lay::Q0);
         const uint32_t sQ = smem_u32(tQ), sK = smem_u32(sm + (b ? Lay::K1 : Lay::K0));
+        const float den_in = have_den && row < valid ? __ldg(p.den + static_cast<size_t>(bh) * p.N + c0 + row) : 1.f;
         {   // this chunk's phi(Q), phi(K) from the transform warps and V, G, O by TMA
             bool bad = false;
             if (t == 0) {
@@ -545,20 +548,26 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             fence_after_sync();
         }
         if (t == 0) {
+            if (!have_den) {  // den = rowsum(tril(qf kf^T)) + qf . Z
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
-                mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
-                         ID_16_KMN, k > 0);
+                for (int k = 0; k < D / 16; ++k) {
+                    mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
+                    mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
+                             ID_16_KMN, k > 0);
+                }
+                mma_commit(mma_bar);
             }
-            mma_commit(mma_bar);
             mma_state_update(sK, sV, true);  // tracked by the next commit
-            tma_store_wait_read();       // staging and g tiles are free again
+            tma_store_wait_read();           // staging and g tiles are free again
         }
-        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
-        fence_after_sync();
+        if (have_den) {
+            bar_sync(kBarE, kBT);  // thread 0 has seen the g tile's last store read out
+        } else {
+            if (wait_bar(mma_bar, mma_phase)) goto cleanup;
+            fence_after_sync();
+        }
         {   // den, gn, gd -> g tile (bf16) and gd scratch
-            const float part = masked_half<false>(tm + lane + Lay::T_P, nullptr, row, q, g);
+            const float part = have_den ? 0.f : masked_half<false>(tm + lane + Lay::T_P, nullptr, row, q, g);
             float gv[32], ov[32];
             read_row32(sm + Lay::G, row, 4 * g, gv);
             read_row32(sm + Lay::O, row, 4 * g, ov);
@@ -567,10 +576,14 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             for (int e = 0; e < 32; ++e) go = fmaf(gv[e], ov[e], go);
             xch[g * 128 + row] = part;
             xch[256 + g * 128 + row] = go;
-            float dz[16];
-            tmem_ld16(tm + lane + Lay::T_DEN, dz);
+            float dz0 = 0.f;
+            if (!have_den) {
+                float dz[16];
+                tmem_ld16(tm + lane + Lay::T_DEN, dz);
+                dz0 = dz[0];
+            }
             bar_sync(kBarE, kBT);
-            const float den = xch[row] + xch[128 + row] + dz[0];
+            const float den = have_den ? den_in : xch[row] + xch[128 + row] + dz0;
             const float go_all = xch[256 + row] + xch[384 + row];
             const bool ok = row < valid;
             const float inv = ok ? 1.f / den : 0.f;
@@ -860,7 +873,7 @@ cleanup:
 cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                  const __nv_bfloat16* V, const __nv_bfloat16* O,
                                  const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
-                                 __nv_bfloat16* dV, int BH, int N) {
+                                 __nv_bfloat16* dV, int BH, int N, const float* Den) {
     using namespace tcb;
     auto kf = bwd_prefix_tc_kernel;
     auto kr = bwd_suffix_tc_kernel;
@@ -885,8 +898,10 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     const size_t gn_bytes = sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
     const size_t gd_bytes = sizeof(float) * static_cast<size_t>(BH) * N;
     const size_t o_bytes = O ? 0 : gn_bytes;
+    const size_t den_bytes = O ? 0 : gd_bytes;  // the recomputed forward's normaliser
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gn_bytes) + up(gd_bytes) + up(o_bytes);
+    const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gn_bytes) + up(gd_bytes) + up(o_bytes) +
+                         up(den_bytes);
     char* ws = nullptr;
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), total)) != cudaSuccess) return e;
     BwdParams p;
@@ -907,13 +922,17 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     p.gd = reinterpret_cast<float*>(q);
     q += up(gd_bytes);
     __nv_bfloat16* Ow = O ? nullptr : reinterpret_cast<__nv_bfloat16*>(q);
+    q += up(o_bytes);
+    float* Dw = O ? nullptr : reinterpret_cast<float*>(q);
+    p.den = Den;
     p.status = c.status_word;
     do {
         if (!O) {  // the output is needed for gd: recompute it
             if ((e = causal_forward_tc<64, 64>(c, Q, K, V, Ow, BH, N, nullptr, nullptr, nullptr,
-                                               nullptr)) != cudaSuccess)
+                                               nullptr, Den ? nullptr : Dw)) != cudaSuccess)
                 break;
             O = Ow;
+            if (!Den) p.den = Dw;
         }
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
         CUtensorMap mQ, mK, mV, mG, mO, mGn, mdQ, mdK, mdV;

@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kThreads)
 causal_forward_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                       T* __restrict__ O, const float* __restrict__ prefix,
                       const float* __restrict__ S_init, const float* __restrict__ Z_init,
-                      float* __restrict__ S_final, float* __restrict__ Z_final, int N, int spans,
-                      int span_len) {
+                      float* __restrict__ S_final, float* __restrict__ Z_final,
+                      float* __restrict__ Den, int N, int spans, int span_len) {
     using C = Cfg<D, M>;
     constexpr int L = C::L, DP = C::DP, MP = C::MP, LP = C::LP;
     extern __shared__ float smem[];
@@ -181,6 +181,8 @@ causal_forward_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T*
         __syncthreads();
         row_den<D, L>(dens, Ps, qs, Zs);
         __syncthreads();
+        if (Den)  // the normaliser, kept for the backward
+            for (int i = threadIdx.x; i < rows; i += kThreads) Den[(size_t)bh * N + c0 + i] = dens[i];
         {   // O_c = (P V_c + phi(Q_c) S_{c-1}) / den
             Frag<L, M> o;
             o.zero();
@@ -476,7 +478,7 @@ inline cudaError_t allow_smem(K kernel, size_t bytes) {
 template <typename T, int D, int M>
 cudaError_t causal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O, int BH,
                            int N, const float* S_init, const float* Z_init, float* S_final,
-                           float* Z_final) {
+                           float* Z_final, float* Den) {
     using namespace ffma;
     using C = Cfg<D, M>;
     int spans, span_len;
@@ -494,7 +496,7 @@ cudaError_t causal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* 
     }
     LA_TRY(allow_smem(causal_forward_kernel<T, D, M>, Smem<D, M>::fwd));
     causal_forward_kernel<T, D, M><<<dim3(BH, spans), kThreads, Smem<D, M>::fwd, c.stream>>>(
-        Q, K, V, O, agg, S_init, Z_init, S_final, Z_final, N, spans, span_len);
+        Q, K, V, O, agg, S_init, Z_init, S_final, Z_final, Den, N, spans, span_len);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (agg) scratch_free(c, agg);

@@ -90,6 +90,7 @@ struct FwdParams {
     const float* Z_init;   // [BH][D] or null
     float* S_final;        // [BH][D][M] or null
     float* Z_final;        // [BH][D] or null
+    float* den;            // [BH][N] or null: the normaliser of every token
     unsigned* status;      // device error word
 };
 
@@ -424,6 +425,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             float dv[16];
             tmem_ld16(tm + lane + Lay::T_O + M, dv);
             const float inv = 1.f / dv[0];
+            if (p.den && g == 0 && row < valid) p.den[static_cast<size_t>(h) * p.N + c0 + row] = dv[0];
             for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                 float v[32];
                 tmem_ld32(tm + lane + Lay::T_O + j0, v);
@@ -456,7 +458,7 @@ template <int D, int M>
 cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
                               const float* S_init, const float* Z_init, float* S_final,
-                              float* Z_final) {
+                              float* Z_final, float* Den) {
     using namespace tcf;
     using Lay = Layout<D, M>;
     const int chunks = (N + L - 1) / L;
@@ -495,6 +497,7 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     p.Z_init = Z_init;
     p.S_final = S_final;
     p.Z_final = Z_final;
+    p.den = Den;
     p.status = c.status_word;
     do {
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
@@ -513,10 +516,10 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
 template cudaError_t causal_forward_tc<64, 64>(const LaunchCtx&, const __nv_bfloat16*,
                                                const __nv_bfloat16*, const __nv_bfloat16*,
                                                __nv_bfloat16*, int, int, const float*, const float*,
-                                               float*, float*);
+                                               float*, float*, float*);
 template cudaError_t causal_forward_tc<128, 128>(const LaunchCtx&, const __nv_bfloat16*,
                                                  const __nv_bfloat16*, const __nv_bfloat16*,
                                                  __nv_bfloat16*, int, int, const float*,
-                                                 const float*, float*, float*);
+                                                 const float*, float*, float*, float*);
 
 }  // namespace la

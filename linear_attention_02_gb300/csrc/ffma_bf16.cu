@@ -6,7 +6,7 @@ namespace la {
 #define LA_INST(T, D, M)                                                                        \
     template cudaError_t causal_forward<T, D, M>(const LaunchCtx&, const T*, const T*, const T*, \
                                                  T*, int, int, const float*, const float*,     \
-                                                 float*, float*);                              \
+                                                 float*, float*, float*);                      \
     template cudaError_t causal_backward<T, D, M>(const LaunchCtx&, const T*, const T*,        \
                                                   const T*, const T*, const T*, T*, T*, T*,    \
                                                   int, int);                                   \

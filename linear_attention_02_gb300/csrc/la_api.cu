@@ -160,22 +160,24 @@ struct UseTensorCores<__nv_bfloat16, 128, 128> {
 struct FwdCausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
-                           int BH, int N, const float* Si, const float* Zi, float* Sf, float* Zf) {
+                           int BH, int N, const float* Si, const float* Zi, float* Sf, float* Zf,
+                           float* Den) {
         if constexpr (UseTensorCores<T, D, M>::value)
             return causal_forward_tc<D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N,
-                                           Si, Zi, Sf, Zf);
+                                           Si, Zi, Sf, Zf, Den);
         else
             return causal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N,
-                                           Si, Zi, Sf, Zf);
+                                           Si, Zi, Sf, Zf, Den);
     }
 };
 struct BwdCausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V,
-                           const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N) {
+                           const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N,
+                           const float* Den) {
         if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 64 && M == 64)
             return causal_backward_tc64(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
-                                        (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
+                                        (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N, Den);
         else
             return causal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V,
                                             (const T*)O, (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH,
@@ -238,7 +240,8 @@ extern "C" {
 
 la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out, int B, int H,
                             int N, int D, int M, la_dtype dtype, const float* S_init,
-                            const float* Z_init, float* S_final, float* Z_final, void* stream) {
+                            const float* Z_init, float* S_final, float* Z_final, float* Den,
+                            void* stream) {
     static const char* fn = "la_forward_causal";
     const void* p[] = {Q, K, V, Out};
     const char* nm[] = {"Q", "K", "V", "Out"};
@@ -250,32 +253,33 @@ la_status la_forward_causal(const void* Q, const void* K, const void* V, void* O
     if ((S_final == nullptr) != (Z_final == nullptr))
         return fail(LA_ERR_INVALID_ARG, "%s: S_final and Z_final must both be given or both NULL", fn);
     if ((s = check_optional(fn, S_init, "S_init")) || (s = check_optional(fn, Z_init, "Z_init")) ||
-        (s = check_optional(fn, S_final, "S_final")) || (s = check_optional(fn, Z_final, "Z_final")))
+        (s = check_optional(fn, S_final, "S_final")) || (s = check_optional(fn, Z_final, "Z_final")) ||
+        (s = check_optional(fn, Den, "Den")))
         return s;
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     const size_t bh = (size_t)B * H;
     if (empty) return finish(empty_forward_state(ctx.stream, bh, D, M, S_init, Z_init, S_final, Z_final), fn);
     return finish(dispatch<FwdCausal>(dtype, D, M, &ctx, Q, K, V, Out, (int)bh, N, S_init, Z_init,
-                                      S_final, Z_final),
+                                      S_final, Z_final, Den),
                   fn);
 }
 
 la_status la_backward_causal(const void* Q, const void* K, const void* V, const void* Out,
                              const void* dOut, void* dQ, void* dK, void* dV, int B, int H, int N,
-                             int D, int M, la_dtype dtype, void* stream) {
+                             int D, int M, la_dtype dtype, const float* Den, void* stream) {
     static const char* fn = "la_backward_causal";
     const void* p[] = {Q, K, V, dOut, dQ, dK, dV};
     const char* nm[] = {"Q", "K", "V", "dOut", "dQ", "dK", "dV"};
     bool empty = false;
     la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 7, &empty);
     if (s != LA_OK) return s;
-    if ((s = check_optional(fn, Out, "Out"))) return s;
+    if ((s = check_optional(fn, Out, "Out")) || (s = check_optional(fn, Den, "Den"))) return s;
     if (empty) return LA_OK;
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     return finish(dispatch<BwdCausal>(dtype, D, M, &ctx, Q, K, V, Out, dOut, dQ, dK, dV,
-                                      (int)((size_t)B * H), N),
+                                      (int)((size_t)B * H), N, Den),
                   fn);
 }
 

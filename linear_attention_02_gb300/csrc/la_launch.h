@@ -30,20 +30,21 @@ void scratch_free(const LaunchCtx& c, void* p);
 template <typename T, int D, int M>
 cudaError_t causal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O, int BH,
                            int N, const float* S_init, const float* Z_init, float* S_final,
-                           float* Z_final);
+                           float* Z_final, float* Den);
 
 // Tensor-core causal forward for bf16 storage with D = M in {64, 128}.
 template <int D, int M>
 cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
                               const float* S_init, const float* Z_init, float* S_final,
-                              float* Z_final);
+                              float* Z_final, float* Den);
 
-// Tensor-core causal backward for bf16 storage with D = M = 64.
+// Tensor-core causal backward for bf16 storage with D = M = 64; Den (the
+// forward's normaliser per token) may be null.
 cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                  const __nv_bfloat16* V, const __nv_bfloat16* O,
                                  const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
-                                 __nv_bfloat16* dV, int BH, int N);
+                                 __nv_bfloat16* dV, int BH, int N, const float* Den);
 
 template <typename T, int D, int M>
 cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,

@@ -57,7 +57,7 @@ def _load():
     lib.lao_default_threads.restype = I
     lib.lao_default_threads.argtypes = []
     lib.lao_causal_forward_quadratic.argtypes = [I, I, I, I, P, P, P, P]
-    lib.lao_causal_forward_recurrent.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, I]
+    lib.lao_causal_forward_recurrent.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, I]
     lib.lao_noncausal_forward_quadratic.argtypes = [I, I, I, I, P, P, P, P]
     lib.lao_noncausal_forward_assoc.argtypes = [I, I, I, I, P, P, P, P, P, P, I]
     lib.lao_causal_backward_cumsum.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I]
@@ -112,8 +112,9 @@ def causal_forward_quadratic(Q, K, V) -> np.ndarray:
     return O
 
 
-def causal_forward_recurrent(Q, K, V, S0=None, Z0=None, nthreads: int = 0):
-    """Returns (O, S_N, Z_N)."""
+def causal_forward_recurrent(Q, K, V, S0=None, Z0=None, nthreads: int = 0, return_den=False):
+    """Returns (O, S_N, Z_N), plus the per-token denominator phi(Q_t).Z_t
+    (shape [..., N]) with return_den."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     lead, nh, N = _heads(Q, Q.shape[-1])
     D, M = Q.shape[-1], V.shape[-1]
@@ -122,9 +123,10 @@ def causal_forward_recurrent(Q, K, V, S0=None, Z0=None, nthreads: int = 0):
     O = np.empty(lead + (N, M))
     S = np.empty(lead + (D, M))
     Z = np.empty(lead + (D,))
+    den = np.empty(lead + (N,)) if return_den else None
     _load().lao_causal_forward_recurrent(nh, N, D, M, _p(Q), _p(K), _p(V), _p(S0), _p(Z0),
-                                         _p(O), _p(S), _p(Z), int(nthreads))
-    return O, S, Z
+                                         _p(O), _p(S), _p(Z), _p(den), int(nthreads))
+    return (O, S, Z, den) if return_den else (O, S, Z)
 
 
 def noncausal_forward_quadratic(Q, K, V) -> np.ndarray:

@@ -136,11 +136,12 @@ void lao_noncausal_forward_quadratic(int nh, int N, int D, int M, const double* 
 typedef struct {
     int N, D, M;
     const double *Q, *K, *V, *S0, *Z0;
-    double *O, *S_out, *Z_out;
+    double *O, *S_out, *Z_out, *den_out;
 } rec_ctx;
 
 /* Section 三: S_t = S_{t-1} + phi(K_t) V_t^T, Z_t = Z_{t-1} + phi(K_t), then
- * eq. output V'_t = phi(Q_t)^T S_t / phi(Q_t)^T Z_t. */
+ * eq. output V'_t = phi(Q_t)^T S_t / phi(Q_t)^T Z_t; the denominator
+ * phi(Q_t)^T Z_t is also returned per token when den_out is given. */
 static void recurrent_head(int h, void* p) {
     rec_ctx* c = (rec_ctx*)p;
     const int N = c->N, D = c->D, M = c->M;
@@ -163,6 +164,7 @@ static void recurrent_head(int h, void* p) {
         }
         for (int d = 0; d < D; ++d) qf[d] = lao_phi(Qh[(size_t)t * D + d]);
         double den = dot(qf, Z, D);
+        if (c->den_out) c->den_out[(size_t)h * N + t] = den;
         for (int e = 0; e < M; ++e) {
             double num = 0.0;
             for (int d = 0; d < D; ++d) num += qf[d] * S[(size_t)d * M + e];
@@ -180,8 +182,8 @@ static void recurrent_head(int h, void* p) {
 void lao_causal_forward_recurrent(int nh, int N, int D, int M, const double* Q,
                                   const double* K, const double* V,
                                   const double* S0, const double* Z0, double* O,
-                                  double* S_out, double* Z_out, int nthreads) {
-    rec_ctx c = {N, D, M, Q, K, V, S0, Z0, O, S_out, Z_out};
+                                  double* S_out, double* Z_out, double* den_out, int nthreads) {
+    rec_ctx c = {N, D, M, Q, K, V, S0, Z0, O, S_out, Z_out, den_out};
     for_heads(nh, nthreads, recurrent_head, &c);
 }
 

@@ -37,11 +37,12 @@ void lao_causal_forward_quadratic(int nh, int N, int D, int M, const double* Q,
                                   const double* K, const double* V, double* O);
 
 /* Causal forward, recurrent S/Z form.  S0/Z0 (nullable) give the state before
- * the first token; S_out/Z_out (nullable) receive the state after the last. */
+ * the first token; S_out/Z_out (nullable) receive the state after the last;
+ * den_out (nullable, [nh][N]) the denominator phi(Q_t)^T Z_t of every token. */
 void lao_causal_forward_recurrent(int nh, int N, int D, int M, const double* Q,
                                   const double* K, const double* V,
                                   const double* S0, const double* Z0, double* O,
-                                  double* S_out, double* Z_out, int nthreads);
+                                  double* S_out, double* Z_out, double* den_out, int nthreads);
 
 /* Non-causal forward, quadratic form (sums over all j). */
 void lao_noncausal_forward_quadratic(int nh, int N, int D, int M, const double* Q,

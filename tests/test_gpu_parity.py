@@ -59,12 +59,14 @@ def test_causal_forward_small(dt, shape):
     B, H, N, D, M = shape
     x = synth.qkv(B, H, N, D, M, dt, seed=11 + N)
     g = _dev(x)
-    O, S, Z = la.la_forward_causal(g["Q"], g["K"], g["V"], return_state=True)
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    O, S, Z = la.la_forward_causal(g["Q"], g["K"], g["V"], return_state=True, den=den)
     torch.cuda.synchronize()
-    Ro, Rs, Rz = oracle.causal_forward_recurrent(x["Q"], x["K"], x["V"])
+    Ro, Rs, Rz, Rd = oracle.causal_forward_recurrent(x["Q"], x["K"], x["V"], return_den=True)
     assert rel_err(O, Ro) <= TOL[dt]
     assert rel_err(S, Rs) <= TOL[dt]
     assert rel_err(Z, Rz) <= TOL[dt]
+    assert rel_err(den, Rd) <= TOL[dt]
 
 
 # The tensor-core kernels cut the chunks of all heads (head-major) into equal
@@ -83,14 +85,16 @@ def test_causal_forward_bf16_span_shapes(shape):
     B, H, N, D, M = shape
     x = synth.qkv(B, H, N, D, M, "bf16", seed=13 + N)
     g = _dev(x)
-    O, S, Z = la.la_forward_causal(g["Q"], g["K"], g["V"], return_state=True)
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    O, S, Z = la.la_forward_causal(g["Q"], g["K"], g["V"], return_state=True, den=den)
     la.la_check_device_status()
     idx = list(range(min(B * H, 6)))
     hs = [x[n].reshape(B * H, N, -1)[idx] for n in ("Q", "K", "V")]
-    Ro, Rs, Rz = oracle.causal_forward_recurrent(*hs)
+    Ro, Rs, Rz, Rd = oracle.causal_forward_recurrent(*hs, return_den=True)
     assert rel_err(O.reshape(B * H, N, M)[idx], Ro) <= TOL["bf16"]
     assert rel_err(S.reshape(B * H, D, M)[idx], Rs) <= TOL["bf16"]
     assert rel_err(Z.reshape(B * H, D)[idx], Rz) <= TOL["bf16"]
+    assert rel_err(den.reshape(B * H, N)[idx], Rd) <= TOL["bf16"]
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -115,16 +119,25 @@ def test_causal_forward_carried_state_and_empty(dt):
     assert torch.equal(Se, Sb) and torch.equal(Ze, Zb)
 
 
+def _saved(la, g, saved):
+    """The forward's outputs handed to the backward: none, Out, or Out and den."""
+    if saved == "none":
+        return None, None
+    B, H, N, _ = g["Q"].shape
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda") if saved == "out+den" else None
+    return la.la_forward_causal(g["Q"], g["K"], g["V"], den=den), den
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", [s for s in SMALL if s[2] > 1])
-@pytest.mark.parametrize("pass_out", [True, False])
-def test_causal_backward_small(dt, shape, pass_out):
+@pytest.mark.parametrize("saved", ["out", "none", "out+den"])
+def test_causal_backward_small(dt, shape, saved):
     la = _la()
     B, H, N, D, M = shape
     x = synth.qkv(B, H, N, D, M, dt, seed=21 + N, with_grad=True)
     g = _dev(x)
-    O = la.la_forward_causal(g["Q"], g["K"], g["V"]) if pass_out else None
-    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O)
+    O, den = _saved(la, g, saved)
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den)
     torch.cuda.synchronize()
     RdQ, RdK, RdV = oracle.causal_backward_cumsum(x["Q"], x["K"], x["V"], x["G"])
     assert rel_err(dQ, RdQ) <= TOL[dt]
@@ -139,14 +152,14 @@ def test_causal_backward_small(dt, shape, pass_out):
     (1, 1, 128, 64, 64),
     (2, 3, 8300, 64, 64),     # several chunks per range, ranges crossing heads, ragged last chunk
 ])
-@pytest.mark.parametrize("pass_out", [True, False])
-def test_causal_backward_bf16_span_shapes(shape, pass_out):
+@pytest.mark.parametrize("saved", ["out", "none", "out+den"])
+def test_causal_backward_bf16_span_shapes(shape, saved):
     la = _la()
     B, H, N, D, M = shape
     x = synth.qkv(B, H, N, D, M, "bf16", seed=23 + N, with_grad=True)
     g = _dev(x)
-    O = la.la_forward_causal(g["Q"], g["K"], g["V"]) if pass_out else None
-    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O)
+    O, den = _saved(la, g, saved)
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den)
     la.la_check_device_status()
     idx = list(range(min(B * H, 6)))
     hs = [x[n].reshape(B * H, N, -1)[idx] for n in ("Q", "K", "V", "G")]
@@ -267,14 +280,18 @@ def test_full_causal_train_bf16():
     w = synth.WORKLOADS["causal_train_bf16"]
     x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, with_grad=True)
     g = _dev(x)
-    O = la.la_forward_causal(g["Q"], g["K"], g["V"])
-    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O)
+    # the training step as the bench runs it: the forward keeps Out and the
+    # normaliser, the backward takes both
+    den = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    O = la.la_forward_causal(g["Q"], g["K"], g["V"], den=den)
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den)
     torch.cuda.synchronize()
     idx = _sample_heads(w.B * w.H)
     hs = [_heads(x[n], idx) for n in ("Q", "K", "V", "G")]
-    Ro = oracle.causal_forward_recurrent(*hs[:3])[0]
+    Ro, _, _, Rd = oracle.causal_forward_recurrent(*hs[:3], return_den=True)
     RdQ, RdK, RdV = oracle.causal_backward_cumsum(*hs)
     assert rel_err(_heads(O, idx), Ro) <= TOL[w.dtype]
+    assert rel_err(_heads(den, idx), Rd) <= TOL[w.dtype]
     assert rel_err(_heads(dQ, idx), RdQ) <= TOL[w.dtype]
     assert rel_err(_heads(dK, idx), RdK) <= TOL[w.dtype]
     assert rel_err(_heads(dV, idx), RdV) <= TOL[w.dtype]

@@ -95,10 +95,11 @@ def test_golden_forward_causal_both_forms():
     Q, K, V = (np.array(g[k], float) for k in ("Q", "K", "V"))
     want = _arr(g["causal_O"])
     np.testing.assert_allclose(oracle.causal_forward_quadratic(Q, K, V), want, rtol=1e-14)
-    O, S, Z = oracle.causal_forward_recurrent(Q, K, V)
+    O, S, Z, den = oracle.causal_forward_recurrent(Q, K, V, return_den=True)
     np.testing.assert_allclose(O, want, rtol=1e-14)
     np.testing.assert_allclose(S, _arr(g["S_total"]), rtol=1e-14)
     np.testing.assert_allclose(Z, _arr(g["Z_total"]), rtol=1e-14)
+    np.testing.assert_allclose(den, _arr(g["causal_den"]), rtol=1e-14)
     # the state after two tokens
     _, S2, Z2 = oracle.causal_forward_recurrent(Q[:2], K[:2], V[:2])
     np.testing.assert_allclose(S2, _arr(g["S_after_2"]), rtol=1e-14)
