@@ -100,8 +100,6 @@ constexpr uint32_t ID_NE_MNMN = idesc_bf16(128, NE, true, true);  // state updat
 constexpr uint32_t ID_16_KMN = idesc_bf16(128, 16, false, true);  // qf . [Z block]
 constexpr uint32_t ID_D_KK = idesc_bf16(128, D, false, false);
 constexpr uint32_t ID_D_KMN = idesc_bf16(128, D, false, true);
-constexpr uint32_t ID_D_MNMN = idesc_bf16(128, D, true, true);
-constexpr uint32_t ID_M_MNMN = idesc_bf16(128, M, true, true);
 constexpr uint32_t ID_M_KMN = idesc_bf16(128, M, false, true);
 
 // K-major descriptor for K step k of a tile whose 64-column atoms are `atom` bytes apart.
@@ -157,6 +155,50 @@ __device__ __forceinline__ float masked_half(uint32_t taddr, uint8_t* tile, int 
     }
     return sum;
 }
+
+// The same masking for the A operand of an MMA reading tensor memory: the
+// warpgroup's 64 columns of row i are rounded to bf16 and packed in pairs back
+// into the first 32 of those columns (each warp rewrites only its own lanes and
+// only columns it has already read), so K step k of the product sits at column
+// 8k + 32 (k >= 4).
+__device__ __forceinline__ void masked_half_to_tmem(uint32_t taddr, int i, int q, int g) {
+    const int j0 = 64 * g;
+    uint32_t pk[32];
+    if (j0 > 32 * q + 31) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) pk[u] = 0u;
+    } else {
+        float v[64];
+        tmem_ld64(taddr + j0, v);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int j = j0 + 2 * u;
+            pk[u] = pack_bf16(j <= i ? v[2 * u] : 0.f, j + 1 <= i ? v[2 * u + 1] : 0.f);
+        }
+    }
+    tmem_st32u(taddr + j0, pk);
+}
+// Transposed form: row j of a TMEM block holding X^T (columns i), masked to
+// i >= j and packed in place like masked_half_to_tmem.
+__device__ __forceinline__ void masked_half_t_to_tmem(uint32_t taddr, int j, int q, int g) {
+    const int i0 = 64 * g;
+    uint32_t pk[32];
+    if (i0 + 63 < 32 * q) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) pk[u] = 0u;
+    } else {
+        float v[64];
+        tmem_ld64(taddr + i0, v);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int i = i0 + 2 * u;
+            pk[u] = pack_bf16(i >= j ? v[2 * u] : 0.f, i + 1 >= j ? v[2 * u + 1] : 0.f);
+        }
+    }
+    tmem_st32u(taddr + i0, pk);
+}
+// TMEM column of K step k of an A operand packed by masked_half_to_tmem.
+__device__ __forceinline__ uint32_t packed_a_col(int k) { return 8 * k + (k >= 4 ? 32 : 0); }
 
 // This warpgroup's 32 columns of a 64-column TMEM row -> bf16 tile row, times
 // phi'(x) = min(phi, 1) taken from `phi_tile` when given.
@@ -266,42 +308,88 @@ __device__ __forceinline__ void publish_half(uint32_t taddr, float* out, int d, 
     }
 }
 
-constexpr int kTW = 4;                    // transform warps (8 .. 11, one per scheduler)
+// CTA roles: warps 0 .. 7 compute (epilogues, one TMEM lane quarter and column
+// half each), warp 8 issues every MMA, TMA copy and store (lane 0) and hands
+// work to and from the compute warps, warps 9 .. 11 transform (load Q and K
+// of the next chunk, apply phi; one on each scheduler the MMA warp leaves).  Because no compute thread issues MMAs, the
+// MMAs that no epilogue waits for run underneath the epilogues.
+constexpr int kMW = kBT / 32;             // the MMA warp
+constexpr int kTW = 3;                    // transform warps
 constexpr int kTT = 32 * kTW;             // their threads
-constexpr int kCT = kBT + kTT;            // threads per CTA
-constexpr uint32_t kBarE = 1, kBarT = 2;  // named barriers of the compute and transform warps
+constexpr int kT0 = kBT + 32;             // first transform thread
+constexpr int kCT = kT0 + kTT;            // threads per CTA
+constexpr int kEM = kBT + 32;             // compute warps + MMA warp
+// Named barriers: compute warps among themselves; transform warps; compute ->
+// MMA warp hand-overs (compute warps arrive, the MMA warp waits); MMA warp ->
+// compute hand-overs (the MMA warp arrives, the compute warps wait).  Each
+// side meets each hand-over barrier alternately with the other side, so no
+// arrival can fall into the previous use.
+constexpr uint32_t kBarE = 3, kBarT = 2, kBarEM = 1, kBarME = 4;
 
-// Hand-over among the compute warps: their shared-memory writes become
-// visible to the tensor core and TMA, and tcgen05 work is ordered around it.
+// Hand-over among the compute warps when they issue MMAs themselves (phase 1):
+// their shared-memory writes become visible to the tensor core and TMA, and
+// tcgen05 work is ordered around it.
 __device__ __forceinline__ void sync_tc() {
     fence_proxy_async();
     fence_before_sync();
     bar_sync(kBarE, kBT);
     fence_after_sync();
 }
+// Compute warps -> MMA warp: their shared-memory and TMEM writes are done.
+__device__ __forceinline__ void hand_to_mma() {
+    fence_proxy_async();
+    fence_before_sync();
+    bar_arrive(kBarEM, kEM);
+}
+__device__ __forceinline__ void take_from_compute() {
+    bar_sync(kBarEM, kEM);
+    fence_after_sync();
+}
+// MMA warp -> compute warps: the tiles it waited for are in, the buffers free.
+__device__ __forceinline__ void hand_to_compute() {
+    fence_before_sync();
+    bar_arrive(kBarME, kEM);
+}
+__device__ __forceinline__ void take_from_mma() {
+    bar_sync(kBarME, kEM);
+    fence_after_sync();
+}
 
 // Barriers and flags at the end of shared memory.
 struct Bars {
-    uint64_t tma, mma;   // compute warps' own copies; MMA completion
+    uint64_t tma, mma;   // copies of the MMA warp (and of phase 1); MMA completion
     uint64_t full[2];    // Q, K copies of buffer b landed
     uint64_t ready[2];   // phi(Q), phi(K) of buffer b are in place
-    uint64_t freeb[2];   // the compute warps are done with buffer b
+    uint64_t freeb[2];   // the chunk using buffer b is done with it
+    uint64_t rbar;       // completion of each chunk's last MMAs (R update included)
     uint32_t tmem, pad;
-    int unit, abort_e, abort_t, pad2;
+    int unit, broken, pad2, pad3;
 };
 static_assert(sizeof(Bars) <= 128, "barrier block");
 
+// One thread's bounded wait for the phase of `bar` with the given parity.  A
+// timeout sets the error word and marks the CTA broken; from then on every wait
+// is short and the kernel runs its hand-over protocol to the end with the
+// remaining work unguarded, so no thread is left waiting at a named barrier.
+__device__ __forceinline__ void poll(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* status) {
+    volatile int* broken = &bars->broken;
+    if (!mbar_wait(bar, parity, *broken ? 64u : kWaitLimit)) {
+        atomicOr(status, kErrWait);
+        *broken = 1;
+    }
+}
+
 // Transform warps: for each global chunk of the unit's range [start, end) in
 // processing order (reversed for the suffix kernel), load Q and K into buffer
-// (i & 1) once the compute warps have released it, apply phi (zeroing K's
-// rows past the end of the head) and hand the pair over.  Gives up when the
-// compute warps have given up.
+// (i & 1) once the chunk before it in that buffer has released it, apply phi
+// (zeroing K's rows past the end of the head) and hand the pair over.
 __device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                                  uint8_t* q0, uint8_t* q1, uint8_t* k0, uint8_t* k1,
                                                  Bars* bars, int start, int end, int CH, int N,
                                                  bool reverse, unsigned* status) {
-    const int tt = threadIdx.x - kBT;
-    const volatile int* abort_e = &bars->abort_e;
+    const int tt = threadIdx.x - kT0;
+    const volatile int* broken = &bars->broken;
+    int pend[2] = {-1, -1};  // parity of a copy into buffer b not seen to land (thread tt == 0)
     for (int i = 0; i < end - start; ++i) {
         const int gc = reverse ? end - 1 - i : start + i;
         const int bh = gc / CH;
@@ -310,24 +398,15 @@ __device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const C
         const uint32_t u = static_cast<uint32_t>(i) >> 1;
         uint8_t* const tq = b ? q1 : q0;
         uint8_t* const tk = b ? k1 : k0;
-        bool bad = false;
         if (tt == 0) {
-            const int r = i >= 2 ? mbar_wait_or(&bars->freeb[b], (u - 1) & 1u, kWaitLimit, abort_e) : 0;
-            if (r == 0) {
-                mbar_arrive_expect_tx(&bars->full[b], 2 * kAtom);
-                tma_load_3d(tq, tmQ, &bars->full[b], 0, c0, bh);
-                tma_load_3d(tk, tmK, &bars->full[b], 0, c0, bh);
-                if (!mbar_wait(&bars->full[b], u & 1u, kWaitLimit)) {
-                    atomicOr(status, kErrWait);
-                    bad = true;
-                }
-            } else {
-                if (r == 2) atomicOr(status, kErrWait);
-                bad = true;
-            }
-            if (bad) *reinterpret_cast<volatile int*>(&bars->abort_t) = 1;
+            if (i >= 2) poll(&bars->freeb[b], (u - 1) & 1u, bars, status);
+            mbar_arrive_expect_tx(&bars->full[b], 2 * kAtom);
+            tma_load_3d(tq, tmQ, &bars->full[b], 0, c0, bh);
+            tma_load_3d(tk, tmK, &bars->full[b], 0, c0, bh);
+            poll(&bars->full[b], u & 1u, bars, status);
+            pend[b] = *broken ? static_cast<int>(u & 1u) : -1;
         }
-        if (bar_sync_or(kBarT, kTT, bad)) return;
+        bar_sync(kBarT, kTT);
         const int valid = min(L, N - c0);
         phi_atom<false, kTT>(tq, valid, tt);
         phi_atom<true, kTT>(tk, valid, tt);
@@ -335,27 +414,33 @@ __device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const C
         bar_sync(kBarT, kTT);
         if (tt == 0) mbar_arrive(&bars->ready[b]);
     }
+    if (tt == 0)  // copies not seen to land: wait for them before the CTA exits
+        for (int b = 0; b < 2; ++b)
+            if (pend[b] >= 0) mbar_wait(&bars->full[b], static_cast<uint32_t>(pend[b]), kWaitLimit);
 }
 
-// Per-thread bookkeeping of the compute warps' own TMA loads (thread 0): the
-// bytes expected on the pending phase of `tma` but not issued yet, so that a
-// kernel giving up early can still drain the copies it started.
+// Bookkeeping of one thread's TMA loads on `tma`: how many phases it has
+// opened, and the bytes expected on the open one but not issued yet, so that a
+// kernel ending early can still drain the copies it started.
 struct TmaBook {
     bool pending = false;
     uint32_t missing = 0;
+    uint32_t count = 0;  // phases opened on the barrier so far (by any thread, in order)
     __device__ void expect(uint64_t* bar, uint32_t bytes) {
         mbar_arrive_expect_tx(bar, bytes);
         pending = true;
         missing = bytes;
+        ++count;
     }
     __device__ void load(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
         tma_load_3d(dst, map, bar, x, y, z);
         missing -= kAtom;
     }
-    __device__ void drain(uint64_t* bar, uint32_t parity) {
+    __device__ void drain(uint64_t* bar) {
         if (!pending) return;
         if (missing) mbar_complete_tx(bar, missing);
-        mbar_wait(bar, parity, kWaitLimit);
+        mbar_wait(bar, (count - 1) & 1u, kWaitLimit);
+        pending = false;
     }
 };
 
@@ -375,22 +460,20 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         return;
     }
     Bars* bars = reinterpret_cast<Bars*>(sm + Lay::BARS);
-    volatile int* abort_e = &bars->abort_e;
-    const volatile int* abort_t = &bars->abort_t;
     uint64_t* tma_bar = &bars->tma;
     uint64_t* mma_bar = &bars->mma;
     float* xch = reinterpret_cast<float*>(sm + Lay::XCH);  // [2 sums][2 warpgroups][128 rows]
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
+        mbar_init(&bars->rbar, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->full[b], 1);
             mbar_init(&bars->ready[b], 1);
             mbar_init(&bars->freeb[b], 1);
         }
         fence_mbar_init();
-        bars->abort_e = 0;
-        bars->abort_t = 0;
+        bars->broken = 0;
     }
     if (warp == 0) {
         tmem_alloc(&bars->tmem, Lay::T_COLS);
@@ -410,23 +493,13 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const UnitRange ur(unit, p.per, p.CH, p.BH);
     const int first_end = min(ur.end, (ur.hA + 1) * p.CH);  // end of the first piece
     const bool have_den = p.den != nullptr;
+    const int g0 = max(ur.start, ur.hB * p.CH);           // phase 1 covers [g0, end) when publishing
+    const uint32_t n1 = ur.publish ? static_cast<uint32_t>(ur.end - g0) : 0u;  // its chunks
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
-    const uint32_t sP = smem_u32(sm + Lay::P), sS = smem_u32(sm + Lay::S);
-    uint32_t tma_phase = 0, mma_phase = 0;
-    TmaBook book;
+    const uint32_t sS = smem_u32(sm + Lay::S);
+    TmaBook book;  // thread 0 (phase 1) or the MMA warp's lane 0 (phase 2)
 
-    // Compute warps: waits by thread 0, the outcome shared at the barrier.
-    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) -> bool {  // true: give up
-        bool bad = false;
-        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) {
-            atomicOr(p.status, kErrWait);
-            *abort_e = 1;
-            bad = true;
-        }
-        phase ^= 1u;
-        return bar_sync_or(kBarE, kBT, bad);
-    };
     // S_ext (+)= kf^T [V | 1] from K at sK and V at sv (a ones atom right after it)
     auto mma_state_update = [&](uint32_t sK, uint32_t sv, bool accumulate_first) {
 #pragma unroll
@@ -439,8 +512,18 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // Phase 1 alternates K and V between (K0, V) and (K1, G) -- a ones atom written into O,
     // right after G -- so the next chunk's copy overlaps this chunk's phi and MMA.
     auto prelude = [&]() -> bool {  // false: give up
+        uint32_t tma_phase = 0, mma_phase = 0;
+        auto wait_bar = [&](uint64_t* bar, uint32_t& phase) -> bool {  // true: give up
+            bool bad = false;
+            if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) {
+                atomicOr(p.status, kErrWait);
+                bad = true;
+            }
+            phase ^= 1u;
+            return bar_sync_or(kBarE, kBT, bad);
+        };
         if (ur.publish) {
-            const int h = ur.hB, g0 = max(ur.start, h * p.CH);
+            const int h = ur.hB;
             auto load_kv = [&](int c0, int b) {  // thread 0 only
                 book.expect(tma_bar, 2 * kAtom);
                 book.load(sm + (b ? Lay::K1 : Lay::K0), &tmK, tma_bar, 0, c0, h);
@@ -484,7 +567,6 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 while (ld_acquire(p.flags + sp) == 0u) {
                     if (++n > kSpinLimit) {
                         atomicOr(p.status, kErrLookback);
-                        *abort_e = 1;
                         bad = true;
                         break;
                     }
@@ -501,164 +583,192 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         sync_tc();
         return true;
     };
-    const bool bad_pre = warp < kBT / 32 && !prelude();
+    const bool bad_pre = warp < kMW && !prelude();
     if (__syncthreads_or(bad_pre)) goto cleanup;
 
-    if (warp >= kBT / 32) {  // transform warps
+    // --------------------------------------------------- phase 2: dQ, gn, gd
+    if (warp > kMW) {  // transform warps
         transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars,
                          ur.start, ur.end, p.CH, p.N, false, p.status);
-        goto cleanup;
-    }
-
-    // ------------------------------------------ phase 2: dQ, gn, gd (compute warps)
-    if (t == 0) {  // V, G, O of the first chunk; Q and K come from the transform warps
-        const int c0 = (ur.start - ur.hA * p.CH) * L;
-        book.expect(tma_bar, 3 * kAtom);
-        book.load(sm + Lay::V, &tmV, tma_bar, 0, c0, ur.hA);
-        book.load(sm + Lay::G, &tmG, tma_bar, 0, c0, ur.hA);
-        book.load(sm + Lay::O, &tmO, tma_bar, 0, c0, ur.hA);
-    }
-    for (int gc = ur.start; gc < ur.end; ++gc) {
-        const int bh = gc / p.CH, cc = gc - bh * p.CH;
-        const int c0 = cc * L;
-        const int valid = min(L, p.N - c0);
-        const int hn = (gc + 1) / p.CH, cn0 = (gc + 1 - hn * p.CH) * L;  // the next chunk
-        const bool more = gc + 1 < ur.end;
-        const bool in_first = gc < first_end;  // this chunk's qf^T g enters the published R share
-        const int b = (gc - ur.start) & 1;
-        const uint32_t u = static_cast<uint32_t>(gc - ur.start) >> 1;
-        uint8_t* const tQ = sm + (b ? Lay::Q1 : Lay::Q0);
-        const uint32_t sQ = smem_u32(tQ), sK = smem_u32(sm + (b ? Lay::K1 : Lay::K0));
-        const float den_in = have_den && row < valid ? __ldg(p.den + static_cast<size_t>(bh) * p.N + c0 + row) : 1.f;
-        {   // this chunk's phi(Q), phi(K) from the transform warps and V, G, O by TMA
-            bool bad = false;
-            if (t == 0) {
-                const int r = mbar_wait_or(&bars->ready[b], u & 1u, kWaitLimit, abort_t);
-                if (r == 0 && mbar_wait(tma_bar, tma_phase, kWaitLimit)) {
-                    tma_phase ^= 1u;
-                    book.pending = false;
-                    if (more) book.expect(tma_bar, 3 * kAtom);  // the next chunk's V, G, O
-                } else {
-                    if (r != 1) atomicOr(p.status, kErrWait);
-                    *abort_e = 1;
-                    bad = true;
-                }
-            }
-            if (bar_sync_or(kBarE, kBT, bad)) goto cleanup;
-            fence_after_sync();
+    } else if (warp == kMW) {  // MMA warp: lane 0 issues, the warp meets the hand-overs
+        const bool lead = (t & 31) == 0;
+        uint32_t tma_phase = n1 & 1u;  // phase 1 completed n1 phases of each barrier
+        uint32_t ncommit = n1;         // commits to mma_bar so far
+        uint32_t r_phase = 0;
+        book.count = n1;
+        if (lead) {  // V, G, O of the first chunk; Q and K come from the transform warps
+            const int c0 = (ur.start - ur.hA * p.CH) * L;
+            book.expect(tma_bar, 3 * kAtom);
+            book.load(sm + Lay::V, &tmV, tma_bar, 0, c0, ur.hA);
+            book.load(sm + Lay::G, &tmG, tma_bar, 0, c0, ur.hA);
+            book.load(sm + Lay::O, &tmO, tma_bar, 0, c0, ur.hA);
         }
-        if (t == 0) {
-            if (!have_den) {  // den = rowsum(tril(qf kf^T)) + qf . Z
+        for (int gc = ur.start; gc < ur.end; ++gc) {
+            const int bh = gc / p.CH, c0 = (gc - bh * p.CH) * L;
+            const int hn = (gc + 1) / p.CH, cn0 = (gc + 1 - hn * p.CH) * L;  // the next chunk
+            const bool more = gc + 1 < ur.end;
+            const bool in_first = gc < first_end;          // qf^T g enters the published R share
+            const bool publish_here = gc == first_end - 1;  // the share is read out after this chunk
+            const int b = (gc - ur.start) & 1;
+            const uint32_t u = static_cast<uint32_t>(gc - ur.start) >> 1;
+            const uint32_t sQ = smem_u32(sm + (b ? Lay::Q1 : Lay::Q0));
+            const uint32_t sK = smem_u32(sm + (b ? Lay::K1 : Lay::K0));
+            auto mma_r = [&]() {  // the first piece's share of R: qf^T g
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
-                    mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
-                             ID_16_KMN, k > 0);
-                }
-                mma_commit(mma_bar);
-            }
-            mma_state_update(sK, sV, true);  // tracked by the next commit
-            tma_store_wait_read();           // staging and g tiles are free again
-        }
-        if (have_den) {
-            bar_sync(kBarE, kBT);  // thread 0 has seen the g tile's last store read out
-        } else {
-            if (wait_bar(mma_bar, mma_phase)) goto cleanup;
-            fence_after_sync();
-        }
-        {   // den, gn, gd -> g tile (bf16) and gd scratch
-            const float part = have_den ? 0.f : masked_half<false>(tm + lane + Lay::T_P, nullptr, row, q, g);
-            float gv[32], ov[32];
-            read_row32(sm + Lay::G, row, 4 * g, gv);
-            read_row32(sm + Lay::O, row, 4 * g, ov);
-            float go = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) go = fmaf(gv[e], ov[e], go);
-            xch[g * 128 + row] = part;
-            xch[256 + g * 128 + row] = go;
-            float dz0 = 0.f;
-            if (!have_den) {
-                float dz[16];
-                tmem_ld16(tm + lane + Lay::T_DEN, dz);
-                dz0 = dz[0];
-            }
-            bar_sync(kBarE, kBT);
-            const float den = have_den ? den_in : xch[row] + xch[128 + row] + dz0;
-            const float go_all = xch[256 + row] + xch[384 + row];
-            const bool ok = row < valid;
-            const float inv = ok ? 1.f / den : 0.f;
-            const float gd = -go_all * inv;
-            uint32_t pk[16];
-#pragma unroll
-            for (int u2 = 0; u2 < 16; ++u2) pk[u2] = pack_bf16(gv[2 * u2] * inv, gv[2 * u2 + 1] * inv);
-            store_row32(sm + Lay::GH, kAtom, row, 32 * g, pk);
-            if (g == 0) {
-                *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
-                    make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-                if (ok) p.gd[static_cast<size_t>(bh) * p.N + c0 + row] = gd;
-            }
-        }
-        sync_tc();
-        if (t == 0) {
-            if (more) {  // G and O are consumed
-                book.load(sm + Lay::G, &tmG, tma_bar, 0, cn0, hn);
-                book.load(sm + Lay::O, &tmO, tma_bar, 0, cn0, hn);
-            }
-            tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
-            tma_store_commit();
-#pragma unroll
-            for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T  (the P block of TMEM is free again)
-                mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
-            mma_commit(mma_bar);
-#pragma unroll
-            for (int k = 0; k < NE / 16; ++k)  // dqf = g [S | Z]^T
-                mma_bf16(tm + Lay::T_DQ, kmaj(sGh, k, kAtom), kmaj(sS, k, S_ATOM), ID_D_KK, k > 0);
-            if (in_first) {
-#pragma unroll
-                for (int k = 0; k < L / 16; ++k)  // the first piece's share of R: qf^T g
+                for (int k = 0; k < L / 16; ++k)
                     mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN,
                              (gc > ur.start || k > 0) ? 1u : 0u);
+            };
+            if (lead) {
+                poll(tma_bar, tma_phase, bars, p.status);  // V, G, O
+                tma_phase ^= 1u;
+                book.pending = false;
+                if (more) book.expect(tma_bar, 3 * kAtom);
+                if (gc > ur.start) {  // the previous chunk's MMAs are all done: its Q, K are free
+                    poll(&bars->rbar, r_phase, bars, p.status);
+                    r_phase ^= 1u;
+                    mbar_arrive(&bars->freeb[b ^ 1]);
+                }
+                tma_store_wait_read_but_last();  // the g tile is read out (the dQ store may go on)
+            }
+            __syncwarp();
+            hand_to_compute();  // G, O in; the g tile free: the compute warps start on gn, gd
+            if (lead) {
+                poll(&bars->ready[b], u & 1u, bars, p.status);  // phi(Q), phi(K)
+                fence_after_sync();
+                if (!have_den) {  // den = rowsum(tril(qf kf^T)) + qf . Z
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
+                        mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
+                                 ID_16_KMN, k > 0);
+                    }
+                    mma_commit(mma_bar);
+                    ++ncommit;
+                }
+                mma_state_update(sK, sV, true);  // S_c, read by the compute warps after the dP commit
+            }
+            __syncwarp();
+            take_from_compute();  // the g tile (gn | gd) is written
+            if (lead) {
+                if (more) {  // G and O are consumed
+                    book.load(sm + Lay::G, &tmG, tma_bar, 0, cn0, hn);
+                    book.load(sm + Lay::O, &tmO, tma_bar, 0, cn0, hn);
+                }
+                tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
+                tma_store_commit();
+#pragma unroll
+                for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
+                    mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
+                mma_commit(mma_bar);
+                const uint32_t dp_commit = ncommit++;
+#pragma unroll
+                for (int k = 0; k < NE / 16; ++k)  // dqf = g [S | Z]^T
+                    mma_bf16(tm + Lay::T_DQ, kmaj(sGh, k, kAtom), kmaj(sS, k, S_ATOM), ID_D_KK, k > 0);
+                if (publish_here) mma_r();  // covered by the next commit: read out after this chunk
+                poll(mma_bar, dp_commit & 1u, bars, p.status);  // V is consumed (S update, dP)
+                if (more) book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
+            }
+            __syncwarp();
+            take_from_compute();  // dP is masked and packed in TMEM
+            if (lead) {
+                tma_store_wait_read_but_last();  // the previous dQ store is read out: the staging
+                                                 // tile is free once this chunk's MMA3 commits
+#pragma unroll
+                for (int k = 0; k < L / 16; ++k)  // dqf += dP kf, dP read from TMEM
+                    mma_bf16_ts(tm + Lay::T_DQ, tm + Lay::T_P + packed_a_col(k), mnmaj(sK, k, kAtom),
+                                ID_D_KMN, 1u);
+                mma_commit(mma_bar);
+                ++ncommit;
+                if (in_first && !publish_here) mma_r();  // under the dQ epilogue
+                mma_commit(&bars->rbar);
+            }
+            __syncwarp();
+            take_from_compute();  // dQ staged, S_c copied
+            if (lead) {
+                tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
+                tma_store_commit();
             }
         }
-        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
-        fence_after_sync();
-        if (t == 0 && more) book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);  // V consumed
-        masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);  // dP, masked, bf16
-        sync_tc();
-        if (t == 0) {
+        if (lead) poll(&bars->rbar, r_phase, bars, p.status);  // the last chunk's MMAs
+    } else {  // compute warps
+        uint32_t e_commit = n1;  // commits to mma_bar waited for so far
+        auto wait_mma = [&]() {
+            if (t == 0) poll(mma_bar, e_commit & 1u, bars, p.status);
+            ++e_commit;
+            bar_sync(kBarE, kBT);
+            fence_after_sync();
+        };
+        for (int gc = ur.start; gc < ur.end; ++gc) {
+            const int bh = gc / p.CH, cc = gc - bh * p.CH;
+            const int c0 = cc * L;
+            const int valid = min(L, p.N - c0);
+            const bool next_head = gc + 1 < ur.end && cc == p.CH - 1;  // the next chunk starts a head
+            const int b = (gc - ur.start) & 1;
+            uint8_t* const tQ = sm + (b ? Lay::Q1 : Lay::Q0);
+            const float den_in =
+                have_den && row < valid ? __ldg(p.den + static_cast<size_t>(bh) * p.N + c0 + row) : 1.f;
+            take_from_mma();
+            if (!have_den) wait_mma();
+            {   // den, gn, gd -> g tile (bf16) and gd scratch
+                const float part = have_den ? 0.f : masked_half<false>(tm + lane + Lay::T_P, nullptr, row, q, g);
+                float gv[32], ov[32];
+                read_row32(sm + Lay::G, row, 4 * g, gv);
+                read_row32(sm + Lay::O, row, 4 * g, ov);
+                float go = 0.f;
 #pragma unroll
-            for (int k = 0; k < L / 16; ++k)  // dqf += dP kf
-                mma_bf16(tm + Lay::T_DQ, kmaj(sP, k, kAtom), mnmaj(sK, k, kAtom), ID_D_KMN, 1u);
-            mma_commit(mma_bar);
-        }
-        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
-        fence_after_sync();
-        if (q < D / 32) {
-            if (gc == first_end - 1)  // the first piece is complete: publish its share of R
-                publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
-            if (more && hn != bh) {  // the next chunk starts a head: zero state
-                float zero[32];
+                for (int e = 0; e < 32; ++e) go = fmaf(gv[e], ov[e], go);
+                xch[g * 128 + row] = part;
+                xch[256 + g * 128 + row] = go;
+                float dz0 = 0.f;
+                if (!have_den) {
+                    float dz[16];
+                    tmem_ld16(tm + lane + Lay::T_DEN, dz);
+                    dz0 = dz[0];
+                }
+                bar_sync(kBarE, kBT);
+                const float den = have_den ? den_in : xch[row] + xch[128 + row] + dz0;
+                const float go_all = xch[256 + row] + xch[384 + row];
+                const bool ok = row < valid;
+                const float inv = ok ? 1.f / den : 0.f;
+                const float gd = -go_all * inv;
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) zero[e] = 0.f;
-                put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, zero, 0.f, 0.f);
-            } else {
-                state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
+                for (int u2 = 0; u2 < 16; ++u2) pk[u2] = pack_bf16(gv[2 * u2] * inv, gv[2 * u2 + 1] * inv);
+                store_row32(sm + Lay::GH, kAtom, row, 32 * g, pk);
+                if (g == 0) {
+                    *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
+                        make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                    if (ok) p.gd[static_cast<size_t>(bh) * p.N + c0 + row] = gd;
+                }
             }
-        }
-        tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);  // dQ
-        sync_tc();
-        if (t == 0) {
-            tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
-            tma_store_commit();
-            mbar_arrive(&bars->freeb[b]);  // this chunk's Q and K buffers
+            hand_to_mma();
+            wait_mma();  // dP (and the S update before it)
+            masked_half_to_tmem(tm + lane + Lay::T_P, row, q, g);  // dP, masked, bf16 in TMEM
+            hand_to_mma();
+            wait_mma();  // dqf complete
+            if (q < D / 32) {
+                if (gc == first_end - 1)  // the first piece is complete: publish its share of R
+                    publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
+                if (next_head) {  // the next chunk starts a head: zero state
+                    float zero[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) zero[e] = 0.f;
+                    put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, zero, 0.f, 0.f);
+                } else {
+                    state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
+                }
+            }
+            tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);  // dQ
+            hand_to_mma();
         }
     }
 
 cleanup:
-    if (t == 0) {
-        book.drain(tma_bar, tma_phase);
+    if (t == 0 || t == 32 * kMW) {  // phase 1's or the MMA warp's copies and stores
+        book.drain(tma_bar);
         tma_store_wait_all();
     }
     fence_before_sync();
@@ -682,21 +792,19 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         return;
     }
     Bars* bars = reinterpret_cast<Bars*>(sm + Lay::BARS);
-    volatile int* abort_e = &bars->abort_e;
-    const volatile int* abort_t = &bars->abort_t;
     uint64_t* tma_bar = &bars->tma;
     uint64_t* mma_bar = &bars->mma;
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
+        mbar_init(&bars->rbar, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->full[b], 1);
             mbar_init(&bars->ready[b], 1);
             mbar_init(&bars->freeb[b], 1);
         }
         fence_mbar_init();
-        bars->abort_e = 0;
-        bars->abort_t = 0;
+        bars->broken = 0;
     }
     if (warp == 0) {
         tmem_alloc(&bars->tmem, Lay::T_COLS);
@@ -714,153 +822,165 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const UnitRange ur(unit, p.per, p.CH, p.BH);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
-    const uint32_t sP = smem_u32(sm + Lay::P), sDP = smem_u32(sm + Lay::DP);
     const uint32_t sR = smem_u32(sm + Lay::R);
-    uint32_t tma_phase = 0, mma_phase = 0;
-    TmaBook book;
-    float gd_next = 0.f;
+    TmaBook book;  // the MMA warp's lane 0
 
-    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) -> bool {  // true: give up
-        bool bad = false;
-        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) {
-            atomicOr(p.status, kErrWait);
-            *abort_e = 1;
-            bad = true;
-        }
-        phase ^= 1u;
-        return bar_sync_or(kBarE, kBT, bad);
-    };
-    // gd of rows 0 .. 127 of global chunk gc (zero past the end of its head)
-    auto gd_rows = [&](int gc) {
-        const int h = gc / p.CH, c0 = (gc - h * p.CH) * L;
-        return row < p.N - c0 ? __ldcg(p.gd + static_cast<size_t>(h) * p.N + c0 + row) : 0.f;
-    };
-
-    if (warp < kBT / 32) {
+    if (warp < kMW) {
         if (q < D / 32) {  // R, r after the last piece: the first-piece shares of the later units
             float vals[32];
             const int sp0 = ur.publish ? unit + 1 : 0, sp1 = ur.publish ? ur.u_last + 1 : 0;
             const float r = sum_states(p.ragg, sp0, sp1, row, g, vals);
             put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, vals, r, 0.f);
         }
-        if (g == 0) gd_next = gd_rows(ur.end - 1);
-        if (t == 0) {  // V and g of the first chunk; Q and K come from the transform warps
+        fence_proxy_async();
+        fence_before_sync();
+    }
+    __syncthreads();
+    fence_after_sync();
+
+    if (warp > kMW) {  // transform warps
+        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars,
+                         ur.start, ur.end, p.CH, p.N, true, p.status);
+    } else if (warp == kMW) {  // MMA warp: lane 0 issues, the warp writes gd and meets the hand-overs
+        const int ln = t & 31;
+        const bool lead = ln == 0;
+        uint32_t tma_phase = 0, r_phase = 0;
+        // gd of rows 4 ln .. 4 ln + 3 of global chunk gc (zero past the end of its head)
+        auto gd_rows = [&](int gc, float (&v)[4]) {
+            const int h = gc / p.CH, c0 = (gc - h * p.CH) * L;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * ln + r;
+                v[r] = i < p.N - c0 ? __ldcg(p.gd + static_cast<size_t>(h) * p.N + c0 + i) : 0.f;
+            }
+        };
+        float gdn[4];
+        gd_rows(ur.end - 1, gdn);
+        if (lead) {  // V and g of the first chunk; Q and K come from the transform warps
             const int c0 = (ur.end - 1 - ur.hB * p.CH) * L;
             book.expect(tma_bar, 2 * kAtom);
             book.load(sm + Lay::V, &tmV, tma_bar, 0, c0, ur.hB);
             book.load(sm + Lay::GH, &tmGn, tma_bar, 0, c0, ur.hB);
         }
-        sync_tc();
-    }
-    __syncthreads();
-    if (warp >= kBT / 32) {  // transform warps
-        transform_chunks(&tmQ, &tmK, sm + Lay::Q0, sm + Lay::Q1, sm + Lay::K0, sm + Lay::K1, bars,
-                         ur.start, ur.end, p.CH, p.N, true, p.status);
-        goto cleanup;
-    }
-
-    for (int gc = ur.end - 1; gc >= ur.start; --gc) {
-        const int bh = gc / p.CH, cc = gc - bh * p.CH;
-        const int c0 = cc * L;
-        const bool more = gc > ur.start;
-        const int hn = (gc - 1) / p.CH, cn0 = (gc - 1 - hn * p.CH) * L;  // the next chunk (if more)
-        const int i = ur.end - 1 - gc;
-        const int b = i & 1;
-        const uint32_t u = static_cast<uint32_t>(i) >> 1;
-        uint8_t* const tK = sm + (b ? Lay::K1 : Lay::K0);
-        const uint32_t sQ = smem_u32(sm + (b ? Lay::Q1 : Lay::Q0)), sK = smem_u32(tK);
-        if (g == 0) {  // gd into the extension atom of the g tile (zero for padding rows)
-            const float gd = gd_next;
-            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 0)) =
-                make_uint4(pack_bf16(gd, 0.f), 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
-            if (more) gd_next = gd_rows(gc - 1);
+        for (int gc = ur.end - 1; gc >= ur.start; --gc) {
+            const int bh = gc / p.CH, cc = gc - bh * p.CH;
+            const int c0 = cc * L;
+            const bool more = gc > ur.start;
+            const int hn = (gc - 1) / p.CH, cn0 = (gc - 1 - hn * p.CH) * L;  // the next chunk (if more)
+            const int i = ur.end - 1 - gc;
+            const int b = i & 1;
+            const uint32_t u = static_cast<uint32_t>(i) >> 1;
+            const uint32_t sQ = smem_u32(sm + (b ? Lay::Q1 : Lay::Q0));
+            const uint32_t sK = smem_u32(sm + (b ? Lay::K1 : Lay::K0));
+            // gd into the extension atom of the g tile (the previous chunk's MMAs are done)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int rr = 4 * ln + r;
+                *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(rr, 0)) =
+                    make_uint4(pack_bf16(gdn[r], 0.f), 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(rr, 1)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (more) gd_rows(gc - 1, gdn);
             fence_proxy_async();
-        }
-        {   // this chunk's phi(Q), phi(K) from the transform warps and V, g by TMA
-            bool bad = false;
-            if (t == 0) {
-                const int r = mbar_wait_or(&bars->ready[b], u & 1u, kWaitLimit, abort_t);
-                if (r == 0 && mbar_wait(tma_bar, tma_phase, kWaitLimit)) {
-                    tma_phase ^= 1u;
-                    book.pending = false;
-                    if (more) book.expect(tma_bar, 2 * kAtom);  // the next chunk's V, g
-                } else {
-                    if (r != 1) atomicOr(p.status, kErrWait);
-                    *abort_e = 1;
-                    bad = true;
+            __syncwarp();
+            if (lead) {
+                poll(&bars->ready[b], u & 1u, bars, p.status);  // phi(Q), phi(K)
+                poll(tma_bar, tma_phase, bars, p.status);       // V, gn
+                tma_phase ^= 1u;
+                book.pending = false;
+                if (more) book.expect(tma_bar, 2 * kAtom);
+                if (i > 0) mbar_arrive(&bars->freeb[b ^ 1]);  // the previous chunk's Q, K
+                fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)  // P^T = kf qf^T
+                    mma_bf16(tm + Lay::T_P, kmaj(sK, k, kAtom), kmaj(sQ, k, kAtom), ID_P, k > 0);
+#pragma unroll
+                for (int k = 0; k < NE / 16; ++k)  // dP^T = [V | 1] g^T
+                    mma_bf16(tm + Lay::T_DP, kmaj(sV, k, kAtom), kmaj(sGh, k, kAtom), ID_P, k > 0);
+                mma_commit(mma_bar);
+            }
+            __syncwarp();
+            hand_to_compute();
+            take_from_compute();  // P^T and dP^T are masked and packed in TMEM
+            if (lead) {
+                tma_store_wait_read();  // the staging tiles are read out before dV, dK commit
+#pragma unroll
+                for (int k = 0; k < L / 16; ++k)  // dV = P^T gn, P^T read from TMEM
+                    mma_bf16_ts(tm + Lay::T_DV, tm + Lay::T_P + packed_a_col(k), mnmaj(sGh, k, kAtom),
+                                ID_M_KMN, k > 0);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)  // dV += kf R
+                    mma_bf16(tm + Lay::T_DV, kmaj(sK, k, kAtom), mnmaj(sR, k, S_ATOM), ID_M_KMN, 1u);
+                mma_commit(mma_bar);
+#pragma unroll
+                for (int k = 0; k < L / 16; ++k)  // dkf = dP^T qf, dP^T read from TMEM
+                    mma_bf16_ts(tm + Lay::T_DK, tm + Lay::T_DP + packed_a_col(k), mnmaj(sQ, k, kAtom),
+                                ID_D_KMN, k > 0);
+#pragma unroll
+                for (int k = 0; k < NE / 16; ++k)  // dkf += [V | 1] [R | r]^T
+                    mma_bf16(tm + Lay::T_DK, kmaj(sV, k, kAtom), kmaj(sR, k, S_ATOM), ID_D_KK, 1u);
+                mma_commit(mma_bar);
+                if (cc > 0) {  // R += qf^T g (not needed before a head's first chunk)
+#pragma unroll
+                    for (int k = 0; k < L / 16; ++k)
+                        mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN, 1u);
+                }
+                mma_commit(&bars->rbar);
+                poll(&bars->rbar, r_phase, bars, p.status);  // V and g are consumed
+                r_phase ^= 1u;
+                if (more) {
+                    book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
+                    book.load(sm + Lay::GH, &tmGn, tma_bar, 0, cn0, hn);
                 }
             }
-            if (bar_sync_or(kBarE, kBT, bad)) goto cleanup;
+            __syncwarp();
+            take_from_compute();  // dK, dV staged, R_c copied
+            if (lead) {
+                tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
+                tma_store_3d(&tmdV, sm + Lay::DP, 0, c0, bh);
+                tma_store_commit();
+            }
+        }
+    } else {  // compute warps
+        uint32_t e_commit = 0, e_r = 0;
+        auto wait_on = [&](uint64_t* bar, uint32_t& n) {
+            if (t == 0) poll(bar, n & 1u, bars, p.status);
+            ++n;
+            bar_sync(kBarE, kBT);
             fence_after_sync();
-        }
-        if (t == 0) {
+        };
+        for (int gc = ur.end - 1; gc >= ur.start; --gc) {
+            const int bh = gc / p.CH, cc = gc - bh * p.CH;
+            const bool more = gc > ur.start;
+            const int b = (ur.end - 1 - gc) & 1;
+            uint8_t* const tK = sm + (b ? Lay::K1 : Lay::K0);
+            (void)bh;
+            take_from_mma();
+            wait_on(mma_bar, e_commit);  // P^T, dP^T
+            masked_half_t_to_tmem(tm + lane + Lay::T_P, row, q, g);   // P^T, masked, bf16 in TMEM
+            masked_half_t_to_tmem(tm + lane + Lay::T_DP, row, q, g);  // dP^T likewise
+            hand_to_mma();
+            wait_on(mma_bar, e_commit);  // dV
+            tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);  // dV
+            wait_on(mma_bar, e_commit);  // dkf
+            tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, tK);        // dK
+            wait_on(&bars->rbar, e_r);   // R_c
+            if (q < D / 32) {
+                if (cc > 0) {
+                    state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
+                } else if (more) {  // the next chunk ends the previous head: R starts from zero
+                    float zero[32];
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)  // P = qf kf^T
-                mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
-#pragma unroll
-            for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
-                mma_bf16(tm + Lay::T_DP, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
-            mma_commit(mma_bar);
-            // R += qf^T g: the R tile already holds R after chunk gc + 1, so the TMEM sum can
-            // move on now; tracked by the next commit, not needed before a head's first chunk
-            if (cc > 0) {
-#pragma unroll
-                for (int k = 0; k < L / 16; ++k)
-                    mma_bf16(tm + Lay::T_R, mnmaj(sQ, k, kAtom), mnmaj(sGh, k, kAtom), ID_NE_MNMN, 1u);
+                    for (int e = 0; e < 32; ++e) zero[e] = 0.f;
+                    put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, zero, 0.f, 0.f);
+                }
             }
-            tma_store_wait_read();  // the staging tiles (P, dP areas) are free again
-        }
-        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
-        fence_after_sync();
-        masked_half<true>(tm + lane + Lay::T_P, sm + Lay::P, row, q, g);
-        masked_half<true>(tm + lane + Lay::T_DP, sm + Lay::DP, row, q, g);
-        sync_tc();
-        if (t == 0) {
-#pragma unroll
-            for (int k = 0; k < L / 16; ++k)  // dV = P^T gn
-                mma_bf16(tm + Lay::T_DV, mnmaj(sP, k, kAtom), mnmaj(sGh, k, kAtom), ID_M_MNMN, k > 0);
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k)  // dV += kf R
-                mma_bf16(tm + Lay::T_DV, kmaj(sK, k, kAtom), mnmaj(sR, k, S_ATOM), ID_M_KMN, 1u);
-#pragma unroll
-            for (int k = 0; k < L / 16; ++k)  // dkf = dP^T qf
-                mma_bf16(tm + Lay::T_DK, mnmaj(sDP, k, kAtom), mnmaj(sQ, k, kAtom), ID_D_MNMN, k > 0);
-#pragma unroll
-            for (int k = 0; k < NE / 16; ++k)  // dkf += [V | 1] [R | r]^T
-                mma_bf16(tm + Lay::T_DK, kmaj(sV, k, kAtom), kmaj(sR, k, S_ATOM), ID_D_KK, 1u);
-            mma_commit(mma_bar);
-        }
-        if (wait_bar(mma_bar, mma_phase)) goto cleanup;
-        fence_after_sync();
-        if (t == 0 && more) {  // V and g are consumed (the R update included)
-            book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
-            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, cn0, hn);
-        }
-        if (q < D / 32) {
-            if (cc > 0) {
-                state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
-            } else if (more) {  // the next chunk ends the previous head: R starts from zero
-                float zero[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) zero[e] = 0.f;
-                put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, zero, 0.f, 0.f);
-            }
-        }
-        tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, tK);        // dK
-        tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);  // dV
-        sync_tc();
-        if (t == 0) {
-            tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
-            tma_store_3d(&tmdV, sm + Lay::DP, 0, c0, bh);
-            tma_store_commit();
-            mbar_arrive(&bars->freeb[b]);  // this chunk's Q and K buffers
+            hand_to_mma();
         }
     }
 
-cleanup:
-    if (t == 0) {
-        book.drain(tma_bar, tma_phase);
+    if (t == 32 * kMW) {  // the MMA warp's copies and stores
+        book.drain(tma_bar);
         tma_store_wait_all();
     }
     fence_before_sync();

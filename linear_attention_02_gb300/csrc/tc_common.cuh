@@ -102,15 +102,19 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int atoms, int valid) {
     }
 }
 
-// phi_tile for one atom, worked by NT threads numbered `tid` = 0 .. NT - 1.
+// phi_tile for one atom, worked by NT threads numbered `tid` = 0 .. NT - 1
+// (NT need not divide the atom's 1024 chunks).
 template <bool ZERO_TAIL, int NT>
 __device__ __forceinline__ void phi_atom(uint8_t* tile, int valid, int tid) {
     constexpr int U = 1024 / NT < 8 ? 1024 / NT : 8;
+    constexpr bool EXACT = 1024 % (NT * U) == 0;
 #pragma unroll 1
     for (int base = tid; base < 1024; base += NT * U) {
         uint4 u[U];
 #pragma unroll
-        for (int j = 0; j < U; ++j) u[j] = *reinterpret_cast<const uint4*>(tile + (base + j * NT) * 16);
+        for (int j = 0; j < U; ++j)
+            if (EXACT || base + j * NT < 1024)
+                u[j] = *reinterpret_cast<const uint4*>(tile + (base + j * NT) * 16);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             if (ZERO_TAIL && ((base + j * NT) >> 3) >= valid) {
@@ -123,7 +127,9 @@ __device__ __forceinline__ void phi_atom(uint8_t* tile, int valid, int tid) {
             }
         }
 #pragma unroll
-        for (int j = 0; j < U; ++j) *reinterpret_cast<uint4*>(tile + (base + j * NT) * 16) = u[j];
+        for (int j = 0; j < U; ++j)
+            if (EXACT || base + j * NT < 1024)
+                *reinterpret_cast<uint4*>(tile + (base + j * NT) * 16) = u[j];
     }
 }
 
