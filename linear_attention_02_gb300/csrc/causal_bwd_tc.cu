@@ -49,22 +49,30 @@ constexpr uint32_t S_ATOM = D * 128;   // one atom column of a D-row state tile
 
 // prefix-kernel shared memory.  An MN-major operand of D = 64 rows is read by
 // an M = 128 MMA as two atoms (the second one's rows land in accumulator lanes
-// nobody reads), so the atom after each Q and K buffer must be allocated.
+// nobody reads), so the atom after each Q and K buffer must be allocated.  The
+// bf16 state [S | Z] sits right under V and the ones atom: read K-major, the
+// 192 rows [V ; S] (K columns 0 .. 63) and [1 ; Z] (columns 64 .. 79) are one
+// B operand, so dP = g [V | 1]^T and dqf = g [S | Z]^T are one N = 192 product.
 struct LayF {
     static constexpr uint32_t Q0 = 0, Q1 = kAtom, K0 = 2 * kAtom, K1 = 3 * kAtom;  // two buffers each
-    static constexpr uint32_t V = 4 * kAtom, ONES = 5 * kAtom;
-    static constexpr uint32_t G = 6 * kAtom, O = 7 * kAtom;
-    static constexpr uint32_t GH = 8 * kAtom;    // [gn | gd 0..0]: gn atom + extension atom
-    static constexpr uint32_t P = 10 * kAtom;    // dP (bf16), then the dQ staging tile
-    static constexpr uint32_t S = 12 * kAtom;    // [S | Z] bf16, 2 atoms of D rows
-    static constexpr uint32_t XCH = S + 2 * S_ATOM;  // 2 x [2][128] fp32 partial row sums
+    static constexpr uint32_t V = 4 * kAtom;
+    static constexpr uint32_t S_LO = V + kAtom;          // S: D rows x M columns (one S atom)
+    static constexpr uint32_t ONES = S_LO + S_ATOM;      // the ones atom
+    static constexpr uint32_t S_HI = ONES + kAtom;       // Z (and 15 copies): D rows
+    static constexpr uint32_t VS_K = ONES - V;           // K-atom stride of the [V ; S] operand
+    static constexpr uint32_t G = S_HI + S_ATOM, O = G + kAtom;
+    static constexpr uint32_t GH = O + kAtom;            // [gn | gd 0..0]: gn atom + extension atom
+    static constexpr uint32_t P = GH + 2 * kAtom;        // the dQ staging tile
+    static constexpr uint32_t XCH = P + kAtom;           // 2 x [2][128] fp32 partial row sums
     static constexpr uint32_t BARS = XCH + 2048;
     static constexpr uint32_t BYTES = BARS + 128;
-    static constexpr uint32_t T_P = 0, T_DEN = 128, T_DQ = 160, T_S = 224, T_R = 304;
+    static constexpr uint32_t T_P = 0, T_DQ = 128, T_DEN = 192, T_S = 224, T_R = 304;
     static constexpr uint32_t T_COLS = 512;
 };
 static_assert(LayF::K1 + 2 * kAtom <= LayF::BYTES && LayF::Q1 + kAtom == LayF::K0, "padding atoms");
-static_assert(LayF::ONES == LayF::V + kAtom && LayF::O == LayF::G + kAtom, "[V | 1] is two adjacent atoms");
+static_assert(LayF::S_HI - LayF::S_LO == LayF::VS_K && LayF::O == LayF::G + kAtom, "operand layout");
+static_assert(LayF::G % 1024 == 0 && LayF::ONES % 1024 == 0 && LayF::S_HI % 1024 == 0, "alignment");
+static_assert(LayF::T_DQ == LayF::T_P + 128, "dP and dqf are one accumulator block");
 
 constexpr int kBT = 256;  // two warpgroups: warp w reads TMEM lanes 32 (w % 4) ..., and the
                           // two warps of a lane quarter split the columns of every row
@@ -96,6 +104,7 @@ struct BwdParams {
 };
 
 constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);     // K-major x K-major
+constexpr uint32_t ID_PQ = idesc_bf16(128, 128 + D, false, false);  // [dP | dqf]
 constexpr uint32_t ID_NE_MNMN = idesc_bf16(128, NE, true, true);  // state updates
 constexpr uint32_t ID_16_KMN = idesc_bf16(128, 16, false, true);  // qf . [Z block]
 constexpr uint32_t ID_D_KK = idesc_bf16(128, D, false, false);
@@ -220,7 +229,8 @@ __device__ __forceinline__ void tmem_half_to_tile(uint32_t taddr, uint8_t* tile,
 
 // State row d: this warpgroup's 32 of the M columns (and, for g == 0, the 16
 // extension columns) from TMEM -> bf16 state tile [D rows].
-__device__ __forceinline__ void state_half_to_tile(uint32_t taddr, uint8_t* tile, int d, int g) {
+__device__ __forceinline__ void state_half_to_tile(uint32_t taddr, uint8_t* tile, int d, int g,
+                                                   uint32_t hi_off = S_ATOM) {
     float v[32];
     tmem_ld32(taddr + 32 * g, v);
     uint32_t pk[16];
@@ -233,8 +243,8 @@ __device__ __forceinline__ void state_half_to_tile(uint32_t taddr, uint8_t* tile
         uint32_t zk[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) zk[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
-        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(zk[0], zk[1], zk[2], zk[3]);
-        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(zk[4], zk[5], zk[6], zk[7]);
+        *reinterpret_cast<uint4*>(tile + hi_off + swz(d, 0)) = make_uint4(zk[0], zk[1], zk[2], zk[3]);
+        *reinterpret_cast<uint4*>(tile + hi_off + swz(d, 1)) = make_uint4(zk[4], zk[5], zk[6], zk[7]);
     }
 }
 
@@ -242,7 +252,8 @@ __device__ __forceinline__ void state_half_to_tile(uint32_t taddr, uint8_t* tile
 // state tile; g == 0 also writes the extension columns (`ext`, then
 // `ext_rest` fifteen times).
 __device__ __forceinline__ void put_state_half(uint32_t taddr, uint8_t* tile, int d, int g,
-                                               const float (&vals)[32], float ext, float ext_rest) {
+                                               const float (&vals)[32], float ext, float ext_rest,
+                                               uint32_t hi_off = S_ATOM) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         float v[16];
@@ -264,8 +275,8 @@ __device__ __forceinline__ void put_state_half(uint32_t taddr, uint8_t* tile, in
         for (int u = 1; u < 16; ++u) e[u] = ext_rest;
         tmem_st16(taddr + M, e);
         const uint32_t e0 = pack_bf16(ext, ext_rest), er = pack_bf16(ext_rest, ext_rest);
-        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 0)) = make_uint4(e0, er, er, er);
-        *reinterpret_cast<uint4*>(tile + S_ATOM + swz(d, 1)) = make_uint4(er, er, er, er);
+        *reinterpret_cast<uint4*>(tile + hi_off + swz(d, 0)) = make_uint4(e0, er, er, er);
+        *reinterpret_cast<uint4*>(tile + hi_off + swz(d, 1)) = make_uint4(er, er, er, er);
     }
 }
 
@@ -497,14 +508,14 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t n1 = ur.publish ? static_cast<uint32_t>(ur.end - g0) : 0u;  // its chunks
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
-    const uint32_t sS = smem_u32(sm + Lay::S);
+    const uint32_t sSh = smem_u32(sm + Lay::S_HI);
     TmaBook book;  // thread 0 (phase 1) or the MMA warp's lane 0 (phase 2)
 
-    // S_ext (+)= kf^T [V | 1] from K at sK and V at sv (a ones atom right after it)
-    auto mma_state_update = [&](uint32_t sK, uint32_t sv, bool accumulate_first) {
+    // S_ext (+)= kf^T [V | 1] from K at sK and V at sv, its ones atom lbo bytes after it
+    auto mma_state_update = [&](uint32_t sK, uint32_t sv, uint32_t lbo, bool accumulate_first) {
 #pragma unroll
         for (int k = 0; k < L / 16; ++k)
-            mma_bf16(tm + Lay::T_S, mnmaj(sK, k, kAtom), mnmaj(sv, k, kAtom), ID_NE_MNMN,
+            mma_bf16(tm + Lay::T_S, mnmaj(sK, k, kAtom), mnmaj(sv, k, lbo), ID_NE_MNMN,
                      (accumulate_first || k > 0) ? 1u : 0u);
     };
 
@@ -548,7 +559,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 sync_tc();
                 if (t == 0) {
                     mma_state_update(smem_u32(sm + (b ? Lay::K1 : Lay::K0)), b ? smem_u32(sm + Lay::G) : sV,
-                                     gc > g0);
+                                     b ? kAtom : Lay::VS_K, gc > g0);
                     mma_commit(mma_bar);
                 }
             }
@@ -578,7 +589,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (q < D / 32) {
             float vals[32];
             const float z = sum_states(p.sagg, ur.look ? ur.u_first : unit, unit, row, g, vals);
-            put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, vals, z, z);
+            put_state_half(tm + lane + Lay::T_S, sm + Lay::S_LO, row, g, vals, z, z, Lay::VS_K);
         }
         sync_tc();
         return true;
@@ -607,8 +618,10 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int bh = gc / p.CH, c0 = (gc - bh * p.CH) * L;
             const int hn = (gc + 1) / p.CH, cn0 = (gc + 1 - hn * p.CH) * L;  // the next chunk
             const bool more = gc + 1 < ur.end;
-            const bool in_first = gc < first_end;          // qf^T g enters the published R share
-            const bool publish_here = gc == first_end - 1;  // the share is read out after this chunk
+            // qf^T g of the first piece is published for the earlier units of its head (none when
+            // the piece starts the head)
+            const bool in_first = ur.look && gc < first_end;
+            const bool publish_here = ur.look && gc == first_end - 1;  // read out after this chunk
             const int b = (gc - ur.start) & 1;
             const uint32_t u = static_cast<uint32_t>(gc - ur.start) >> 1;
             const uint32_t sQ = smem_u32(sm + (b ? Lay::Q1 : Lay::Q0));
@@ -640,13 +653,13 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         mma_bf16(tm + Lay::T_P, kmaj(sQ, k, kAtom), kmaj(sK, k, kAtom), ID_P, k > 0);
-                        mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sS + S_ATOM, k, S_ATOM),
+                        mma_bf16(tm + Lay::T_DEN, kmaj(sQ, k, kAtom), mnmaj(sSh, k, S_ATOM),
                                  ID_16_KMN, k > 0);
                     }
                     mma_commit(mma_bar);
                     ++ncommit;
                 }
-                mma_state_update(sK, sV, true);  // S_c, read by the compute warps after the dP commit
+                mma_state_update(sK, sV, Lay::VS_K, true);  // S_c, read after the dP commit
             }
             __syncwarp();
             take_from_compute();  // the g tile (gn | gd) is written
@@ -658,13 +671,10 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
                 tma_store_commit();
 #pragma unroll
-                for (int k = 0; k < NE / 16; ++k)  // dP = g [V | 1]^T
-                    mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, kAtom), ID_P, k > 0);
+                for (int k = 0; k < NE / 16; ++k)  // [dP | dqf] = g [V | 1 ; S | Z]^T
+                    mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, Lay::VS_K), ID_PQ, k > 0);
                 mma_commit(mma_bar);
                 const uint32_t dp_commit = ncommit++;
-#pragma unroll
-                for (int k = 0; k < NE / 16; ++k)  // dqf = g [S | Z]^T
-                    mma_bf16(tm + Lay::T_DQ, kmaj(sGh, k, kAtom), kmaj(sS, k, S_ATOM), ID_D_KK, k > 0);
                 if (publish_here) mma_r();  // covered by the next commit: read out after this chunk
                 poll(mma_bar, dp_commit & 1u, bars, p.status);  // V is consumed (S update, dP)
                 if (more) book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
@@ -750,15 +760,15 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             hand_to_mma();
             wait_mma();  // dqf complete
             if (q < D / 32) {
-                if (gc == first_end - 1)  // the first piece is complete: publish its share of R
+                if (ur.look && gc == first_end - 1)  // the first piece is complete: publish its R share
                     publish_half(tm + lane + Lay::T_R, p.ragg + static_cast<size_t>(unit) * W, row, g);
                 if (next_head) {  // the next chunk starts a head: zero state
                     float zero[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) zero[e] = 0.f;
-                    put_state_half(tm + lane + Lay::T_S, sm + Lay::S, row, g, zero, 0.f, 0.f);
+                    put_state_half(tm + lane + Lay::T_S, sm + Lay::S_LO, row, g, zero, 0.f, 0.f, Lay::VS_K);
                 } else {
-                    state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S, row, g);  // S_c, Z_c
+                    state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S_LO, row, g, Lay::VS_K);  // S_c, Z_c
                 }
             }
             tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);  // dQ
