@@ -222,6 +222,7 @@ def run_ours(args):
     Q, K, V, G = x["Q"], x["K"], x["V"], x["G"]
     O = torch.empty_like(V)
     den = torch.empty((B, H, N), dtype=torch.float32, device="cuda")  # normaliser kept for the backward
+    ckpt = torch.empty(la.la_causal_ckpt_floats(B, H, N, D, M), dtype=torch.float32, device="cuda")
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
 
     ev = []
@@ -230,10 +231,10 @@ def run_ours(args):
         if record:
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
-        la.la_forward_causal(Q, K, V, out=O, den=den)
+        la.la_forward_causal(Q, K, V, out=O, den=den, ckpt=ckpt)
         if record:
             e1.record(stream)
-        la.la_backward_causal(Q, K, V, G, Out=O, dQ=dQ, dK=dK, dV=dV, Den=den)
+        la.la_backward_causal(Q, K, V, G, Out=O, dQ=dQ, dK=dK, dV=dV, Den=den, Ckpt=ckpt)
         if record:
             e2.record(stream)
             ev.append((e0, e1, e2))
@@ -273,8 +274,9 @@ def run_ours(args):
     def e2e_step():
         for k in dx:
             dx[k].copy_(hx[k], non_blocking=True)
-        la.la_forward_causal(dx["Q"], dx["K"], dx["V"], out=O, den=den)
-        la.la_backward_causal(dx["Q"], dx["K"], dx["V"], dx["G"], Out=O, dQ=dQ, dK=dK, dV=dV, Den=den)
+        la.la_forward_causal(dx["Q"], dx["K"], dx["V"], out=O, den=den, ckpt=ckpt)
+        la.la_backward_causal(dx["Q"], dx["K"], dx["V"], dx["G"], Out=O, dQ=dQ, dK=dK, dV=dV, Den=den,
+                              Ckpt=ckpt)
         for h, d in zip(hout, (O, dQ, dK, dV)):
             h.copy_(d, non_blocking=True)
 
@@ -325,7 +327,7 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": f"{HEADLINE}: causal linear attention fwd+bwd, B={B} H={H} "
                                    f"N={N} D=M={D}, bf16 storage, fp32 accumulation, "
-                                   "phi=elu+1, Out and the normaliser kept from the forward",
+                                   "phi=elu+1, Out, the normaliser and state checkpoints kept from the forward",
                        "global_batch": B * world, "seq_len": N, "heads": H, "head_dim": D,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": "inputs larger than L2 (4 x 64 MiB resident per rank)"},

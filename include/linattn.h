@@ -67,14 +67,26 @@ typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
  *   Z_final [B][H][D]    fp32, nullable (written) must be NULL iff S_final is NULL
  *   Den     [B][H][N]    fp32, nullable (written) the normaliser phi(Q_i).Z_i
  *           of every token (the denominator of eq. output), for the backward
+ *   Ckpt    fp32, nullable (written) la_causal_ckpt_floats(B, H, N, D, M)
+ *           words: the state (S_i, Z_i) of every head before every 1024th
+ *           token, for the backward (written by the bf16 D = M = 64 path;
+ *           the other paths leave it untouched)
  * With S_init/Z_init a sequence can be processed in pieces; S_final/Z_final
  * hand a prefill's state to la_decode_step (section 三（二）: the state phi(K)V^T
- * is kept as an internal RNN state).  Out and Den may not alias any input.
+ * is kept as an internal RNN state).  Out, Den and Ckpt may not alias any input.
  */
 la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out,
                             int B, int H, int N, int D, int M, la_dtype dtype,
                             const float* S_init, const float* Z_init,
-                            float* S_final, float* Z_final, float* Den, void* stream);
+                            float* S_final, float* Z_final, float* Den, float* Ckpt,
+                            void* stream);
+
+/*
+ * Size in fp32 words of the optional state checkpoints of la_forward_causal /
+ * la_backward_causal: B * H * ceil(ceil(N / 128) / 8) * (D * M + D), or 0 for
+ * non-positive sizes.  Pure arithmetic; no device call.
+ */
+size_t la_causal_ckpt_floats(int B, int H, int N, int D, int M);
 
 /*
  * Causal backward of L(Out) given dOut = dL/dOut: the numerator gradients of
@@ -88,13 +100,17 @@ la_status la_forward_causal(const void* Q, const void* K, const void* V, void* O
  *        normaliser per token (la_forward_causal's Den, from the same inputs);
  *        the bf16 D = M = 64 path then skips recomputing it, the other paths
  *        ignore it.  The results agree within the bf16 tolerance either way.
+ *   Ckpt nullable (read) la_forward_causal's checkpoints from the same inputs
+ *        and no S_init; the bf16 D = M = 64 path then starts each part of a
+ *        sequence from the nearest one instead of re-reading K and V from the
+ *        head's start; the other paths ignore it.
  *   dQ, dK [B][H][N][D]; dV [B][H][N][M] dtype           (written)
  * Outputs may not alias inputs or each other.
  */
 la_status la_backward_causal(const void* Q, const void* K, const void* V, const void* Out,
                              const void* dOut, void* dQ, void* dK, void* dV,
                              int B, int H, int N, int D, int M, la_dtype dtype,
-                             const float* Den, void* stream);
+                             const float* Den, const float* Ckpt, void* stream);
 
 /*
  * Non-causal forward V' = phi(Q)(phi(K)^T V) / phi(Q) sum_j phi(K_j)

@@ -70,12 +70,19 @@ def _dtype(t):
     return _DT[t.dtype]
 
 
+def la_causal_ckpt_floats(B, H, N, D, M):
+    """fp32 words of the optional state checkpoints (la_forward_causal(ckpt=...))."""
+    return int(_lib.la_causal_ckpt_floats(B, H, N, D, M))
+
+
 def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=False,
-                      den=None, stream=None):
+                      den=None, ckpt=None, stream=None):
     """Causal forward.  Returns Out, or (Out, S_final, Z_final) with return_state.
 
     den: optional fp32 [B, H, N] tensor that receives the normaliser
-    phi(Q_i).Z_i of every token, to hand to la_backward_causal(Den=...)."""
+    phi(Q_i).Z_i of every token, to hand to la_backward_causal(Den=...).
+    ckpt: optional fp32 tensor of la_causal_ckpt_floats(B, H, N, D, M) elements
+    that receives state checkpoints, to hand to la_backward_causal(Ckpt=...)."""
     B, H, N, D, M = _dims(Q, V)
     dev = Q.device
     for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
@@ -94,6 +101,7 @@ def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=
         _need(den, "den", torch.float32, dev)
         if tuple(den.shape) != (B, H, N):
             raise ValueError(f"den must be [B, H, N] = {(B, H, N)}, got {tuple(den.shape)}")
+    _check_ckpt(ckpt, "ckpt", B, H, N, D, M, dev)
     S_f = Z_f = None
     if return_state:
         S_f = torch.empty((B, H, D, M), dtype=torch.float32, device=dev)
@@ -101,14 +109,23 @@ def la_forward_causal(Q, K, V, out=None, S_init=None, Z_init=None, return_state=
     with torch.cuda.device(dev):
         _check(_lib.la_forward_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D, M,
                                       _dtype(Q), _ptr(S_init), _ptr(Z_init), _ptr(S_f), _ptr(Z_f),
-                                      _ptr(den), _stream_handle(stream)))
+                                      _ptr(den), _ptr(ckpt), _stream_handle(stream)))
     return (out, S_f, Z_f) if return_state else out
 
 
+def _check_ckpt(c, name, B, H, N, D, M, dev):
+    if c is None:
+        return
+    _need(c, name, torch.float32, dev)
+    if c.numel() != la_causal_ckpt_floats(B, H, N, D, M):
+        raise ValueError(f"{name} must hold la_causal_ckpt_floats(...) = "
+                         f"{la_causal_ckpt_floats(B, H, N, D, M)} floats, got {c.numel()}")
+
+
 def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, Den=None,
-                       stream=None):
-    """Causal backward; returns (dQ, dK, dV).  Out (the forward output) and Den
-    (the forward's normaliser, fp32 [B, H, N]) are optional."""
+                       Ckpt=None, stream=None):
+    """Causal backward; returns (dQ, dK, dV).  Out (the forward output), Den
+    (its normaliser, fp32 [B, H, N]) and Ckpt (its state checkpoints) are optional."""
     B, H, N, D, M = _dims(Q, V)
     dev = Q.device
     for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (dOut, "dOut")):
@@ -119,6 +136,7 @@ def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, Den=N
         _need(Den, "Den", torch.float32, dev)
         if tuple(Den.shape) != (B, H, N):
             raise ValueError(f"Den must be [B, H, N] = {(B, H, N)}, got {tuple(Den.shape)}")
+    _check_ckpt(Ckpt, "Ckpt", B, H, N, D, M, dev)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
@@ -127,7 +145,7 @@ def la_backward_causal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, Den=N
     with torch.cuda.device(dev):
         _check(_lib.la_backward_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Out), _ptr(dOut), _ptr(dQ),
                                        _ptr(dK), _ptr(dV), B, H, N, D, M, _dtype(Q), _ptr(Den),
-                                       _stream_handle(stream)))
+                                       _ptr(Ckpt), _stream_handle(stream)))
     return dQ, dK, dV
 
 

@@ -17,8 +17,9 @@ LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
 # (name, argtypes) of every exported entry point.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
 SIGNATURES = {
-    "la_forward_causal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _F, _P],
-    "la_backward_causal": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P],
+    "la_forward_causal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _F, _F, _P],
+    "la_backward_causal": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P],
+    "la_causal_ckpt_floats": [_I, _I, _I, _I, _I],
     "la_forward_noncausal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_forward_noncausal_noalloc": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_decode_step": [_P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _P],
@@ -28,6 +29,7 @@ SIGNATURES = {
     "la_kernel_launch_count": [],
 }
 _RESTYPES = {"la_status_string": ctypes.c_char_p, "la_last_error_message": ctypes.c_char_p,
+             "la_causal_ckpt_floats": ctypes.c_size_t,
              "la_kernel_launch_count": ctypes.c_uint64}
 
 

@@ -100,6 +100,7 @@ struct BwdParams {
     unsigned* ticket;
     float* gd;            // [BH][N]
     const float* den;     // [BH][N] the forward's normaliser per token, or null (recomputed)
+    const float* ckpt;    // the forward's state checkpoints (see kCkptChunks), or null
     unsigned* status;
 };
 
@@ -505,7 +506,11 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int first_end = min(ur.end, (ur.hA + 1) * p.CH);  // end of the first piece
     const bool have_den = p.den != nullptr;
     const int g0 = max(ur.start, ur.hB * p.CH);           // phase 1 covers [g0, end) when publishing
-    const uint32_t n1 = ur.publish ? static_cast<uint32_t>(ur.end - g0) : 0u;  // its chunks
+    // chunks of the aggregate pass before phase 2 (each opens one phase of the TMA and MMA
+    // barriers): phase 1, or with checkpoints the way from the nearest one to the first piece
+    const uint32_t n1 = static_cast<uint32_t>(
+        p.ckpt ? (ur.look ? (ur.start - ur.hA * p.CH) % kCkptChunks : 0)
+               : (ur.publish ? ur.end - g0 : 0));
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sV = smem_u32(sm + Lay::V), sGh = smem_u32(sm + Lay::GH);
     const uint32_t sSh = smem_u32(sm + Lay::S_HI);
@@ -533,8 +538,10 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             phase ^= 1u;
             return bar_sync_or(kBarE, kBT, bad);
         };
-        if (ur.publish) {
-            const int h = ur.hB;
+        // T_S (+)= sum over the chunks [ga, gb) of head h of kf^T [V | 1]: onto its contents
+        // when acc, from zero otherwise.
+        auto aggregate = [&](int h, int ga, int gb, bool acc) -> bool {
+            if (ga >= gb) return true;
             auto load_kv = [&](int c0, int b) {  // thread 0 only
                 book.expect(tma_bar, 2 * kAtom);
                 book.load(sm + (b ? Lay::K1 : Lay::K0), &tmK, tma_bar, 0, c0, h);
@@ -544,27 +551,58 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 reinterpret_cast<uint4*>(sm + Lay::O)[i] =
                     make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
             fence_proxy_async();
-            if (t == 0) load_kv((g0 - h * p.CH) * L, 0);
-            for (int gc = g0; gc < ur.end; ++gc) {
+            if (t == 0) load_kv((ga - h * p.CH) * L, 0);
+            for (int gc = ga; gc < gb; ++gc) {
                 const int c0 = (gc - h * p.CH) * L;
-                const int b = (gc - g0) & 1;
+                const int b = (gc - ga) & 1;
                 if (wait_bar(tma_bar, tma_phase)) return false;
                 if (t == 0) book.pending = false;
-                if (gc > g0) {  // the previous chunk's MMA has released the other buffer
+                if (gc > ga) {  // the previous chunk's MMA has released the other buffer
                     if (wait_bar(mma_bar, mma_phase)) return false;
                     fence_after_sync();
                 }
-                if (t == 0 && gc + 1 < ur.end) load_kv(c0 + L, b ^ 1);
+                if (t == 0 && gc + 1 < gb) load_kv(c0 + L, b ^ 1);
                 phi_tile<true, kBT>(sm + (b ? Lay::K1 : Lay::K0), 1, min(L, p.N - c0));
                 sync_tc();
                 if (t == 0) {
                     mma_state_update(smem_u32(sm + (b ? Lay::K1 : Lay::K0)), b ? smem_u32(sm + Lay::G) : sV,
-                                     b ? kAtom : Lay::VS_K, gc > g0);
+                                     b ? kAtom : Lay::VS_K, acc || gc > ga);
                     mma_commit(mma_bar);
                 }
             }
             if (wait_bar(mma_bar, mma_phase)) return false;
             fence_after_sync();
+            return true;
+        };
+        if (p.ckpt) {  // the first piece starts from the forward's nearest checkpoint
+            float vals[32];
+            float z = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) vals[e] = 0.f;
+            const int h = ur.hA, kc = (ur.start - h * p.CH) / kCkptChunks;
+            if (ur.look && kc > 0 && q < D / 32) {
+                const float* ck = p.ckpt + (static_cast<size_t>(h) * ckpt_slots(p.CH) + kc) * W;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(ck + row * M + 32 * g) + u);
+                    vals[4 * u] = x.x;
+                    vals[4 * u + 1] = x.y;
+                    vals[4 * u + 2] = x.z;
+                    vals[4 * u + 3] = x.w;
+                }
+                z = __ldg(ck + D * M + row);
+            }
+            if (q < D / 32) put_state_half(tm + lane + Lay::T_S, sm + Lay::S_LO, row, g, vals, z, z, Lay::VS_K);
+            sync_tc();
+            if (ur.look) {  // the chunks between the checkpoint and the piece
+                if (!aggregate(h, h * p.CH + kc * kCkptChunks, ur.start, true)) return false;
+                if (q < D / 32) state_half_to_tile(tm + lane + Lay::T_S, sm + Lay::S_LO, row, g, Lay::VS_K);
+                sync_tc();
+            }
+            return true;
+        }
+        if (ur.publish) {  // phase 1: the last piece's aggregate, for the later units of its head
+            if (!aggregate(ur.hB, g0, ur.end, false)) return false;
             if (q < D / 32) publish_half(tm + lane + Lay::T_S, p.sagg + static_cast<size_t>(unit) * W, row, g);
             __threadfence();
             fence_before_sync();
@@ -1003,7 +1041,8 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                  const __nv_bfloat16* V, const __nv_bfloat16* O,
                                  const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
-                                 __nv_bfloat16* dV, int BH, int N, const float* Den) {
+                                 __nv_bfloat16* dV, int BH, int N, const float* Den,
+                                 const float* Ckpt) {
     using namespace tcb;
     auto kf = bwd_prefix_tc_kernel;
     auto kr = bwd_suffix_tc_kernel;
@@ -1029,9 +1068,11 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     const size_t gd_bytes = sizeof(float) * static_cast<size_t>(BH) * N;
     const size_t o_bytes = O ? 0 : gn_bytes;
     const size_t den_bytes = O ? 0 : gd_bytes;  // the recomputed forward's normaliser
+    const size_t ck_bytes =  // and its checkpoints
+        O || Ckpt ? 0 : sizeof(float) * static_cast<size_t>(BH) * ckpt_slots(chunks) * W;
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gn_bytes) + up(gd_bytes) + up(o_bytes) +
-                         up(den_bytes);
+                         up(den_bytes) + up(ck_bytes);
     char* ws = nullptr;
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), total)) != cudaSuccess) return e;
     BwdParams p;
@@ -1054,15 +1095,19 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     __nv_bfloat16* Ow = O ? nullptr : reinterpret_cast<__nv_bfloat16*>(q);
     q += up(o_bytes);
     float* Dw = O ? nullptr : reinterpret_cast<float*>(q);
+    q += up(den_bytes);
+    float* Cw = ck_bytes ? reinterpret_cast<float*>(q) : nullptr;
     p.den = Den;
+    p.ckpt = Ckpt;
     p.status = c.status_word;
     do {
         if (!O) {  // the output is needed for gd: recompute it
             if ((e = causal_forward_tc<64, 64>(c, Q, K, V, Ow, BH, N, nullptr, nullptr, nullptr,
-                                               nullptr, Den ? nullptr : Dw)) != cudaSuccess)
+                                               nullptr, Den ? nullptr : Dw, Cw)) != cudaSuccess)
                 break;
             O = Ow;
             if (!Den) p.den = Dw;
+            if (!Ckpt) p.ckpt = Cw;
         }
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
         CUtensorMap mQ, mK, mV, mG, mO, mGn, mdQ, mdK, mdV;

@@ -91,6 +91,7 @@ struct FwdParams {
     float* S_final;        // [BH][D][M] or null
     float* Z_final;        // [BH][D] or null
     float* den;            // [BH][N] or null: the normaliser of every token
+    float* ckpt;           // [BH][ckpt_slots(CH)][W] or null: states before every 8th chunk
     unsigned* status;      // device error word
 };
 
@@ -399,10 +400,19 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                 }
                 if (gc + 1 < ur.end) put_state(h + 1, 0, 0);
-            } else {  // S_c -> bf16 copy for the next chunk's O_ext
+            } else {  // S_c -> bf16 copy for the next chunk's O_ext (and a checkpoint)
+                float* ck = p.ckpt && (cc + 1) % kCkptChunks == 0
+                                ? p.ckpt + (static_cast<size_t>(h) * ckpt_slots(p.CH) + (cc + 1) / kCkptChunks) * W
+                                : nullptr;
                 for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                     float v[32];
                     tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                    if (ck) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            reinterpret_cast<float4*>(ck + d * M + j0)[u] =
+                                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) pk[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
@@ -411,6 +421,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (g == 0) {
                     float z[16];
                     tmem_ld16(tm + lane + Lay::T_S + M, z);
+                    if (ck) ck[D * M + d] = z[0];
                     uint32_t zk[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) zk[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
@@ -458,7 +469,7 @@ template <int D, int M>
 cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
                               const float* S_init, const float* Z_init, float* S_final,
-                              float* Z_final, float* Den) {
+                              float* Z_final, float* Den, float* Ckpt) {
     using namespace tcf;
     using Lay = Layout<D, M>;
     const int chunks = (N + L - 1) / L;
@@ -498,6 +509,7 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     p.S_final = S_final;
     p.Z_final = Z_final;
     p.den = Den;
+    p.ckpt = Ckpt;
     p.status = c.status_word;
     do {
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
@@ -516,10 +528,10 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
 template cudaError_t causal_forward_tc<64, 64>(const LaunchCtx&, const __nv_bfloat16*,
                                                const __nv_bfloat16*, const __nv_bfloat16*,
                                                __nv_bfloat16*, int, int, const float*, const float*,
-                                               float*, float*, float*);
+                                               float*, float*, float*, float*);
 template cudaError_t causal_forward_tc<128, 128>(const LaunchCtx&, const __nv_bfloat16*,
                                                  const __nv_bfloat16*, const __nv_bfloat16*,
                                                  __nv_bfloat16*, int, int, const float*,
-                                                 const float*, float*, float*, float*);
+                                                 const float*, float*, float*, float*, float*);
 
 }  // namespace la

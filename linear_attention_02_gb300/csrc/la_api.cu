@@ -161,10 +161,10 @@ struct FwdCausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
                            int BH, int N, const float* Si, const float* Zi, float* Sf, float* Zf,
-                           float* Den) {
+                           float* Den, float* Ckpt) {
         if constexpr (UseTensorCores<T, D, M>::value)
             return causal_forward_tc<D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N,
-                                           Si, Zi, Sf, Zf, Den);
+                                           Si, Zi, Sf, Zf, Den, Ckpt);
         else
             return causal_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, BH, N,
                                            Si, Zi, Sf, Zf, Den);
@@ -174,10 +174,10 @@ struct BwdCausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V,
                            const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N,
-                           const float* Den) {
+                           const float* Den, const float* Ckpt) {
         if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 64 && M == 64)
             return causal_backward_tc64(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
-                                        (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N, Den);
+                                        (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N, Den, Ckpt);
         else
             return causal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V,
                                             (const T*)O, (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH,
@@ -241,7 +241,7 @@ extern "C" {
 la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out, int B, int H,
                             int N, int D, int M, la_dtype dtype, const float* S_init,
                             const float* Z_init, float* S_final, float* Z_final, float* Den,
-                            void* stream) {
+                            float* Ckpt, void* stream) {
     static const char* fn = "la_forward_causal";
     const void* p[] = {Q, K, V, Out};
     const char* nm[] = {"Q", "K", "V", "Out"};
@@ -254,33 +254,42 @@ la_status la_forward_causal(const void* Q, const void* K, const void* V, void* O
         return fail(LA_ERR_INVALID_ARG, "%s: S_final and Z_final must both be given or both NULL", fn);
     if ((s = check_optional(fn, S_init, "S_init")) || (s = check_optional(fn, Z_init, "Z_init")) ||
         (s = check_optional(fn, S_final, "S_final")) || (s = check_optional(fn, Z_final, "Z_final")) ||
-        (s = check_optional(fn, Den, "Den")))
+        (s = check_optional(fn, Den, "Den")) || (s = check_optional(fn, Ckpt, "Ckpt")))
         return s;
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     const size_t bh = (size_t)B * H;
     if (empty) return finish(empty_forward_state(ctx.stream, bh, D, M, S_init, Z_init, S_final, Z_final), fn);
     return finish(dispatch<FwdCausal>(dtype, D, M, &ctx, Q, K, V, Out, (int)bh, N, S_init, Z_init,
-                                      S_final, Z_final, Den),
+                                      S_final, Z_final, Den, Ckpt),
                   fn);
 }
 
 la_status la_backward_causal(const void* Q, const void* K, const void* V, const void* Out,
                              const void* dOut, void* dQ, void* dK, void* dV, int B, int H, int N,
-                             int D, int M, la_dtype dtype, const float* Den, void* stream) {
+                             int D, int M, la_dtype dtype, const float* Den, const float* Ckpt,
+                             void* stream) {
     static const char* fn = "la_backward_causal";
     const void* p[] = {Q, K, V, dOut, dQ, dK, dV};
     const char* nm[] = {"Q", "K", "V", "dOut", "dQ", "dK", "dV"};
     bool empty = false;
     la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 7, &empty);
     if (s != LA_OK) return s;
-    if ((s = check_optional(fn, Out, "Out")) || (s = check_optional(fn, Den, "Den"))) return s;
+    if ((s = check_optional(fn, Out, "Out")) || (s = check_optional(fn, Den, "Den")) ||
+        (s = check_optional(fn, Ckpt, "Ckpt")))
+        return s;
     if (empty) return LA_OK;
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     return finish(dispatch<BwdCausal>(dtype, D, M, &ctx, Q, K, V, Out, dOut, dQ, dK, dV,
-                                      (int)((size_t)B * H), N, Den),
+                                      (int)((size_t)B * H), N, Den, Ckpt),
                   fn);
+}
+
+size_t la_causal_ckpt_floats(int B, int H, int N, int D, int M) {
+    if (B <= 0 || H <= 0 || N <= 0 || D <= 0 || M <= 0) return 0;
+    const size_t chunks = ((size_t)N + 127) / 128;
+    return (size_t)B * H * ((chunks + kCkptChunks - 1) / kCkptChunks) * ((size_t)D * M + D);
 }
 
 la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void* Out, int B,

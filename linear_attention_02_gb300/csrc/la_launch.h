@@ -22,6 +22,12 @@ void note_launch(int n = 1);
 // Sets the text returned by la_last_error_message() on this host thread.
 void set_error_message(const char* msg);
 
+// Optional checkpoints kept by the causal forward for the backward: the fp32
+// state [S | Z] (D*M + D words) of every head before every kCkptChunks-th chunk
+// of 128 tokens, laid out [BH][ceil(chunks / kCkptChunks)][D*M + D]; slot 0
+// (the zero state) is never written or read.
+constexpr int kCkptChunks = 8;
+
 // Stream-ordered scratch from the library pool.  Returns cudaSuccess or the error.
 cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes);
 void scratch_free(const LaunchCtx& c, void* p);
@@ -37,14 +43,15 @@ template <int D, int M>
 cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
                               const float* S_init, const float* Z_init, float* S_final,
-                              float* Z_final, float* Den);
+                              float* Z_final, float* Den, float* Ckpt);
 
 // Tensor-core causal backward for bf16 storage with D = M = 64; Den (the
-// forward's normaliser per token) may be null.
+// forward's normaliser per token) and Ckpt (its state checkpoints) may be null.
 cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                  const __nv_bfloat16* V, const __nv_bfloat16* O,
                                  const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
-                                 __nv_bfloat16* dV, int BH, int N, const float* Den);
+                                 __nv_bfloat16* dV, int BH, int N, const float* Den,
+                                 const float* Ckpt);
 
 template <typename T, int D, int M>
 cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,

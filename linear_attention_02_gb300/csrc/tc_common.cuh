@@ -147,6 +147,11 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, uint32_t atom_bytes, 
 
 // ------------------------------------------------------------------ host
 
+// Checkpoint slots per head (see kCkptChunks).
+__host__ __device__ constexpr int ckpt_slots(int chunks_per_head) {
+    return (chunks_per_head + kCkptChunks - 1) / kCkptChunks;
+}
+
 // Work split of the causal kernels: the chunks of all heads, head-major, cut
 // into `units` equal ranges of `per` chunks, one per resident CTA (one wave,
 // every CTA busy for the same number of chunks whatever the head count).

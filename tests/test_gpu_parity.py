@@ -97,6 +97,27 @@ def test_causal_forward_bf16_span_shapes(shape):
     assert rel_err(den.reshape(B * H, N)[idx], Rd) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 3000, 64, 64), (2, 3, 8300, 64, 64)])
+def test_causal_forward_checkpoints(shape):
+    # slot k holds the state (S, Z) after the first 1024 k tokens of each head
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=29 + N)
+    g = _dev(x)
+    ck = torch.full((la.la_causal_ckpt_floats(B, H, N, D, M),), float("nan"), device="cuda")
+    la.la_forward_causal(g["Q"], g["K"], g["V"], ckpt=ck)
+    la.la_check_device_status()
+    slots = -(-(-(-N // 128)) // 8)
+    ck = ck.reshape(B * H, slots, D * M + D)
+    assert bool(torch.isnan(ck[:, 0]).all())  # slot 0 (the zero state) is left alone
+    heads = [x[n].reshape(B * H, N, -1)[:2] for n in ("Q", "K", "V")]
+    for k in range(1, slots):
+        _, Rs, Rz = oracle.causal_forward_recurrent(*(h[:, :1024 * k] for h in heads))
+        got = ck[:2, k]
+        assert rel_err(got[:, :D * M].reshape(2, D, M), Rs) <= TOL["bf16"]
+        assert rel_err(got[:, D * M:], Rz) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_causal_forward_carried_state_and_empty(dt):
     la = _la()
@@ -120,24 +141,28 @@ def test_causal_forward_carried_state_and_empty(dt):
 
 
 def _saved(la, g, saved):
-    """The forward's outputs handed to the backward: none, Out, or Out and den."""
+    """The forward's outputs handed to the backward: none, Out, Out and den, or Out, den
+    and the state checkpoints."""
     if saved == "none":
-        return None, None
-    B, H, N, _ = g["Q"].shape
-    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda") if saved == "out+den" else None
-    return la.la_forward_causal(g["Q"], g["K"], g["V"], den=den), den
+        return None, None, None
+    B, H, N, D = g["Q"].shape
+    M = g["V"].shape[3]
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda") if "den" in saved else None
+    ck = (torch.empty(la.la_causal_ckpt_floats(B, H, N, D, M), dtype=torch.float32, device="cuda")
+          if "ckpt" in saved else None)
+    return la.la_forward_causal(g["Q"], g["K"], g["V"], den=den, ckpt=ck), den, ck
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", [s for s in SMALL if s[2] > 1])
-@pytest.mark.parametrize("saved", ["out", "none", "out+den"])
+@pytest.mark.parametrize("saved", ["out", "none", "out+den", "out+den+ckpt"])
 def test_causal_backward_small(dt, shape, saved):
     la = _la()
     B, H, N, D, M = shape
     x = synth.qkv(B, H, N, D, M, dt, seed=21 + N, with_grad=True)
     g = _dev(x)
-    O, den = _saved(la, g, saved)
-    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den)
+    O, den, ck = _saved(la, g, saved)
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den, Ckpt=ck)
     torch.cuda.synchronize()
     RdQ, RdK, RdV = oracle.causal_backward_cumsum(x["Q"], x["K"], x["V"], x["G"])
     assert rel_err(dQ, RdQ) <= TOL[dt]
@@ -152,14 +177,14 @@ def test_causal_backward_small(dt, shape, saved):
     (1, 1, 128, 64, 64),
     (2, 3, 8300, 64, 64),     # several chunks per range, ranges crossing heads, ragged last chunk
 ])
-@pytest.mark.parametrize("saved", ["out", "none", "out+den"])
+@pytest.mark.parametrize("saved", ["out", "none", "out+den", "out+den+ckpt"])
 def test_causal_backward_bf16_span_shapes(shape, saved):
     la = _la()
     B, H, N, D, M = shape
     x = synth.qkv(B, H, N, D, M, "bf16", seed=23 + N, with_grad=True)
     g = _dev(x)
-    O, den = _saved(la, g, saved)
-    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den)
+    O, den, ck = _saved(la, g, saved)
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den, Ckpt=ck)
     la.la_check_device_status()
     idx = list(range(min(B * H, 6)))
     hs = [x[n].reshape(B * H, N, -1)[idx] for n in ("Q", "K", "V", "G")]
@@ -280,11 +305,13 @@ def test_full_causal_train_bf16():
     w = synth.WORKLOADS["causal_train_bf16"]
     x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, with_grad=True)
     g = _dev(x)
-    # the training step as the bench runs it: the forward keeps Out and the
-    # normaliser, the backward takes both
+    # the training step as the bench runs it: the forward keeps Out, the
+    # normaliser and the state checkpoints, the backward takes them
     den = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
-    O = la.la_forward_causal(g["Q"], g["K"], g["V"], den=den)
-    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den)
+    ck = torch.empty(la.la_causal_ckpt_floats(w.B, w.H, w.N, w.D, w.M), dtype=torch.float32,
+                     device="cuda")
+    O = la.la_forward_causal(g["Q"], g["K"], g["V"], den=den, ckpt=ck)
+    dQ, dK, dV = la.la_backward_causal(g["Q"], g["K"], g["V"], g["G"], Out=O, Den=den, Ckpt=ck)
     torch.cuda.synchronize()
     idx = _sample_heads(w.B * w.H)
     hs = [_heads(x[n], idx) for n in ("Q", "K", "V", "G")]
