@@ -16,18 +16,23 @@
 // Two kernels over the same work split as the forward (the chunks of all heads,
 // head-major, cut into equal ranges, one per CTA; a range's pieces in
 // successive heads are its segments):
-//   prefix kernel -- phase 1 / look-back exactly as the forward to get the
-//     first piece's starting S, Z (later pieces start a head from zero); then
-//     per chunk: P and qf.Z by MMA, den, gn, gd (written to scratch), dP and
-//     dqf by MMA, dQ out; the first piece's sum qf^T g (its share of R) is
-//     published for the suffix kernel;
+//   prefix kernel -- the first piece's starting S, Z come from the forward's
+//     nearest state checkpoint plus a short aggregate pass, or, without
+//     checkpoints, from phase 1 / look-back as in the forward (later pieces
+//     start a head from zero); then per chunk: den (from the forward, or from
+//     P and qf.Z by MMA), gn, gd (written to scratch), [dP | dqf] by one MMA,
+//     dqf += dP kf with dP read from TMEM, dQ out; the first piece's sum
+//     qf^T g (its share of R) is published for the suffix kernel when earlier
+//     units of its head exist;
 //   suffix kernel -- walks its chunks in reverse; the last piece starts from
 //     the shares of the later units of its head (all complete, the prefix
-//     kernel has finished), earlier pieces from zero: P and dP again, dV and
-//     dkf by MMA, R += qf^T g.
-// Each CTA has eight compute warps and four transform warps: the transform
-// warps load the next chunk's Q and K into the free one of two buffers and
-// apply phi there, so that work leaves the compute warps' chain.
+//     kernel has finished), earlier pieces from zero: P^T and dP^T by MMA,
+//     masked and packed in TMEM, dV = P^T gn + kf R and dkf = dP^T qf +
+//     [V | 1][R | r]^T with P^T, dP^T read from TMEM, R += qf^T g.
+// Each CTA has eight compute warps (the epilogues), one MMA warp (every MMA,
+// TMA copy and store) and three transform warps (the next chunk's Q and K into
+// the free one of two buffers, phi there), handing work over through mbarriers
+// and named barriers, so the MMAs no epilogue waits for run underneath them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
