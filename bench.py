@@ -266,30 +266,55 @@ def run_ours(args):
     tokens = B * N * world
     value = tokens / (ms_step / 1e3)
 
-    # end to end: pinned host inputs -> device -> fwd + bwd -> host outputs
+    # end to end: pinned host inputs -> device -> fwd + bwd -> host outputs, every step.
+    # Pipelined over three streams with two device buffer sets: step k's input copy and
+    # step k-1's output copy run while step k computes (separate copy engines), the way a
+    # training loop feeds a device; every byte still crosses the link inside the timed region.
     hx = {k: v.cpu().pin_memory() for k, v in x.items()}
-    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (O, dQ, dK, dV)]
-    dx = {k: torch.empty_like(v) for k, v in x.items()}
-
-    def e2e_step():
-        for k in dx:
-            dx[k].copy_(hx[k], non_blocking=True)
-        la.la_forward_causal(dx["Q"], dx["K"], dx["V"], out=O, den=den, ckpt=ckpt)
-        la.la_backward_causal(dx["Q"], dx["K"], dx["V"], dx["G"], Out=O, dQ=dQ, dK=dK, dV=dV, Den=den,
-                              Ckpt=ckpt)
-        for h, d in zip(hout, (O, dQ, dK, dV)):
-            h.copy_(d, non_blocking=True)
-
+    slots = []
     for _ in range(2):
-        e2e_step()
+        dxs = {k: torch.empty_like(v) for k, v in x.items()}
+        outs = [torch.empty_like(t) for t in (O, dQ, dK, dV)]
+        slots.append((dxs, outs, [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]))
+    hout = slots[0][2]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_cmp + ev_out:
+        e.record(stream)
+
+    def e2e_step(k):
+        dxs, outs, houts = slots[k & 1]
+        s_in.wait_event(ev_cmp[k & 1])          # step k - 2 is done with these inputs
+        with torch.cuda.stream(s_in):
+            for name in dxs:
+                dxs[name].copy_(hx[name], non_blocking=True)
+        ev_in[k & 1].record(s_in)
+        stream.wait_event(ev_in[k & 1])
+        stream.wait_event(ev_out[k & 1])        # step k - 2's outputs are read out
+        Ok, dQk, dKk, dVk = outs
+        la.la_forward_causal(dxs["Q"], dxs["K"], dxs["V"], out=Ok, den=den, ckpt=ckpt, stream=stream)
+        la.la_backward_causal(dxs["Q"], dxs["K"], dxs["V"], dxs["G"], Out=Ok, dQ=dQk, dK=dKk, dV=dVk,
+                              Den=den, Ckpt=ckpt, stream=stream)
+        ev_cmp[k & 1].record(stream)
+        s_out.wait_event(ev_cmp[k & 1])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(houts, outs):
+                h.copy_(d, non_blocking=True)
+        ev_out[k & 1].record(s_out)
+
+    for k in range(2):
+        e2e_step(k)
     torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(4, min(args.steps, 20))
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
+    a.record(s_in)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    s_out.wait_event(ev_cmp[(e2e_steps - 1) & 1])
+    b.record(s_out)
     b.synchronize()
     e2e_ms = a.elapsed_time(b) / e2e_steps
     if world > 1:
@@ -334,7 +359,10 @@ def run_ours(args):
             "roofline": roofline,
             "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4),
+                    "pipelining": "input copies, compute and output copies on three streams, "
+                                  "two device buffer sets; every step's bytes cross inside the "
+                                  "timed region"},
             "gpu_launches": launches,
             "clocks": clocks,
             "paths": paths,
