@@ -245,16 +245,20 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             reinterpret_cast<uint4*>(sm + Lay::P + MA * kAtom)[i] =
                 make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
         fence_proxy_async();
-        if (t == 0) load_kv((g0 - h * p.CH) * L, 0);
-        for (int gc = g0; gc < ur.end; ++gc) {
+        // The chunks are summed last to first: the ones phase 2 reads first are then the most
+        // recently read, and still in L2.
+        const int n1 = ur.end - g0;
+        if (t == 0) load_kv((ur.end - 1 - h * p.CH) * L, 0);
+        for (int i1 = 0; i1 < n1; ++i1) {
+            const int gc = ur.end - 1 - i1;
             const int c0 = (gc - h * p.CH) * L;
-            const int b = (gc - g0) & 1;
+            const int b = i1 & 1;
             wait_bar(tma_bar, tma_phase);
-            if (gc > g0) {  // the previous chunk's MMA has released the other buffer
+            if (i1 > 0) {  // the previous chunk's MMA has released the other buffer
                 wait_bar(mma_bar, mma_phase);
                 fence_after_sync();
             }
-            if (t == 0 && gc + 1 < ur.end) load_kv(c0 + L, b ^ 1);
+            if (t == 0 && i1 + 1 < n1) load_kv(c0 - L, b ^ 1);
             phi_tile<true, NT>(sm + (b ? Lay::Q : Lay::K), DA, min(L, p.N - c0));
             fence_proxy_async();
             fence_before_sync();
@@ -262,7 +266,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             fence_after_sync();
             if (sh[1]) goto cleanup;
             if (t == 0) {
-                mma_state_update(b ? sQ : sK, b ? sP : sV, gc > g0);
+                mma_state_update(b ? sQ : sK, b ? sP : sV, i1 > 0);
                 mma_commit(mma_bar);
             }
         }
