@@ -342,6 +342,7 @@ constexpr int kEM = kBT + 32;             // compute warps + MMA warp
 // side meets each hand-over barrier alternately with the other side, so no
 // arrival can fall into the previous use.
 constexpr uint32_t kBarE = 3, kBarT = 2, kBarEM = 1, kBarME = 4;
+constexpr uint32_t kBarEM2 = 5;  // a second compute -> MMA warp hand-over within a chunk
 
 // Hand-over among the compute warps when they issue MMAs themselves (phase 1):
 // their shared-memory writes become visible to the tensor core and TMA, and
@@ -353,13 +354,13 @@ __device__ __forceinline__ void sync_tc() {
     fence_after_sync();
 }
 // Compute warps -> MMA warp: their shared-memory and TMEM writes are done.
-__device__ __forceinline__ void hand_to_mma() {
+__device__ __forceinline__ void hand_to_mma(uint32_t id = kBarEM) {
     fence_proxy_async();
     fence_before_sync();
-    bar_arrive(kBarEM, kEM);
+    bar_arrive(id, kEM);
 }
-__device__ __forceinline__ void take_from_compute() {
-    bar_sync(kBarEM, kEM);
+__device__ __forceinline__ void take_from_compute(uint32_t id = kBarEM) {
+    bar_sync(id, kEM);
     fence_after_sync();
 }
 // MMA warp -> compute warps: the tiles it waited for are in, the buffers free.
@@ -379,6 +380,8 @@ struct Bars {
     uint64_t ready[2];   // phi(Q), phi(K) of buffer b are in place
     uint64_t freeb[2];   // the chunk using buffer b is done with it
     uint64_t rbar;       // completion of each chunk's last MMAs (R update included)
+    uint64_t cb[4];      // suffix kernel: P^T, dP^T, dV, dK products of each chunk, one
+                         // barrier per product so no waiter can fall two phases behind
     uint32_t tmem, pad;
     int unit, broken, pad2, pad3;
 };
@@ -851,6 +854,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
         mbar_init(&bars->rbar, 1);
+        for (int j = 0; j < 4; ++j) mbar_init(&bars->cb[j], 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->full[b], 1);
             mbar_init(&bars->ready[b], 1);
@@ -938,23 +942,27 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             __syncwarp();
             if (lead) {
                 poll(&bars->ready[b], u & 1u, bars, p.status);  // phi(Q), phi(K)
-                poll(tma_bar, tma_phase, bars, p.status);       // V, gn
-                tma_phase ^= 1u;
-                book.pending = false;
-                if (more) book.expect(tma_bar, 2 * kAtom);
                 if (i > 0) mbar_arrive(&bars->freeb[b ^ 1]);  // the previous chunk's Q, K
                 fence_after_sync();
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k)  // P^T = kf qf^T
+                for (int k = 0; k < D / 16; ++k)  // P^T = kf qf^T (needs no V or g)
                     mma_bf16(tm + Lay::T_P, kmaj(sK, k, kAtom), kmaj(sQ, k, kAtom), ID_P, k > 0);
-#pragma unroll
-                for (int k = 0; k < NE / 16; ++k)  // dP^T = [V | 1] g^T
-                    mma_bf16(tm + Lay::T_DP, kmaj(sV, k, kAtom), kmaj(sGh, k, kAtom), ID_P, k > 0);
-                mma_commit(mma_bar);
+                mma_commit(&bars->cb[0]);
             }
             __syncwarp();
             hand_to_compute();
-            take_from_compute();  // P^T and dP^T are masked and packed in TMEM
+            if (lead) {
+                poll(tma_bar, tma_phase, bars, p.status);  // V, gn
+                tma_phase ^= 1u;
+                book.pending = false;
+                if (more) book.expect(tma_bar, 2 * kAtom);
+#pragma unroll
+                for (int k = 0; k < NE / 16; ++k)  // dP^T = [V | 1] g^T
+                    mma_bf16(tm + Lay::T_DP, kmaj(sV, k, kAtom), kmaj(sGh, k, kAtom), ID_P, k > 0);
+                mma_commit(&bars->cb[1]);
+            }
+            __syncwarp();
+            take_from_compute();  // P^T is masked and packed in TMEM
             if (lead) {
                 tma_store_wait_read();  // the staging tiles are read out before dV, dK commit
 #pragma unroll
@@ -964,7 +972,11 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)  // dV += kf R
                     mma_bf16(tm + Lay::T_DV, kmaj(sK, k, kAtom), mnmaj(sR, k, S_ATOM), ID_M_KMN, 1u);
-                mma_commit(mma_bar);
+                mma_commit(&bars->cb[2]);
+            }
+            __syncwarp();
+            take_from_compute(kBarEM2);  // dP^T is masked and packed in TMEM
+            if (lead) {
 #pragma unroll
                 for (int k = 0; k < L / 16; ++k)  // dkf = dP^T qf, dP^T read from TMEM
                     mma_bf16_ts(tm + Lay::T_DK, tm + Lay::T_DP + packed_a_col(k), mnmaj(sQ, k, kAtom),
@@ -972,7 +984,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
                 for (int k = 0; k < NE / 16; ++k)  // dkf += [V | 1] [R | r]^T
                     mma_bf16(tm + Lay::T_DK, kmaj(sV, k, kAtom), kmaj(sR, k, S_ATOM), ID_D_KK, 1u);
-                mma_commit(mma_bar);
+                mma_commit(&bars->cb[3]);
                 if (cc > 0) {  // R += qf^T g (not needed before a head's first chunk)
 #pragma unroll
                     for (int k = 0; k < L / 16; ++k)
@@ -995,10 +1007,9 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
         }
     } else {  // compute warps
-        uint32_t e_commit = 0, e_r = 0;
-        auto wait_on = [&](uint64_t* bar, uint32_t& n) {
-            if (t == 0) poll(bar, n & 1u, bars, p.status);
-            ++n;
+        uint32_t e_r = 0;
+        auto wait_on = [&](uint64_t* bar, uint32_t parity) {
+            if (t == 0) poll(bar, parity, bars, p.status);
             bar_sync(kBarE, kBT);
             fence_after_sync();
         };
@@ -1006,18 +1017,22 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int bh = gc / p.CH, cc = gc - bh * p.CH;
             const bool more = gc > ur.start;
             const int b = (ur.end - 1 - gc) & 1;
+            const uint32_t ph = static_cast<uint32_t>(ur.end - 1 - gc) & 1u;  // this chunk's phase
             uint8_t* const tK = sm + (b ? Lay::K1 : Lay::K0);
             (void)bh;
             take_from_mma();
-            wait_on(mma_bar, e_commit);  // P^T, dP^T
+            wait_on(&bars->cb[0], ph);  // P^T
             masked_half_t_to_tmem(tm + lane + Lay::T_P, row, q, g);   // P^T, masked, bf16 in TMEM
+            hand_to_mma();              // the dV products start
+            wait_on(&bars->cb[1], ph);  // dP^T
             masked_half_t_to_tmem(tm + lane + Lay::T_DP, row, q, g);  // dP^T likewise
-            hand_to_mma();
-            wait_on(mma_bar, e_commit);  // dV
+            hand_to_mma(kBarEM2);       // the dK products start
+            wait_on(&bars->cb[2], ph);  // dV
             tmem_half_to_tile(tm + lane + Lay::T_DV, sm + Lay::DP, row, g, nullptr);  // dV
-            wait_on(mma_bar, e_commit);  // dkf
+            wait_on(&bars->cb[3], ph);  // dkf
             tmem_half_to_tile(tm + lane + Lay::T_DK, sm + Lay::P, row, g, tK);        // dK
-            wait_on(&bars->rbar, e_r);   // R_c
+            wait_on(&bars->rbar, e_r & 1u);  // R_c
+            ++e_r;
             if (q < D / 32) {
                 if (cc > 0) {
                     state_half_to_tile(tm + lane + Lay::T_R, sm + Lay::R, row, g);  // R_c
