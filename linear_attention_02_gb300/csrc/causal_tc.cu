@@ -337,9 +337,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_P, sdesc(sQ + off, 16, 1024), sdesc(sK + off, 16, 1024), ID_P,
                          k > 0 ? 1u : 0u);
             }
-            mma_state_update(sK, sV, true);
             mma_commit(mma_bar);
-            tma_store_wait_read();  // the staging tile (P area) is free again
+            mma_state_update(sK, sV, true);  // under the P epilogue; tracked by the next commit
+            tma_store_wait_read();           // the staging tile (P area) is free again
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
