@@ -113,6 +113,8 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     constexpr int PCOLS = L / Lay::GROUPS;  // columns of P per warpgroup
     constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);
     constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);
+    constexpr uint32_t ID_SV = idesc_bf16(128, M, true, true);   // phi(K)^T V
+    constexpr uint32_t ID_S1 = idesc_bf16(128, 16, true, true);  // phi(K)^T 1
     constexpr uint32_t ID_O = idesc_bf16(128, NE, false, true);
 
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -127,10 +129,14 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     uint64_t* mma_bar = tma_bar + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
     volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);  // [0] unit, [1] abort
+    uint64_t* kv_bar1 = tma_bar + 4;  // phase 1's copies into its second and third K, V buffers
+    uint64_t* kv_bar2 = tma_bar + 5;
 
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
+        mbar_init(kv_bar1, 1);
+        mbar_init(kv_bar2, 1);
         fence_mbar_init();
         sh[1] = 0;
     }
@@ -229,47 +235,62 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     };
 
     // ------------------------- phase 1: aggregate of a last segment that stops mid-head
-    // K and V alternate between their own tiles and a second buffer in the idle Q and P
-    // areas (a ones atom written after the second V), so the next chunk's copy overlaps
-    // this chunk's phi and MMA.
+    // K and V go round KV_BUFS buffers: their own tiles, the idle Q and P areas and (D = 64)
+    // the second P atom and the S tile, so KV_BUFS - 1 copies are in flight while a chunk is
+    // summed.  V no longer sits before the ones atom there, so the normaliser column takes
+    // its own N = 16 product against the ones atom.
     if (ur.publish) {
+        constexpr int KV_BUFS = D == 64 ? 3 : 2;
         const int h = ur.hB, g0 = max(ur.start, h * p.CH);
+        auto k_buf = [](int b) { return b == 0 ? Lay::K : b == 1 ? Lay::Q : Lay::P + kAtom; };
+        auto v_buf = [](int b) { return b == 0 ? Lay::V : b == 1 ? Lay::P : Lay::S; };
+        auto kv_bar = [&](int b) { return b == 0 ? tma_bar : b == 1 ? kv_bar1 : kv_bar2; };
         auto load_kv = [&](int c0, int b) {  // thread 0 only
-            mbar_arrive_expect_tx(tma_bar, Lay::TX_KV);
+            mbar_arrive_expect_tx(kv_bar(b), Lay::TX_KV);
             for (int a = 0; a < DA; ++a)
-                tma_load_3d(sm + (b ? Lay::Q : Lay::K) + a * kAtom, &tmK, tma_bar, 64 * a, c0, h);
+                tma_load_3d(sm + k_buf(b) + a * kAtom, &tmK, kv_bar(b), 64 * a, c0, h);
             for (int a = 0; a < MA; ++a)
-                tma_load_3d(sm + (b ? Lay::P : Lay::V) + a * kAtom, &tmV, tma_bar, 64 * a, c0, h);
+                tma_load_3d(sm + v_buf(b) + a * kAtom, &tmV, kv_bar(b), 64 * a, c0, h);
         };
-        for (int i = t; i < static_cast<int>(kAtom / 16); i += NT)
-            reinterpret_cast<uint4*>(sm + Lay::P + MA * kAtom)[i] =
-                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        fence_proxy_async();
+        const uint32_t sOnes = smem_u32(sm + Lay::ONES);
         // The chunks are summed last to first: the ones phase 2 reads first are then the most
         // recently read, and still in L2.
         const int n1 = ur.end - g0;
-        if (t == 0) load_kv((ur.end - 1 - h * p.CH) * L, 0);
+        const int c_last = (ur.end - 1 - h * p.CH) * L;  // the first chunk summed
+        if (t == 0)
+            for (int b = 0; b < KV_BUFS - 1 && b < n1; ++b) load_kv(c_last - b * L, b);
         for (int i1 = 0; i1 < n1; ++i1) {
-            const int gc = ur.end - 1 - i1;
-            const int c0 = (gc - h * p.CH) * L;
-            const int b = i1 & 1;
-            wait_bar(tma_bar, tma_phase);
-            if (i1 > 0) {  // the previous chunk's MMA has released the other buffer
+            const int c0 = c_last - i1 * L;
+            const int b = i1 % KV_BUFS;
+            if (t == 0 && !mbar_wait(kv_bar(b), static_cast<uint32_t>(i1 / KV_BUFS) & 1u, kWaitLimit))
+                fail(kErrWait);
+            __syncthreads();
+            if (i1 > 0) {  // the previous chunk's MMA has released its buffer
                 wait_bar(mma_bar, mma_phase);
                 fence_after_sync();
             }
-            if (t == 0 && i1 + 1 < n1) load_kv(c0 - L, b ^ 1);
-            phi_tile<true, NT>(sm + (b ? Lay::Q : Lay::K), DA, min(L, p.N - c0));
+            if (t == 0 && i1 + KV_BUFS - 1 < n1)
+                load_kv(c0 - (KV_BUFS - 1) * L, (i1 + KV_BUFS - 1) % KV_BUFS);
+            phi_tile<true, NT>(sm + k_buf(b), DA, min(L, p.N - c0));
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
             fence_after_sync();
             if (sh[1]) goto cleanup;
             if (t == 0) {
-                mma_state_update(b ? sQ : sK, b ? sP : sV, i1 > 0);
+                const uint32_t sk = smem_u32(sm + k_buf(b)), sv = smem_u32(sm + v_buf(b));
+#pragma unroll
+                for (int k = 0; k < L / 16; ++k) {
+                    const uint32_t acc = (i1 > 0 || k > 0) ? 1u : 0u;
+                    const uint64_t a = sdesc(sk + 2048 * k, kAtom, 1024);
+                    mma_bf16(tm + Lay::T_S, a, sdesc(sv + 2048 * k, kAtom, 1024), ID_SV, acc);
+                    mma_bf16(tm + Lay::T_S + M, a, sdesc(sOnes + 2048 * k, kAtom, 1024), ID_S1, acc);
+                }
                 mma_commit(mma_bar);
             }
         }
+        // slot 0's barrier carries on as phase 2's copy barrier
+        tma_phase = static_cast<uint32_t>((n1 + KV_BUFS - 1) / KV_BUFS) & 1u;
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
         if (q < D / 32) {  // rows d < D of S_ext, this warpgroup's columns
