@@ -428,8 +428,7 @@ __device__ __forceinline__ void transform_chunks(const CUtensorMap* tmQ, const C
         }
         bar_sync(kBarT, kTT);
         const int valid = min(L, N - c0);
-        phi_atom<false, kTT>(tq, valid, tt);
-        phi_atom<true, kTT>(tk, valid, tt);
+        phi_pair<kTT>(tq, tk, valid, tt);
         fence_proxy_async();
         bar_sync(kBarT, kTT);
         if (tt == 0) mbar_arrive(&bars->ready[b]);
