@@ -64,11 +64,15 @@ struct Layout {
     static constexpr uint32_t S_ATOM = D * 128;
     static constexpr uint32_t BARS = S + (MA + 1) * S_ATOM;
     static constexpr uint32_t BYTES = BARS + 64;
-    // tensor memory columns: P and O_ext share the first block, S_ext follows
+    // tensor memory columns: P (fp32, then masked and packed in place to bf16 pairs, the A
+    // operand of P [V | 1]: columns 0 .. 63 for one warpgroup, 0 .. 31 and 64 .. 95 for two),
+    // O_ext after the packed P, S_ext after O_ext
     static constexpr uint32_t T_P = 0;
-    static constexpr uint32_t T_O = 0;
-    static constexpr uint32_t T_S = NE > 128 ? 160 : 128;
+    static constexpr uint32_t T_O = GROUPS == 1 ? 64 : 128;
+    static constexpr uint32_t T_S = T_O + NE;
     static constexpr uint32_t T_COLS = T_S + NE <= 256 ? 256 : 512;
+    // packed column of K step k (16 keys) of P
+    static __device__ __forceinline__ uint32_t p_col(int k) { return GROUPS == 1 ? 8 * k : 8 * k + (k >= 4 ? 32 : 0); }
     static constexpr uint32_t TX_QKV = (2 * DA + MA) * kAtom;
     static constexpr uint32_t TX_KV = (DA + MA) * kAtom;
     // CTAs that fit on one SM: 228 KB of shared memory (1 KB reserved per CTA)
@@ -94,13 +98,6 @@ struct FwdParams {
     float* ckpt;           // [BH][ckpt_slots(CH)][W] or null: states before every 8th chunk
     unsigned* status;      // device error word
 };
-
-// Stores 64 bf16 values (packed in pk[32]) of `row` from column j0 on.
-__device__ __forceinline__ void store_row64(uint8_t* tile, uint32_t atom_bytes, int row, int j0,
-                                            const uint32_t (&pk)[32]) {
-    store_row32(tile, atom_bytes, row, j0, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-    store_row32(tile, atom_bytes, row, j0 + 32, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
-}
 
 template <int D, int M>
 __global__ void __launch_bounds__(Layout<D, M>::THREADS, Layout<D, M>::PER_SM)
@@ -158,7 +155,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const UnitRange ur(unit, p.per, p.CH, p.BH);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
-    const uint32_t sV = smem_u32(sm + Lay::V), sP = smem_u32(sm + Lay::P);
+    const uint32_t sV = smem_u32(sm + Lay::V);
     const uint32_t sS = smem_u32(sm + Lay::S);
     uint32_t tma_phase = 0, mma_phase = 0;
 
@@ -364,7 +361,8 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        {   // P: mask j > i, round to bf16, store K-major into the P tile
+        {   // P: mask j > i, round to bf16 pairs, pack in place in TMEM (each 64 columns read
+            // before their 32 packed ones are written over the first half of them)
 #pragma unroll
             for (int jb = 0; jb < PCOLS / 64; ++jb) {
                 const int j0 = g * PCOLS + jb * 64;
@@ -381,10 +379,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         pk[u] = pack_bf16(j <= row ? v[2 * u] : 0.f, j + 1 <= row ? v[2 * u + 1] : 0.f);
                     }
                 }
-                store_row64(sm + Lay::P, kAtom, row, j0, pk);
+                tmem_st32u(tm + lane + Lay::T_P + g * PCOLS + 32 * jb, pk);
             }
         }
-        fence_proxy_async();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
@@ -394,9 +391,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_bf16(tm + Lay::T_O, sdesc(sQ + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
                          sdesc(sS + 2048 * k, Lay::S_ATOM, 1024), ID_O, k > 0 ? 1u : 0u);
 #pragma unroll
-            for (int k = 0; k < L / 16; ++k)  // O_ext += P [V | 1]
-                mma_bf16(tm + Lay::T_O, sdesc(sP + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
-                         sdesc(sV + 2048 * k, kAtom, 1024), ID_O, 1u);
+            for (int k = 0; k < L / 16; ++k)  // O_ext += P [V | 1], P read from TMEM
+                mma_bf16_ts(tm + Lay::T_O, tm + Lay::T_P + Lay::p_col(k), sdesc(sV + 2048 * k, kAtom, 1024),
+                            ID_O, 1u);
             mma_commit(mma_bar);
         }
         wait_bar(mma_bar, mma_phase);
