@@ -8,7 +8,10 @@
 // The fp32 state S [D][M] is streamed once in and once out with 128-bit
 // accesses; the read-out is fused into the same pass over S (each thread
 // forms phi(q)_d * S_new[d][e] for its rows and the partial sums are reduced
-// with warp shuffles, then across warps in shared memory).
+// with warp shuffles, then across warps in shared memory).  Each thread holds
+// 8 rows of four columns where the block allows (128 threads per head at
+// D = M = 64; 4 and 16 rows measured slower), and its S loads are issued
+// before q, k and v are read, so the two latencies overlap.
 #include "la_common.cuh"
 #include "la_launch.h"
 
@@ -16,35 +19,41 @@ namespace la {
 
 namespace {
 
-constexpr int kDecThreads = 256;
+template <int D, int M, int ROWS = 8>
+struct DecShape {
+    static constexpr int CG = M / 4;  // float4 column groups of a row
+    // ROWS rows per thread where the block allows (at least two warps)
+    static constexpr int THREADS = CG * D / ROWS > 64 ? CG * D / ROWS : 64;
+    static constexpr int RG = THREADS / CG;                             // row groups
+    static constexpr int RPT = D / RG;                                  // rows per thread
+    static constexpr int WARPS = THREADS / 32;
+    static_assert(RPT >= 1 && D % RG == 0 && THREADS % 32 == 0 && CG <= 32, "shape");
+};
 
-template <typename T, int D, int M>
-__global__ void __launch_bounds__(kDecThreads)
+template <typename T, int D, int M, int ROWS = 8>
+__global__ void __launch_bounds__(DecShape<D, M, ROWS>::THREADS)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    float* __restrict__ S, float* __restrict__ Z, float* __restrict__ out, int BH) {
-    constexpr int CG = M / 4;                 // float4 column groups of a row of S
-    constexpr int RG = kDecThreads / CG;      // row groups
-    constexpr int RPT = D / RG;               // rows per thread
-    constexpr int WARPS = kDecThreads / 32;
-    static_assert(RPT >= 1 && D % RG == 0, "shape");
+    using Sh = DecShape<D, M, ROWS>;
+    constexpr int CG = Sh::CG, RG = Sh::RG, RPT = Sh::RPT, WARPS = Sh::WARPS, NT = Sh::THREADS;
     __shared__ float fq[D], fk[D], vv[M];
-    __shared__ float4 red[WARPS][CG < 32 ? CG : 32];
+    __shared__ float4 red[WARPS][CG];
     __shared__ float den_s;
     const int bh = blockIdx.x;
     const int t = threadIdx.x;
-    for (int i = t; i < D; i += kDecThreads) {
+    const int cg = t % CG, rg = t / CG;
+    float4* S4 = reinterpret_cast<float4*>(S + (size_t)bh * D * M);
+    float4 s[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) s[r] = S4[(size_t)(rg + r * RG) * CG + cg];
+    for (int i = t; i < D; i += NT) {
         fq[i] = phi(to_f(q[(size_t)bh * D + i]));
         fk[i] = phi(to_f(k[(size_t)bh * D + i]));
     }
-    for (int i = t; i < M; i += kDecThreads) vv[i] = to_f(v[(size_t)bh * M + i]);
+    for (int i = t; i < M; i += NT) vv[i] = to_f(v[(size_t)bh * M + i]);
     __syncthreads();
 
-    const int cg = t % CG, rg = t / CG;
-    float4* S4 = reinterpret_cast<float4*>(S + (size_t)bh * D * M);
     const float4 v4 = make_float4(vv[4 * cg], vv[4 * cg + 1], vv[4 * cg + 2], vv[4 * cg + 3]);
-    float4 s[RPT];
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) s[r] = (S4[(size_t)(rg + r * RG) * CG + cg]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
@@ -104,7 +113,7 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 template <typename T, int D, int M>
 cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
                         float* Z, float* out, int BH) {
-    decode_step_kernel<T, D, M><<<BH, kDecThreads, 0, c.stream>>>(q, k, v, S, Z, out, BH);
+    decode_step_kernel<T, D, M><<<BH, DecShape<D, M>::THREADS, 0, c.stream>>>(q, k, v, S, Z, out, BH);
     note_launch();
     return cudaGetLastError();
 }
