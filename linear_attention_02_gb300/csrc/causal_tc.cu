@@ -157,7 +157,10 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t sQ = smem_u32(sm + Lay::Q), sK = smem_u32(sm + Lay::K);
     const uint32_t sV = smem_u32(sm + Lay::V);
     const uint32_t sS = smem_u32(sm + Lay::S);
-    uint32_t tma_phase = 0, mma_phase = 0;
+    uint32_t mma_phase = 0;
+    // thread 0's copies issued on, and waits completed on, each copy barrier (tma_bar doubles
+    // as phase 1's first K, V buffer's), so that a CTA ending early drains what is in flight
+    uint32_t put0 = 0, put1 = 0, put2 = 0, got0 = 0, got1 = 0, got2 = 0;
 
     auto fail = [&](unsigned code) {
         atomicOr(p.status, code);
@@ -170,6 +173,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         phase ^= 1u;
     };
     auto load = [&](int h, int c0, bool with_q) {  // thread 0 only
+        ++put0;
         mbar_arrive_expect_tx(tma_bar, with_q ? Lay::TX_QKV : Lay::TX_KV);
         for (int a = 0; a < DA; ++a) {
             if (with_q) tma_load_3d(sm + Lay::Q + a * kAtom, &tmQ, tma_bar, 64 * a, c0, h);
@@ -243,6 +247,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         auto v_buf = [](int b) { return b == 0 ? Lay::V : b == 1 ? Lay::P : Lay::S; };
         auto kv_bar = [&](int b) { return b == 0 ? tma_bar : b == 1 ? kv_bar1 : kv_bar2; };
         auto load_kv = [&](int c0, int b) {  // thread 0 only
+            put0 += b == 0;
+            put1 += b == 1;
+            put2 += b == 2;
             mbar_arrive_expect_tx(kv_bar(b), Lay::TX_KV);
             for (int a = 0; a < DA; ++a)
                 tma_load_3d(sm + k_buf(b) + a * kAtom, &tmK, kv_bar(b), 64 * a, c0, h);
@@ -259,8 +266,13 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int i1 = 0; i1 < n1; ++i1) {
             const int c0 = c_last - i1 * L;
             const int b = i1 % KV_BUFS;
-            if (t == 0 && !mbar_wait(kv_bar(b), static_cast<uint32_t>(i1 / KV_BUFS) & 1u, kWaitLimit))
-                fail(kErrWait);
+            if (t == 0) {
+                const uint32_t done = b == 0 ? got0 : b == 1 ? got1 : got2;
+                if (!mbar_wait(kv_bar(b), done & 1u, kWaitLimit)) fail(kErrWait);
+                got0 += b == 0;
+                got1 += b == 1;
+                got2 += b == 2;
+            }
             __syncthreads();
             if (i1 > 0) {  // the previous chunk's MMA has released its buffer
                 wait_bar(mma_bar, mma_phase);
@@ -286,8 +298,6 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_commit(mma_bar);
             }
         }
-        // slot 0's barrier carries on as phase 2's copy barrier
-        tma_phase = static_cast<uint32_t>((n1 + KV_BUFS - 1) / KV_BUFS) & 1u;
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
         if (q < D / 32) {  // rows d < D of S_ext, this warpgroup's columns
@@ -313,6 +323,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (t == 0) st_release(p.flags + unit, 1u);
     }
 
+    // phase 2's first copy goes out now, under the look-back (it touches no state tile or TMEM)
+    if (t == 0) load(ur.hA, (ur.start - ur.hA * p.CH) * L, true);
+
     // ------------------ look-back: starting state of the first segment
     if (t == 0 && ur.look) {
         for (int sp = ur.u_first; sp < unit && !sh[1]; ++sp) {
@@ -335,12 +348,12 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     fence_after_sync();
 
     // ------------------------------------------------- phase 2: outputs
-    if (t == 0) load(ur.hA, (ur.start - ur.hA * p.CH) * L, true);
     for (int gc = ur.start; gc < ur.end; ++gc) {
         const int h = gc / p.CH, cc = gc - h * p.CH;
         const int c0 = cc * L;
         const int valid = min(L, p.N - c0);
-        wait_bar(tma_bar, tma_phase);
+        if (t == 0 && !mbar_wait(tma_bar, (got0++) & 1u, kWaitLimit)) fail(kErrWait);
+        __syncthreads();
         phi_tile<false, NT>(sm + Lay::Q, DA, valid);
         phi_tile<true, NT>(sm + Lay::K, DA, valid);
         fence_proxy_async();
@@ -479,7 +492,12 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
 
 cleanup:
-    if (t == 0) tma_store_wait_all();
+    if (t == 0) {  // copies still in flight after an early exit land before the CTA leaves
+        for (; got0 < put0; ++got0) mbar_wait(tma_bar, got0 & 1u, kWaitLimit);
+        for (; got1 < put1; ++got1) mbar_wait(kv_bar1, got1 & 1u, kWaitLimit);
+        for (; got2 < put2; ++got2) mbar_wait(kv_bar2, got2 & 1u, kWaitLimit);
+        tma_store_wait_all();
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
