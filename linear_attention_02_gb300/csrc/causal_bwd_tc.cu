@@ -118,12 +118,15 @@ constexpr uint32_t ID_D_KMN = idesc_bf16(128, D, false, true);
 constexpr uint32_t ID_M_KMN = idesc_bf16(128, M, false, true);
 
 // K-major descriptor for K step k of a tile whose 64-column atoms are `atom` bytes apart.
+// The start address is the descriptor's low field (address / 16, shared memory below
+// 256 KB), so a step is the tile's descriptor plus a constant: the MMA warp builds one
+// descriptor per operand and adds, instead of building one per K step.
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t atom) {
-    return sdesc(base + (k >> 2) * atom + 32 * (k & 3), 16, 1024);
+    return sdesc(base, 16, 1024) + (((k >> 2) * atom + 32 * (k & 3)) >> 4);
 }
 // MN-major descriptor for K step k (16 rows) of a tile whose atoms are `lbo` bytes apart.
 __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t lbo) {
-    return sdesc(base + 2048 * k, lbo, 1024);
+    return sdesc(base, lbo, 1024) + 128u * static_cast<uint32_t>(k);
 }
 
 // Reads 32 bf16 values of `row` (16-byte chunks c0 .. c0 + 3) of a swizzled
