@@ -165,6 +165,17 @@ la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void*
  * the last check, LA_ERR_CUDA if the stream reported an error, else LA_OK. */
 la_status la_check_device_status(void* stream);
 
+/* Launches one block whose two bounded device waits cannot be met -- an
+ * mbarrier phase that nothing completes and a flag that nothing sets, each
+ * given up after a few thousand polls (milliseconds) -- so that both set their
+ * bits in the current device's error word, the word and bits the library's
+ * kernels set when a copy, a product or a look-back flag never arrives.  For
+ * testing that failure path: the next la_check_device_status(stream) reports
+ * LA_ERR_TIMEOUT (code 0x3) and clears the word, and the device stays usable.
+ * Asynchronous on `stream` (a cudaStream_t, NULL for the default stream);
+ * LA_OK once launched, LA_ERR_CUDA if the launch failed. */
+la_status la_selftest_expired_waits(void* stream);
+
 /* Static text of a status code. */
 const char* la_status_string(la_status status);
 

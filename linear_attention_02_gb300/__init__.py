@@ -209,6 +209,14 @@ def la_check_device_status(stream=None):
     _check(_lib.la_check_device_status(_stream_handle(stream)))
 
 
+def la_selftest_expired_waits(stream=None):
+    """Launch a block whose bounded device waits expire (tests the error-word path).
+
+    The next la_check_device_status() raises LinAttnError with LA_ERR_TIMEOUT.
+    """
+    _check(_lib.la_selftest_expired_waits(_stream_handle(stream)))
+
+
 def la_kernel_launch_count() -> int:
     return int(_lib.la_kernel_launch_count())
 

@@ -24,6 +24,7 @@ SIGNATURES = {
     "la_forward_noncausal_noalloc": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_decode_step": [_P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _P],
     "la_check_device_status": [_P],
+    "la_selftest_expired_waits": [_P],
     "la_status_string": [_I],
     "la_last_error_message": [],
     "la_kernel_launch_count": [],

@@ -319,6 +319,13 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
     return finish(dispatch<Decode>(dtype, D, M, &ctx, q, k, v, S, Z, out, (int)((size_t)B * H)), fn);
 }
 
+la_status la_selftest_expired_waits(void* stream) {
+    LaunchCtx ctx;
+    la_status s = get_ctx((cudaStream_t)stream, &ctx);
+    if (s != LA_OK) return s;
+    return finish(selftest_expired_waits(ctx), "la_selftest_expired_waits");
+}
+
 la_status la_check_device_status(void* stream) {
     LaunchCtx ctx;
     la_status s = get_ctx((cudaStream_t)stream, &ctx);

@@ -30,6 +30,8 @@ constexpr int kCkptChunks = 8;
 
 // Stream-ordered scratch from the library pool.  Returns cudaSuccess or the error.
 cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes);
+// One block whose bounded waits expire and set their bits in c.status_word.
+cudaError_t selftest_expired_waits(const LaunchCtx& c);
 void scratch_free(const LaunchCtx& c, void* p);
 
 // Each launcher returns cudaSuccess or the first CUDA error it met.
