@@ -341,11 +341,15 @@ constexpr int kCT = kT0 + kTT;            // threads per CTA
 constexpr int kEM = kBT + 32;             // compute warps + MMA warp
 // Named barriers: compute warps among themselves; transform warps; compute ->
 // MMA warp hand-overs (compute warps arrive, the MMA warp waits); MMA warp ->
-// compute hand-overs (the MMA warp arrives, the compute warps wait).  Each
-// side meets each hand-over barrier alternately with the other side, so no
-// arrival can fall into the previous use.
+// compute hand-overs (the MMA warp arrives, the compute warps wait).  Within a
+// chunk every compute -> MMA hand-over has its own barrier (kBarEM, kBarEM2,
+// kBarEM3), and the compute warps wait at kBarME once a chunk, which the MMA
+// warp passes only after it has taken all of the previous chunk's hand-overs:
+// so no side arrives at a barrier twice before the other has met the first
+// arrival, whatever the (bounded, after a timeout short) mbarrier waits do.
 constexpr uint32_t kBarE = 3, kBarT = 2, kBarEM = 1, kBarME = 4;
-constexpr uint32_t kBarEM2 = 5;  // a second compute -> MMA warp hand-over within a chunk
+constexpr uint32_t kBarEM2 = 5;  // the second compute -> MMA warp hand-over of a chunk
+constexpr uint32_t kBarEM3 = 6;  // the third
 
 // Hand-over among the compute warps when they issue MMAs themselves (phase 1):
 // their shared-memory writes become visible to the tensor core and TMA, and
@@ -728,7 +732,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (more) book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
             }
             __syncwarp();
-            take_from_compute();  // dP is masked and packed in TMEM
+            take_from_compute(kBarEM2);  // dP is masked and packed in TMEM
             if (lead) {
                 tma_store_wait_read_but_last();  // the previous dQ store is read out: the staging
                                                  // tile is free once this chunk's MMA3 commits
@@ -742,7 +746,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mma_commit(&bars->rbar);
             }
             __syncwarp();
-            take_from_compute();  // dQ staged, S_c copied
+            take_from_compute(kBarEM3);  // dQ staged, S_c copied
             if (lead) {
                 tma_store_3d(&tmdQ, sm + Lay::P, 0, c0, bh);
                 tma_store_commit();
@@ -805,7 +809,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             hand_to_mma();
             wait_mma();  // dP (and the S update before it)
             masked_half_to_tmem(tm + lane + Lay::T_P, row, q, g);  // dP, masked, bf16 in TMEM
-            hand_to_mma();
+            hand_to_mma(kBarEM2);
             wait_mma();  // dqf complete
             if (q < D / 32) {
                 if (ur.look && gc == first_end - 1)  // the first piece is complete: publish its R share
@@ -820,7 +824,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 }
             }
             tmem_half_to_tile(tm + lane + Lay::T_DQ, sm + Lay::P, row, g, tQ);  // dQ
-            hand_to_mma();
+            hand_to_mma(kBarEM3);
         }
     }
 
@@ -1001,7 +1005,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 }
             }
             __syncwarp();
-            take_from_compute();  // dK, dV staged, R_c copied
+            take_from_compute(kBarEM3);  // dK, dV staged, R_c copied
             if (lead) {
                 tma_store_3d(&tmdK, sm + Lay::P, 0, c0, bh);
                 tma_store_3d(&tmdV, sm + Lay::DP, 0, c0, bh);
@@ -1045,7 +1049,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     put_state_half(tm + lane + Lay::T_R, sm + Lay::R, row, g, zero, 0.f, 0.f);
                 }
             }
-            hand_to_mma();
+            hand_to_mma(kBarEM3);
         }
     }
 
