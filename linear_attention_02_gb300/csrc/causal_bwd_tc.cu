@@ -87,9 +87,9 @@ struct LayR {
     static constexpr uint32_t Q0 = 0, Q1 = kAtom, K0 = 2 * kAtom, K1 = 3 * kAtom;  // two buffers each
     static constexpr uint32_t V = 4 * kAtom, ONES = 5 * kAtom;
     static constexpr uint32_t GH = 6 * kAtom;
-    static constexpr uint32_t P = 8 * kAtom;     // P (bf16), then the dK staging tile
-    static constexpr uint32_t DP = 10 * kAtom;   // dP (bf16), then the dV staging tile
-    static constexpr uint32_t R = 12 * kAtom;    // [R | r 0..0] bf16, 2 atoms of D rows
+    static constexpr uint32_t P = 8 * kAtom;     // the dK staging tile
+    static constexpr uint32_t DP = 9 * kAtom;    // the dV staging tile
+    static constexpr uint32_t R = 10 * kAtom;    // [R | r 0..0] bf16, 2 atoms of D rows
     static constexpr uint32_t BARS = R + 2 * S_ATOM;
     static constexpr uint32_t BYTES = BARS + 128;
     static constexpr uint32_t T_P = 0, T_DP = 128, T_DV = 256, T_DK = 320, T_R = 384;
