@@ -16,8 +16,9 @@
 //   S_ext [128 x NE]   A = phi(K_c)^T MN-major (D = 64 pads to 128 rows whose
 //                      extra rows are never read), B = [V_c | 1] MN-major
 //   O_ext [128 x NE]   A = phi(Q_c) K-major, B = [S | Z] (bf16 copy) MN-major
-//                      then A = P (bf16, masked) K-major, B = [V_c | 1]
-// Tiles arrive by TMA with the 128-byte swizzle; P, the bf16 state and the
+//                      then A = P (bf16, masked, packed in place in TMEM),
+//                      B = [V_c | 1] MN-major
+// Tiles arrive by TMA with the 128-byte swizzle; the bf16 state and the
 // output tile are written by the threads in the same swizzled layout.
 //
 // Work split: the chunks of all heads, head-major, are cut into equal ranges,
@@ -59,7 +60,8 @@ struct Layout {
     static constexpr uint32_t K = Q + DA * kAtom;
     static constexpr uint32_t V = K + DA * kAtom;      // V atoms, then the ones atom
     static constexpr uint32_t ONES = V + MA * kAtom;
-    static constexpr uint32_t P = ONES + kAtom;        // 2 atoms; also the output staging tile
+    static constexpr uint32_t P = ONES + kAtom;        // 2 atoms: the output staging tile (MA atoms),
+                                                       // and phase 1's K, V buffers
     static constexpr uint32_t S = P + 2 * kAtom;       // (MA + 1) atoms of D rows
     static constexpr uint32_t S_ATOM = D * 128;
     static constexpr uint32_t BARS = S + (MA + 1) * S_ATOM;
