@@ -7,8 +7,10 @@ tokens/s counts (b, n) positions across all heads: B*N tokens per step.
 
 Also measured in the same run (the "paths" object): the causal forward alone,
 the long-sequence forward (B=1, H=16, N=65536, D=M=128), the non-causal fp32
-forward (B=8, H=8, N=4096, D=M=64) and one decode step of 256 sequences x 16
-heads (D=M=64, fp32 state), each with its fraction of the HBM roofline.
+forward (B=8, H=8, N=4096, D=M=64), one decode step of 256 sequences x 16
+heads (D=M=64, fp32 state) and the 2048-token prefill that hands the decode
+its state (the causal forward emitting the final S, Z of every head), each
+with its fraction of the HBM roofline.
 
 Timing: W untimed warm-up steps, then K steps between a barrier and a device
 synchronize, timed with CUDA events on the launching stream; max over ranks.
@@ -432,6 +434,19 @@ def measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_
     res["decode_bf16/step"] = entry(ms, _bytes_decode(B, H, D, M, 2), B,
                                     {"l2": "flushed before each step",
                                      "ms_l2_warm": round(ms_warm, 5)})
+    del S, Z, steps, out, flush_buf
+
+    # the prefill that hands the decode its state: the causal forward over every sequence's
+    # prompt, emitting the final S, Z of each head (inputs larger than L2)
+    x = synth.qkv(B, H, w.prefill, D, M, w.dtype, w.seed, w.scale, device="cuda")
+    O = torch.empty_like(x["V"])
+    f = lambda: la.la_forward_causal(x["Q"], x["K"], x["V"], out=O, return_state=True)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 10, stream)
+    res["decode_bf16/prefill"] = entry(ms, _bytes_fwd(B, H, w.prefill, D, M, 2) + B * H * (D * M + D) * 4,
+                                       B * w.prefill)
+    del x, O
     return res
 
 
