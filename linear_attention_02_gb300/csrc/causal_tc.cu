@@ -64,7 +64,12 @@ struct Layout {
                                                        // and phase 1's K, V buffers
     static constexpr uint32_t S = P + 2 * kAtom;       // (MA + 1) atoms of D rows
     static constexpr uint32_t S_ATOM = D * 128;
-    static constexpr uint32_t BARS = S + (MA + 1) * S_ATOM;
+    // phase 1's third K, V buffer: the second P atom and the S tile (D = 64), the S tile and
+    // 16 KB after it (D = 128)
+    static constexpr uint32_t KV2_K = D == 64 ? P + kAtom : S;
+    static constexpr uint32_t KV2_V = D == 64 ? S : S + DA * kAtom;
+    static constexpr uint32_t BARS = S + (MA + 1) * S_ATOM > KV2_V + MA * kAtom ? S + (MA + 1) * S_ATOM
+                                                                                 : KV2_V + MA * kAtom;
     static constexpr uint32_t BYTES = BARS + 64;
     // tensor memory columns: P (fp32, then masked and packed in place to bf16 pairs, the A
     // operand of P [V | 1]: columns 0 .. 63 for one warpgroup, 0 .. 31 and 64 .. 95 for two),
@@ -238,15 +243,15 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     };
 
     // ------------------------- phase 1: aggregate of a last segment that stops mid-head
-    // K and V go round KV_BUFS buffers: their own tiles, the idle Q and P areas and (D = 64)
-    // the second P atom and the S tile, so KV_BUFS - 1 copies are in flight while a chunk is
-    // summed.  V no longer sits before the ones atom there, so the normaliser column takes
+    // K and V go round three buffers: their own tiles, the idle Q and P areas, and the
+    // third buffer of the layout (the S area is idle too), so two copies are in flight while a
+    // chunk is summed.  V no longer sits before the ones atom there, so the normaliser column takes
     // its own N = 16 product against the ones atom.
     if (ur.publish) {
-        constexpr int KV_BUFS = D == 64 ? 3 : 2;
+        constexpr int KV_BUFS = 3;
         const int h = ur.hB, g0 = max(ur.start, h * p.CH);
-        auto k_buf = [](int b) { return b == 0 ? Lay::K : b == 1 ? Lay::Q : Lay::P + kAtom; };
-        auto v_buf = [](int b) { return b == 0 ? Lay::V : b == 1 ? Lay::P : Lay::S; };
+        auto k_buf = [](int b) { return b == 0 ? Lay::K : b == 1 ? Lay::Q : Lay::KV2_K; };
+        auto v_buf = [](int b) { return b == 0 ? Lay::V : b == 1 ? Lay::P : Lay::KV2_V; };
         auto kv_bar = [&](int b) { return b == 0 ? tma_bar : b == 1 ? kv_bar1 : kv_bar2; };
         auto load_kv = [&](int c0, int b) {  // thread 0 only
             put0 += b == 0;
