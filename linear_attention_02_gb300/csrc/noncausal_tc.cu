@@ -34,7 +34,7 @@ namespace tcn {
 using namespace la::tcf;
 
 constexpr int D = 64, M = 64, NE = M + 16, W = D * M + D;
-constexpr int NT = 128;
+constexpr int NT = 256;  // two warpgroups; two CTAs share an SM
 constexpr uint32_t S_ATOM = D * 128;  // 64 state rows x 128 bytes
 
 constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);   // kf^T [V | 1]
@@ -80,13 +80,14 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
 
 // In place: the fp32 [128 x 64] tile at `buf` becomes bf16 hi (buf) and lo
 // (buf + 16 KB), each one K-major 128-row atom; phi is applied first when PHI,
-// and rows >= valid become 0 when ZERO_TAIL.  Each thread reads its eight
+// and rows >= valid become 0 when ZERO_TAIL.  Each thread reads its
 // (row, 8-column) groups before any thread writes.
 template <bool PHI, bool ZERO_TAIL>
 __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
-    float x[8][8];
+    constexpr int IT = 1024 / NT;  // (row, 8-column) groups per thread
+    float x[IT][8];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < IT; ++it) {
         const int item = threadIdx.x + NT * it;
         const int r = item >> 3, j = item & 7;
         const uint4 a = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j));
@@ -102,7 +103,7 @@ __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
     }
     __syncthreads();
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < IT; ++it) {
         const int item = threadIdx.x + NT * it;
         const int r = item >> 3, j = item & 7;
         uint32_t h[4], l[4];
@@ -172,7 +173,8 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     const int bh = unit / p.spans, s = unit - bh * p.spans;
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
     const int nch = (n1 - n0 + L - 1) / L;
-    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V);
     uint32_t tma_phase = 0, mma_phase = 0;
 
@@ -223,18 +225,20 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         fence_after_sync();
         if (t == 0 && c + 1 < nch) load(c0 + L);
     }
-    if (warp < D / 32) {  // publish the span's [S | Z] (rows d < D)
+    if (q < D / 32) {  // publish the span's [S | Z]: row d < D, this warpgroup's 32 columns
         float* out = p.part + static_cast<size_t>(unit) * W;
-        const int d = t;
-        float v[64];
-        tmem_ld64(tm + lane, v);
+        const int d = 32 * q + (t & 31);
+        float v[32];
+        tmem_ld32(tm + lane + 32 * g, v);
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-            reinterpret_cast<float4*>(out + d * M)[u] =
+        for (int u = 0; u < 8; ++u)
+            reinterpret_cast<float4*>(out + d * M + 32 * g)[u] =
                 make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        float z[16];
-        tmem_ld16(tm + lane + M, z);
-        out[D * M + d] = z[0];
+        if (g == 0) {
+            float z[16];
+            tmem_ld16(tm + lane + M, z);
+            out[D * M + d] = z[0];
+        }
     }
 
 cleanup:
@@ -278,7 +282,8 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int bh = unit / p.out_spans, s = unit - bh * p.out_spans;
     const int n0 = s * p.out_len, n1 = min(p.N, n0 + p.out_len);
     const int nch = (n1 - n0 + L - 1) / L;
-    const uint32_t lane = static_cast<uint32_t>(32 * warp) << 16;
+    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sS = smem_u32(sm + Lay::S);
     uint32_t tma_phase = 0, mma_phase = 0;
 
@@ -298,10 +303,11 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     };
     if (t == 0) load(n0);
 
-    if (warp < D / 32) {  // [S | Z] of the head, split into hi and lo MN-major tiles
-        const int d = t;
+    if (q < D / 32) {  // [S | Z] of the head, split into hi and lo MN-major tiles: row d, this
+                       // warpgroup's 32 columns (and Z for the first)
+        const int d = 32 * q + (t & 31);
         const float* base = p.part + static_cast<size_t>(bh) * p.spans * W;
-        for (int j0 = 0; j0 < M; j0 += 8) {
+        for (int j0 = 32 * g; j0 < 32 * g + 32; j0 += 8) {
             float v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) v[u] = 0.f;
@@ -331,16 +337,18 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             *reinterpret_cast<uint4*>(sm + Lay::S + 2 * S_ATOM + swz(d, j0 >> 3)) =
                 make_uint4(l[0], l[1], l[2], l[3]);
         }
-        float z = 0.f;
-        for (int sp = 0; sp < p.spans; ++sp) z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
-        float zh, zl;
-        split_bf16(z, zh, zl);
-        const uint32_t ph = pack_bf16(zh, zh), pl = pack_bf16(zl, zl);
-        const uint4 hz = make_uint4(ph, ph, ph, ph), lz = make_uint4(pl, pl, pl, pl);
-        *reinterpret_cast<uint4*>(sm + Lay::S + S_ATOM + swz(d, 0)) = hz;
-        *reinterpret_cast<uint4*>(sm + Lay::S + S_ATOM + swz(d, 1)) = hz;
-        *reinterpret_cast<uint4*>(sm + Lay::S + 3 * S_ATOM + swz(d, 0)) = lz;
-        *reinterpret_cast<uint4*>(sm + Lay::S + 3 * S_ATOM + swz(d, 1)) = lz;
+        if (g == 0) {
+            float z = 0.f;
+            for (int sp = 0; sp < p.spans; ++sp) z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+            float zh, zl;
+            split_bf16(z, zh, zl);
+            const uint32_t ph = pack_bf16(zh, zh), pl = pack_bf16(zl, zl);
+            const uint4 hz = make_uint4(ph, ph, ph, ph), lz = make_uint4(pl, pl, pl, pl);
+            *reinterpret_cast<uint4*>(sm + Lay::S + S_ATOM + swz(d, 0)) = hz;
+            *reinterpret_cast<uint4*>(sm + Lay::S + S_ATOM + swz(d, 1)) = hz;
+            *reinterpret_cast<uint4*>(sm + Lay::S + 3 * S_ATOM + swz(d, 0)) = lz;
+            *reinterpret_cast<uint4*>(sm + Lay::S + 3 * S_ATOM + swz(d, 1)) = lz;
+        }
     }
 
     for (int c = 0; c < nch; ++c) {
@@ -369,16 +377,16 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
         if (t == 0 && c + 1 < nch) load(c0 + L);  // the Q tile is consumed
-        {   // V' = num / den, fp32 into the swizzled staging tile
-            const int i = t;
+        {   // V' = num / den, this warpgroup's 32 columns, fp32 into the swizzled staging tile
+            const int i = 32 * q + (t & 31);
             float dz[16];
             tmem_ld16(tm + lane + M, dz);
             const float inv = 1.f / dz[0];
-            float v[64];
-            tmem_ld64(tm + lane, v);
+            float v[32];
+            tmem_ld32(tm + lane + 32 * g, v);
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                *reinterpret_cast<float4*>(sm + Lay::OUT + f32_off(i, 4 * u)) =
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(sm + Lay::OUT + f32_off(i, 32 * g + 4 * u)) =
                     make_float4(v[4 * u] * inv, v[4 * u + 1] * inv, v[4 * u + 2] * inv,
                                 v[4 * u + 3] * inv);
         }
