@@ -11,9 +11,8 @@
 // the lo parts are about 2^-17 of |a b|), accumulated in fp32 in TMEM.  The
 // ones block appended to V carries the normaliser through the same products.
 //
-//   state kernel   one CTA per (head, span), in steps of 64 tokens: TMA loads
-//                  fp32 K, V tiles into a ring of three buffers (two copies in
-//                  flight); phi and the split are done in place (the fp32 tile
+//   state kernel   one CTA per (head, span): TMA loads fp32 K, V tiles of 128
+//                  tokens; phi and the split are done in place (the fp32 tile
 //                  becomes its hi and lo bf16 tiles); the MMAs accumulate
 //                  [S | Z] for the span, published as fp32 partials;
 //   read-out kernel one CTA per (head, span): sums the partials of the head,
@@ -39,24 +38,16 @@ constexpr int NT = 256;  // two warpgroups; two CTAs share an SM
 constexpr uint32_t S_ATOM = D * 128;  // 64 state rows x 128 bytes
 
 constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);   // kf^T [V | 1]
-constexpr uint32_t ID_S64 = idesc_bf16(128, M, true, true);  // kf^T V
 constexpr uint32_t ID_O = idesc_bf16(128, NE, false, true);  // qf [S | Z]
 
-// state kernel shared memory: a ring of three buffers, each an fp32 K tile and
-// an fp32 V tile of 64 tokens (two 32-column atoms of 8 KB; after the split,
-// the hi and lo bf16 tiles), then a ones atom.  [V_hi | 1] is an MN-major
-// operand whose second atom is reached through the descriptor's atom stride
-// ONES - V_hi; the V_lo product takes N = 64 (its normaliser column is 0).
-constexpr int HL = 64;            // tokens per step of the state kernel
-constexpr uint32_t HATOM = 8192;  // 64 rows x 128 bytes
+// state kernel shared memory: K tile (fp32, then hi | lo bf16), V tile (fp32,
+// then hi | lo bf16) followed by a ones atom and a zeros atom, so that
+// [V_hi | 1] and [V_lo | 0] are operands with a 32 KB atom stride.
 struct LayA {
-    static constexpr int BUFS = 3;
-    static constexpr uint32_t PAIR = 4 * HATOM;  // K (2 atoms), V (2 atoms)
-    static constexpr uint32_t ONES = BUFS * PAIR;
-    static constexpr uint32_t BARS = ONES + kAtom;
+    static constexpr uint32_t K = 0, V = 2 * kAtom, ONES = 4 * kAtom, ZEROS = 5 * kAtom;
+    static constexpr uint32_t BARS = 6 * kAtom;
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_COLS = 128;
-    static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
 };
 
 // read-out kernel shared memory: Q tile (fp32, then hi | lo bf16), state tiles
@@ -76,10 +67,9 @@ struct NcParams {
     unsigned* status;
 };
 
-// Byte offset of fp32 element (r, c), c < 64, in a tile of two 32-column atoms
-// `atom` bytes apart.
-__device__ __forceinline__ uint32_t f32_off(int r, int c, uint32_t atom = kAtom) {
-    return (c >> 5) * atom + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4;
+// Byte offset of fp32 element (r, c), c < 64, in a tile of two 32-column atoms.
+__device__ __forceinline__ uint32_t f32_off(int r, int c) {
+    return (c >> 5) * kAtom + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4;
 }
 
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
@@ -92,52 +82,6 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
 // (buf + 16 KB), each one K-major 128-row atom; phi is applied first when PHI,
 // and rows >= valid become 0 when ZERO_TAIL.  Each thread reads its
 // (row, 8-column) groups before any thread writes.
-// The same for a 64-row tile whose 32-column fp32 atoms are HATOM bytes apart;
-// hi at buf, lo at buf + HATOM.
-template <bool PHI, bool ZERO_TAIL>
-__device__ __forceinline__ void split_half(uint8_t* buf, int valid) {
-    constexpr int IT = 512 / NT;  // (row, 8-column) groups per thread
-    float x[IT][8];
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int item = threadIdx.x + NT * it;
-        const int r = item >> 3, j = item & 7;
-        const uint4 a = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j, HATOM));
-        const uint4 b = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j + 4, HATOM));
-        x[it][0] = __uint_as_float(a.x);
-        x[it][1] = __uint_as_float(a.y);
-        x[it][2] = __uint_as_float(a.z);
-        x[it][3] = __uint_as_float(a.w);
-        x[it][4] = __uint_as_float(b.x);
-        x[it][5] = __uint_as_float(b.y);
-        x[it][6] = __uint_as_float(b.z);
-        x[it][7] = __uint_as_float(b.w);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int item = threadIdx.x + NT * it;
-        const int r = item >> 3, j = item & 7;
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float v0 = x[it][2 * u], v1 = x[it][2 * u + 1];
-            if (PHI) {
-                v0 = phi_fast(v0);
-                v1 = phi_fast(v1);
-            }
-            if (ZERO_TAIL && r >= valid) v0 = v1 = 0.f;
-            float h0, l0, h1, l1;
-            split_bf16(v0, h0, l0);
-            split_bf16(v1, h1, l1);
-            h[u] = pack_bf16(h0, h1);
-            l[u] = pack_bf16(l0, l1);
-        }
-        *reinterpret_cast<uint4*>(buf + swz(r, j)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(buf + HATOM + swz(r, j)) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
-}
-
 template <bool PHI, bool ZERO_TAIL>
 __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
     constexpr int IT = 1024 / NT;  // (row, 8-column) groups per thread
@@ -201,16 +145,13 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
     }
-    // barriers: a copy barrier per ring buffer, an MMA barrier per step parity (step j commits
-    // to mma_bar[j & 1] and is waited for before step j + 2 commits there), TMEM address, abort
-    uint64_t* copy_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
-    uint64_t* mma_bar = copy_bar + Lay::BUFS;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 2);
-    volatile int* sh = reinterpret_cast<volatile int*>(mma_bar + 3);
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+    uint64_t* mma_bar = tma_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
+    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
     if (t == 0) {
-        for (int i = 0; i < Lay::BUFS; ++i) mbar_init(copy_bar + i, 1);
+        mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
-        mbar_init(mma_bar + 1, 1);
         fence_mbar_init();
         sh[1] = 0;
     }
@@ -218,9 +159,11 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         tmem_alloc(tmem_slot, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += NT)
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += NT) {
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        reinterpret_cast<uint4*>(sm + Lay::ZEROS)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -229,74 +172,59 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     const int unit = blockIdx.x;
     const int bh = unit / p.spans, s = unit - bh * p.spans;
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
-    const int nst = (n1 - n0 + HL - 1) / HL;  // steps of HL tokens
+    const int nch = (n1 - n0 + L - 1) / L;
     const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    uint32_t put[Lay::BUFS] = {0u, 0u, 0u}, got[Lay::BUFS] = {0u, 0u, 0u};  // thread 0's copies
+    const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V);
+    uint32_t tma_phase = 0, mma_phase = 0;
 
     auto fail = [&](unsigned code) {
         atomicOr(p.status, code);
         sh[1] = 1;
     };
-    auto wait_mma = [&](int j) {  // step j's products
-        if (t == 0 && !mbar_wait(mma_bar + (j & 1), (static_cast<uint32_t>(j) >> 1) & 1u, kWaitLimit))
-            fail(kErrWait);
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
         __syncthreads();
-        fence_after_sync();
+        phase ^= 1u;
     };
-    auto load = [&](int i) {  // thread 0: step i into ring buffer i % BUFS
-        const int b = i % Lay::BUFS, c0 = n0 + i * HL;
-        uint8_t* const pk = sm + b * Lay::PAIR;
-        uint64_t* const bar = copy_bar + b;
-        ++put[b];
-        mbar_arrive_expect_tx(bar, 4 * HATOM);
-        tma_load_3d(pk, &tmK, bar, 0, c0, bh);
-        tma_load_3d(pk + HATOM, &tmK, bar, 32, c0, bh);
-        tma_load_3d(pk + 2 * HATOM, &tmV, bar, 0, c0, bh);
-        tma_load_3d(pk + 3 * HATOM, &tmV, bar, 32, c0, bh);
+    auto load = [&](int c0) {
+        mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
+        tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0, bh);
+        tma_load_3d(sm + Lay::K + kAtom, &tmK, tma_bar, 32, c0, bh);
+        tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0, bh);
+        tma_load_3d(sm + Lay::V + kAtom, &tmV, tma_bar, 32, c0, bh);
     };
 
-    if (t == 0)
-        for (int i = 0; i < Lay::BUFS && i < nst; ++i) load(i);
-    for (int h = 0; h < nst; ++h) {
-        const int c0 = n0 + h * HL;
-        const int valid = min(HL, n1 - c0);
-        const int b = h % Lay::BUFS;
-        uint8_t* const pk = sm + b * Lay::PAIR;
-        if (t == 0) {
-            if (!mbar_wait(copy_bar + b, got[b] & 1u, kWaitLimit)) fail(kErrWait);
-            ++got[b];
-        }
-        __syncthreads();
-        split_half<true, true>(pk, valid);              // K: phi, rows past the span zeroed
-        split_half<false, false>(pk + 2 * HATOM, valid);  // V (rows past the head arrive as zeros)
+    if (t == 0) load(n0);
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = n0 + c * L;
+        const int valid = min(L, n1 - c0);
+        wait_bar(tma_bar, tma_phase);
+        split_tile<true, true>(sm + Lay::K, valid);
+        split_tile<false, false>(sm + Lay::V, valid);
         sync_tc();
         if (sh[1]) goto cleanup;
         if (t == 0) {
-            // K_hi^T [V_hi | 1] + K_hi^T V_lo + K_lo^T [V_hi | 1]; the D = 64 rows pad to 128
-            // through the A operand's atom stride (rows never read)
-            const uint32_t sK = smem_u32(pk), sV = smem_u32(pk + 2 * HATOM);
-            const uint32_t lbo = Lay::ONES - (b * Lay::PAIR + 2 * HATOM);  // V_hi -> the ones atom
+            // K_hi^T [V_hi | 1] + K_hi^T [V_lo | 0] + K_lo^T [V_hi | 1]; the D = 64
+            // rows pad to 128 through the A operand's atom stride (rows never read)
 #pragma unroll
-            for (int k = 0; k < HL / 16; ++k)
-                mma_bf16(tm, sdesc(sK + 2048 * k, HATOM, 1024), sdesc(sV + 2048 * k, lbo, 1024), ID_S,
-                         (h > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < L / 16; ++k)
+                mma_bf16(tm, sdesc(sK + 2048 * k, kAtom, 1024), sdesc(sV + 2048 * k, 2 * kAtom, 1024),
+                         ID_S, (c > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
-            for (int k = 0; k < HL / 16; ++k)
-                mma_bf16(tm, sdesc(sK + 2048 * k, HATOM, 1024), sdesc(sV + HATOM + 2048 * k, HATOM, 1024),
-                         ID_S64, 1u);
+            for (int k = 0; k < L / 16; ++k)
+                mma_bf16(tm, sdesc(sK + 2048 * k, kAtom, 1024),
+                         sdesc(sV + kAtom + 2048 * k, 2 * kAtom, 1024), ID_S, 1u);
 #pragma unroll
-            for (int k = 0; k < HL / 16; ++k)
-                mma_bf16(tm, sdesc(sK + HATOM + 2048 * k, HATOM, 1024), sdesc(sV + 2048 * k, lbo, 1024),
-                         ID_S, 1u);
-            mma_commit(mma_bar + (h & 1));
+            for (int k = 0; k < L / 16; ++k)
+                mma_bf16(tm, sdesc(sK + kAtom + 2048 * k, kAtom, 1024),
+                         sdesc(sV + 2048 * k, 2 * kAtom, 1024), ID_S, 1u);
+            mma_commit(mma_bar);
         }
-        if (h > 0) {  // the previous step's products are done: its buffer takes step h + 2
-            wait_mma(h - 1);
-            if (t == 0 && h + Lay::BUFS - 1 < nst) load(h + Lay::BUFS - 1);
-        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        if (t == 0 && c + 1 < nch) load(c0 + L);
     }
-    if (nst > 0) wait_mma(nst - 1);
     if (q < D / 32) {  // publish the span's [S | Z]: row d < D, this warpgroup's 32 columns
         float* out = p.part + static_cast<size_t>(unit) * W;
         const int d = 32 * q + (t & 31);
@@ -314,9 +242,6 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
 
 cleanup:
-    if (t == 0)  // copies still in flight after an early exit land before the CTA leaves
-        for (int i = 0; i < Lay::BUFS; ++i)
-            for (; got[i] < put[i]; ++got[i]) mbar_wait(copy_bar + i, got[i] & 1u, kWaitLimit);
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
@@ -529,8 +454,8 @@ cudaError_t noncausal_forward_tc_f32(const LaunchCtx& c, const float* Q, const f
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&p.part), part_bytes)) != cudaSuccess) return e;
     do {
         CUtensorMap mQ, mK, mV, mO;
-        if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D, HL)) ||
-            (e = make_map_f32(&mV, V, BH, N, M, HL)) || (e = make_map_f32(&mO, O, BH, N, M)))
+        if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D)) ||
+            (e = make_map_f32(&mV, V, BH, N, M)) || (e = make_map_f32(&mO, O, BH, N, M)))
             break;
         ka<<<BH * p.spans, NT, LayA::BYTES, c.stream>>>(mK, mV, p);
         kb<<<BH * p.out_spans, NT, LayB::BYTES, c.stream>>>(mQ, mO, p);
