@@ -1,0 +1,44 @@
+"""bench.py's contract, on the host: the reference arm's JSON line, and the traffic bookkeeping."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_json_line_with_the_contract_keys():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_measured_on(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "linear_attention_02_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.TRAFFIC_SOURCES:
+        (csrc / f).write_text("// " + f)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench._csrc_hash()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"op": {"dram_bytes_per_launch": 123,
+                                                                            "csrc_hash": h}}))
+    assert bench._traffic("op") == 123
+    assert bench._traffic("other op") is None
+    (csrc / "ffma_f32.cu").write_text("// another op's kernel")  # not a source of the measured kernels
+    assert bench._traffic("op") == 123
+    (csrc / bench.TRAFFIC_SOURCES[0]).write_text("// changed")    # the measured kernel changed
+    assert bench._traffic("op") is None
