@@ -488,9 +488,8 @@ def run_reference(args):
     samples = [cpu_baseline(synth) for _ in range(args.steps)]
     wall = time.perf_counter() - t0
     v = statistics.mean(s["value"] for s in samples)
-    tokens_per_sample = v * (wall / max(args.steps, 1))
     out = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "tokens/s",
-           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(wall / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": f"{HEADLINE}: causal linear attention fwd+bwd, B={w.B} H={w.H} "
@@ -500,7 +499,6 @@ def run_reference(args):
                             "cores": samples[0]["cores"], "sample": samples[0]["sample"]},
            "e2e": {"value": round(v, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
-    del tokens_per_sample
     print(json.dumps(out), flush=True)
     return out
 

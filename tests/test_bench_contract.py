@@ -42,3 +42,19 @@ def test_traffic_is_reported_only_for_the_sources_it_was_measured_on(tmp_path, m
     assert bench._traffic("op") == 123
     (csrc / bench.TRAFFIC_SOURCES[0]).write_text("// changed")    # the measured kernel changed
     assert bench._traffic("op") is None
+
+
+def test_reference_arm_under_two_ranks_prints_once_from_rank_0():
+    import socket
+    with socket.socket() as sck:
+        sck.bind(("127.0.0.1", 0))
+        port = sck.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port),
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
