@@ -85,7 +85,7 @@ def _traffic(key: str):
 class ClockSampler:
     """SM clocks and clock-event (throttle) reasons sampled during the timed region.
 
-    Polls NVML (read-only queries through ctypes) every 2 ms on the GPU the
+    Polls NVML (read-only queries through ctypes) every 0.5 ms on the GPU the
     process runs on, matched by PCI bus id; falls back to nvidia-smi at its
     100 ms minimum interval when NVML cannot be loaded."""
 
@@ -130,7 +130,7 @@ class ClockSampler:
                     lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0):
                 r = self._reasons_fn(h, ctypes.byref(rs))
                 self.samples.append((cur.value, mx.value, rs.value if r == 0 else 0))
-            time.sleep(0.002)
+            time.sleep(0.0005)
 
     def _poll_smi(self):
         cmd = ["nvidia-smi", "-i", str(self.cuda_index), "--query-gpu=clocks.sm,clocks.max.sm,"
@@ -344,9 +344,11 @@ def run_ours(args):
                 "algorithmic_bytes": dom_bytes, "avg_ms": round(dom_ms, 5)}
 
     paths = None
+    clk_paths = None
     if not args.no_paths:
-        paths = measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_bytes,
-                              B * N)
+        with ClockSampler(local) as clk_paths:
+            paths = measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_bytes,
+                                  B * N)
 
     if world > 1:
         dist.barrier()
@@ -374,6 +376,7 @@ def run_ours(args):
             "gpu_launches": launches,
             "clocks": clocks,
             "paths": paths,
+            "clocks_paths": clk_paths.summary() if clk_paths is not None else None,
         }
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(synth)
@@ -476,11 +479,23 @@ def cpu_baseline(synth, steps: int = 1):
                       f"forward + cumulative-sum backward, {dt:.2f} s per sample"}
 
 
+def _synth_module():
+    """The seeded input generator, loaded by path: importing it through the package
+    would load the CUDA library, which the CPU-only reference arm must not touch."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_la_synth", os.path.join(ROOT, "linear_attention_02_gb300", "synth.py"))
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[spec.name] = mod  # its dataclasses look their module up by name
+    spec.loader.exec_module(mod)
+    return mod
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    from linear_attention_02_gb300 import synth  # noqa: F401 (inputs only)
+    synth = _synth_module()  # inputs only
     w = synth.WORKLOADS[HEADLINE]
     for _ in range(max(0, min(args.warmup, 1))):
         cpu_baseline(synth)
@@ -506,7 +521,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-paths", action="store_true", help="headline step only")

@@ -28,7 +28,8 @@
  * - Ownership: the caller owns every buffer it passes.  The library never
  *   frees caller memory.  Per-call scratch (span states, gradient rows) is
  *   taken stream-ordered from a library-owned CUDA memory pool of the current
- *   device and given back on the same stream.
+ *   device and given back on the same stream; la_workspace_bytes gives its
+ *   size for each call.
  * - Errors: a status code; no exception or abort crosses the ABI.  On error,
  *   la_last_error_message() gives a one-line reason (per host thread).
  *
@@ -144,10 +145,12 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
  * forbids allocation, or a latency-critical loop that cannot pay for an
  * allocator call.  Arguments, layouts and results are those of
  * la_forward_noncausal (up to the order of floating-point summation).
- * Its scratch is one fixed 16 MiB file-scope device array per device, held
- * from the moment the library's code is loaded on that device until the
- * process exits; this call makes no cudaMalloc, cudaFree or other allocating
- * call.  Limit: 2 * B * H * (D*M + D) * 4 bytes must fit in 16 MiB (B*H <= 127
+ * Its scratch is one fixed 16 MiB file-scope device array per device.  With
+ * CUDA's default lazy module loading the array is committed on a device by
+ * the first call there (its address lookup loads the library's device code),
+ * and it stays until the process exits, so a caller that plans device memory
+ * should make that first call before planning; later calls make no
+ * cudaMalloc, cudaFree or other allocating call.  Limit: 2 * B * H * (D*M + D) * 4 bytes must fit in 16 MiB (B*H <= 127
  * at D = M = 128, <= 504 at D = M = 64); larger calls return
  * LA_ERR_INVALID_ARG with the sizes in the message.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
@@ -159,6 +162,41 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
 la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void* V, void* Out,
                                        int B, int H, int N, int D, int M, la_dtype dtype,
                                        void* stream);
+
+/*
+ * Scratch of one call, for callers that plan device memory.  The pages'
+ * interface keeps the state S, Z (and for the backward the suffix state)
+ * inside the operation ("Overview of Linear Attention", Algorithm forward /
+ * backward; "Transformer与RNN的深层联结" section 2, the decode loop on
+ * state_s, state_z); this library keeps the per-range states, flags and
+ * gradient rows that its parallel split needs in a library-owned pool, and
+ * this function says how many bytes of it one call holds at its peak.
+ *   op       the entry point's name: "la_forward_causal", "la_backward_causal",
+ *            "la_forward_noncausal", "la_decode_step" (0) or
+ *            "la_forward_noncausal_noalloc" (0: it uses its fixed array)
+ *   B..M, dtype  the call's sizes and dtype (N is ignored for decode)
+ *   saved    for "la_backward_causal": an OR of LA_SAVED_OUT, LA_SAVED_DEN and
+ *            LA_SAVED_CKPT for the optional inputs the call will pass
+ *            (Out == NULL makes the call recompute the forward, which needs more)
+ *   num_sms  SM count of the device the call will run on; <= 0 queries the
+ *            current device (the only device call this function makes)
+ * Returns the bytes (0 when the call takes no scratch), or SIZE_MAX for an
+ * unknown op, unsupported sizes or a failed device query, with the reason in
+ * la_last_error_message().  Pure arithmetic when num_sms > 0.
+ */
+#define LA_SAVED_OUT 1u
+#define LA_SAVED_DEN 2u
+#define LA_SAVED_CKPT 4u
+size_t la_workspace_bytes(const char* op, int B, int H, int N, int D, int M, la_dtype dtype,
+                          unsigned saved, int num_sms);
+
+/*
+ * Highest number of bytes of the library's scratch pool on the current device
+ * held at once since the pool was created or last reset; reset != 0 then sets
+ * it back to zero (to the bytes held now).  For checking la_workspace_bytes
+ * against what calls actually take.  SIZE_MAX if a CUDA call failed.
+ */
+size_t la_scratch_peak_bytes(int reset);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word set by bounded device-side waits.  LA_ERR_TIMEOUT if one gave up since

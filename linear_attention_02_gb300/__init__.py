@@ -205,6 +205,32 @@ def la_decode_step(q, k, v, S, Z, out=None, stream=None):
     return out
 
 
+def la_workspace_bytes(op, B, H, N, D, M, dtype, saved=0, num_sms=0):
+    """Scratch bytes one call of entry point `op` takes from the library pool.
+
+    dtype: torch.float32 or torch.bfloat16.  saved: OR of LA_SAVED_OUT,
+    LA_SAVED_DEN, LA_SAVED_CKPT (la_backward_causal's optional inputs).
+    num_sms <= 0 asks the current device for its SM count."""
+    if dtype not in _DT:
+        raise ValueError(f"unsupported dtype {dtype}")
+    n = _lib.la_workspace_bytes(op.encode(), B, H, N, D, M, _DT[dtype], int(saved), int(num_sms))
+    if n == _native.SIZE_MAX:
+        raise LinAttnError(_native.LA_ERR_INVALID_ARG, la_last_error_message())
+    return int(n)
+
+
+def la_scratch_peak_bytes(reset=False):
+    """Peak bytes of the library's scratch pool held at once on the current device."""
+    n = _lib.la_scratch_peak_bytes(1 if reset else 0)
+    if n == _native.SIZE_MAX:
+        raise LinAttnError(_native.LA_ERR_CUDA, la_last_error_message())
+    return int(n)
+
+
+LA_SAVED_OUT, LA_SAVED_DEN, LA_SAVED_CKPT = (_native.LA_SAVED_OUT, _native.LA_SAVED_DEN,
+                                             _native.LA_SAVED_CKPT)
+
+
 def la_check_device_status(stream=None):
     _check(_lib.la_check_device_status(_stream_handle(stream)))
 

@@ -13,6 +13,8 @@ LIB_PATH = os.path.join(_PKG, "lib", "liblinattn.so")
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
+LA_SAVED_OUT, LA_SAVED_DEN, LA_SAVED_CKPT = 1, 2, 4
+SIZE_MAX = ctypes.c_size_t(-1).value
 
 # (name, argtypes) of every exported entry point.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
@@ -23,6 +25,8 @@ SIGNATURES = {
     "la_forward_noncausal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_forward_noncausal_noalloc": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_decode_step": [_P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _P],
+    "la_workspace_bytes": [ctypes.c_char_p, _I, _I, _I, _I, _I, _I, ctypes.c_uint, _I],
+    "la_scratch_peak_bytes": [_I],
     "la_check_device_status": [_P],
     "la_selftest_expired_waits": [_P],
     "la_status_string": [_I],
@@ -30,7 +34,8 @@ SIGNATURES = {
     "la_kernel_launch_count": [],
 }
 _RESTYPES = {"la_status_string": ctypes.c_char_p, "la_last_error_message": ctypes.c_char_p,
-             "la_causal_ckpt_floats": ctypes.c_size_t,
+             "la_causal_ckpt_floats": ctypes.c_size_t, "la_workspace_bytes": ctypes.c_size_t,
+             "la_scratch_peak_bytes": ctypes.c_size_t,
              "la_kernel_launch_count": ctypes.c_uint64}
 
 

@@ -40,6 +40,7 @@
 #include <algorithm>
 
 #include "la_launch.h"
+#include "la_plan.h"
 #include "tc_common.cuh"
 
 namespace la {
@@ -1064,6 +1065,27 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 
 }  // namespace tcb
 
+size_t causal_backward_tc64_scratch(int BH, int N, int num_sms, bool out_given, bool den_given,
+                                    bool ckpt_given) {
+    using namespace tcb;
+    static_assert(LayF::T_COLS == 512, "one CTA per SM");
+    const int chunks = (N + L - 1) / L;
+    const size_t units = static_cast<size_t>(plan::tc_units(BH, chunks, num_sms));
+    const size_t agg = sizeof(float) * units * W, flags = sizeof(unsigned) * (units + 1);
+    const size_t gn = sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
+    const size_t gd = sizeof(float) * static_cast<size_t>(BH) * N;
+    using plan::up256;
+    size_t total = 2 * up256(agg) + up256(flags) + up256(gn) + up256(gd);
+    if (!out_given) {  // Out recomputed: its tile, its normaliser, its checkpoints and the
+                       // forward's own scratch, live at the same time
+        total += up256(gn) + up256(gd);
+        if (!ckpt_given) total += up256(sizeof(float) * static_cast<size_t>(BH) * ckpt_slots(chunks) * W);
+        total += causal_forward_tc_scratch(64, BH, N, num_sms);
+    }
+    (void)den_given;  // the layout reserves the normaliser whenever Out is recomputed
+    return total;
+}
+
 cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                  const __nv_bfloat16* V, const __nv_bfloat16* O,
                                  const __nv_bfloat16* G, __nv_bfloat16* dQ, __nv_bfloat16* dK,
@@ -1083,8 +1105,9 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     int per_sm = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kCT, LayF::BYTES)))
         return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int chunks = (N + L - 1) / L;
-    const int slots = std::max(1, per_sm) * c.num_sms;
+    const int slots = c.num_sms;  // one CTA per SM (512 TMEM columns each)
     const ChunkSplit split = split_chunks(BH, chunks, slots);
     const int units = split.units;
 
@@ -1100,6 +1123,10 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gn_bytes) + up(gd_bytes) + up(o_bytes) +
                          up(den_bytes) + up(ck_bytes);
     char* ws = nullptr;
+    if (total != causal_backward_tc64_scratch(BH, N, c.num_sms, O != nullptr, Den != nullptr,
+                                              Ckpt != nullptr) -
+                     (O ? 0 : causal_forward_tc_scratch(64, BH, N, c.num_sms)))
+        return cudaErrorInvalidValue;  // the plan and this layout must agree
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), total)) != cudaSuccess) return e;
     BwdParams p;
     p.N = N;

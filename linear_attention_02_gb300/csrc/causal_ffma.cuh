@@ -19,6 +19,7 @@
 
 #include "la_common.cuh"
 #include "la_launch.h"
+#include "la_plan.h"
 
 namespace la {
 namespace ffma {
@@ -27,8 +28,8 @@ constexpr int kThreads = 256;
 
 template <int D, int M>
 struct Cfg {
-    static constexpr int L = (D >= 128 || M >= 128) ? 32 : 64;  // chunk length
-    static constexpr int W = D * M + D;                            // state words (S | Z)
+    static constexpr int L = plan::ffma_chunk(D, M);                 // chunk length
+    static constexpr int W = static_cast<int>(plan::state_words(D, M));  // state words (S | Z)
     static constexpr int DP = D + 1;                               // padded row strides
     static constexpr int MP = M + 1;
     static constexpr int LP = L + 1;
@@ -454,12 +455,7 @@ struct Smem {
 
 // Spans per head: enough CTAs for about two per SM, whole chunks per span.
 inline void choose_spans(int BH, int N, int L, int num_sms, int* spans, int* span_len) {
-    const int chunks = (N + L - 1) / L;
-    int s = (2 * num_sms + BH - 1) / std::max(BH, 1);
-    s = std::max(1, std::min(s, chunks));
-    const int per = (chunks + s - 1) / s;
-    *span_len = per * L;
-    *spans = (N + *span_len - 1) / *span_len;
+    plan::ffma_spans(BH, N, L, num_sms, spans, span_len);
 }
 
 template <class K>
@@ -485,7 +481,7 @@ cudaError_t causal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* 
     choose_spans(BH, N, C::L, c.num_sms, &spans, &span_len);
     float* agg = nullptr;
     if (spans > 1) {
-        LA_TRY(scratch_alloc(c, (void**)&agg, sizeof(float) * (size_t)BH * spans * C::W));
+        LA_TRY(scratch_alloc(c, (void**)&agg, plan::ffma_causal_forward(BH, N, D, M, c.num_sms)));
         LA_TRY(allow_smem(span_aggregate_kernel<T, D, M>, Smem<D, M>::agg));
         span_aggregate_kernel<T, D, M><<<dim3(BH, spans), kThreads, Smem<D, M>::agg, c.stream>>>(
             K, V, agg, N, spans, span_len);
@@ -512,9 +508,8 @@ cudaError_t causal_backward(const LaunchCtx& c, const T* Q, const T* K, const T*
     choose_spans(BH, N, C::L, c.num_sms, &spans, &span_len);
     const size_t agg_bytes = sizeof(float) * (size_t)BH * spans * C::W;
     const size_t gn_bytes = sizeof(float) * (size_t)BH * N * M;
-    const size_t gd_bytes = sizeof(float) * (size_t)BH * N;
     char* ws = nullptr;
-    LA_TRY(scratch_alloc(c, (void**)&ws, 2 * agg_bytes + gn_bytes + gd_bytes + 256));
+    LA_TRY(scratch_alloc(c, (void**)&ws, plan::ffma_causal_backward(BH, N, D, M, c.num_sms)));
     float* sagg = (float*)ws;
     float* ragg = (float*)(ws + agg_bytes);
     float* gn = (float*)(ws + 2 * agg_bytes);

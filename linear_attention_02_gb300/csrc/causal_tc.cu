@@ -39,6 +39,7 @@
 #include <mutex>
 
 #include "la_launch.h"
+#include "la_plan.h"
 #include "tc_common.cuh"
 
 namespace la {
@@ -512,6 +513,14 @@ cleanup:
 
 }  // namespace tcf
 
+size_t causal_forward_tc_scratch(int D, int BH, int N, int num_sms) {
+    using namespace tcf;
+    const int per_sm = D == 64 ? Layout<64, 64>::PER_SM : Layout<128, 128>::PER_SM;
+    const int chunks = (N + L - 1) / L;
+    const size_t units = static_cast<size_t>(plan::tc_units(BH, chunks, per_sm * num_sms));
+    return sizeof(float) * units * plan::state_words(D, D) + sizeof(unsigned) * (units + 1) + 256;
+}
+
 template <int D, int M>
 cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
@@ -532,16 +541,17 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     // The occupancy query does not see the carve-out the driver picks at launch
-    // and can report one CTA where two fit: take the larger of it and the fit
-    // computed from shared memory and TMEM.
-    const int slots = std::max(per_sm, Lay::PER_SM) * c.num_sms;  // CTAs resident at once
+    // and can report one CTA where two fit, so the split uses the fit computed
+    // from shared memory and TMEM.  (Correctness does not depend on it: a CTA
+    // only ever waits for CTAs that took their ticket, and so started, before it.)
+    const int slots = Lay::PER_SM * c.num_sms;  // CTAs resident at once
     const ChunkSplit split = split_chunks(BH, chunks, slots);
     const int units = split.units;
 
     const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * Lay::W;
     const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
     char* ws = nullptr;
-    e = scratch_alloc(c, reinterpret_cast<void**>(&ws), agg_bytes + flag_bytes + 256);
+    e = scratch_alloc(c, reinterpret_cast<void**>(&ws), causal_forward_tc_scratch(D, BH, N, c.num_sms));
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.N = N;

@@ -10,8 +10,9 @@
 // forms phi(q)_d * S_new[d][e] for its rows and the partial sums are reduced
 // with warp shuffles, then across warps in shared memory).  Each thread holds
 // 8 rows of four columns where the block allows (128 threads per head at
-// D = M = 64; 4 and 16 rows measured slower), and its S loads are issued
-// before q, k and v are read, so the two latencies overlap.
+// D = M = 64; 4 and 16 rows measured slower), and every load of the block
+// (S rows, then q, k, Z and v) is issued before any is used, so their latencies
+// overlap; Z's update and the denominator are reduced before the first barrier.
 #include "la_common.cuh"
 #include "la_launch.h"
 
@@ -36,21 +37,45 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
                    float* __restrict__ S, float* __restrict__ Z, float* __restrict__ out, int BH) {
     using Sh = DecShape<D, M, ROWS>;
     constexpr int CG = Sh::CG, RG = Sh::RG, RPT = Sh::RPT, WARPS = Sh::WARPS, NT = Sh::THREADS;
+    constexpr int ZW = (D + 31) / 32;  // warps holding a row of Z
+    static_assert(D <= NT && M <= NT, "one element of q, k, Z and v per thread");
     __shared__ float fq[D], fk[D], vv[M];
     __shared__ float4 red[WARPS][CG];
-    __shared__ float den_s;
+    __shared__ float red_den[ZW];
     const int bh = blockIdx.x;
     const int t = threadIdx.x;
     const int cg = t % CG, rg = t / CG;
+    const int warp = t >> 5, lane = t & 31;
     float4* S4 = reinterpret_cast<float4*>(S + (size_t)bh * D * M);
+    // Every load this block needs is issued before any is used: the S rows, then
+    // this thread's element of q, k, Z and v, so their latencies overlap.
     float4 s[RPT];
 #pragma unroll
     for (int r = 0; r < RPT; ++r) s[r] = S4[(size_t)(rg + r * RG) * CG + cg];
-    for (int i = t; i < D; i += NT) {
-        fq[i] = phi(to_f(q[(size_t)bh * D + i]));
-        fk[i] = phi(to_f(k[(size_t)bh * D + i]));
+    float qd = 0.f, kd = 0.f, zd = 0.f, vd = 0.f;
+    if (t < D) {
+        qd = to_f(q[(size_t)bh * D + t]);
+        kd = to_f(k[(size_t)bh * D + t]);
+        zd = Z[(size_t)bh * D + t];
     }
-    for (int i = t; i < M; i += NT) vv[i] = to_f(v[(size_t)bh * M + i]);
+    if (t < M) vd = to_f(v[(size_t)bh * M + t]);
+    // Z += phi(k) and this thread's term of the denominator phi(q) . Z, reduced
+    // per warp before the first barrier
+    float dpart = 0.f;
+    if (t < D) {
+        const float a = phi(kd), b = phi(qd);
+        fk[t] = a;
+        fq[t] = b;
+        zd += a;
+        Z[(size_t)bh * D + t] = zd;
+        dpart = b * zd;
+    }
+    if (t < M) vv[t] = vd;
+    if (warp < ZW) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dpart += __shfl_xor_sync(0xffffffffu, dpart, o);
+        if (lane == 0) red_den[warp] = dpart;
+    }
     __syncthreads();
 
     const float4 v4 = make_float4(vv[4 * cg], vv[4 * cg + 1], vv[4 * cg + 2], vv[4 * cg + 3]);
@@ -77,20 +102,7 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
         acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
     }
-    const int warp = t >> 5, lane = t & 31;
     if (lane < CG) red[warp][lane] = acc;
-    if (warp == 0) {
-        // Z update and denominator: phi(q) . (Z + phi(k))
-        float dsum = 0.f;
-        for (int d = lane; d < D; d += 32) {
-            const float z = Z[(size_t)bh * D + d] + fk[d];
-            Z[(size_t)bh * D + d] = z;
-            dsum = fmaf(fq[d], z, dsum);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-        if (lane == 0) den_s = dsum;
-    }
     __syncthreads();
     if (t < CG) {
         // warps that hold distinct row groups: each warp covers 32 / CG row groups
@@ -102,7 +114,10 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
             a.z += b.z;
             a.w += b.w;
         }
-        const float inv_den = 1.f / den_s;
+        float den = red_den[0];
+#pragma unroll
+        for (int w = 1; w < ZW; ++w) den += red_den[w];
+        const float inv_den = 1.f / den;
         float4 o4 = make_float4(a.x * inv_den, a.y * inv_den, a.z * inv_den, a.w * inv_den);
         reinterpret_cast<float4*>(out + (size_t)bh * M)[t] = o4;
     }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
+#include <cstdint>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -12,6 +14,7 @@
 #include <type_traits>
 
 #include "la_launch.h"
+#include "la_plan.h"
 #include "linattn.h"
 
 namespace la {
@@ -36,7 +39,7 @@ la_status cuda_fail(cudaError_t e, const char* where) {
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-    bool ready = false;
+    std::atomic<bool> ready{false};  // set (release) once the fields below are filled
     int num_sms = 0;
     cudaMemPool_t pool = nullptr;
     unsigned int* status_word = nullptr;
@@ -50,9 +53,9 @@ la_status get_ctx(cudaStream_t stream, LaunchCtx* ctx) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(LA_ERR_CUDA, "device ordinal %d out of range", dev);
     DeviceState& d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_dev_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             int sms = 0;
             if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
                 return cuda_fail(e, "cudaDeviceGetAttribute");
@@ -72,7 +75,7 @@ la_status get_ctx(cudaStream_t stream, LaunchCtx* ctx) {
             d.num_sms = sms;
             d.pool = pool;
             d.status_word = word;
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     ctx->stream = stream;
@@ -232,11 +235,77 @@ void scratch_free(const LaunchCtx& c, void* p) {
     if (p) cudaFreeAsync(p, c.stream);
 }
 
+// Scratch bytes of one call, following the same dispatch as the entry points.
+size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, unsigned saved,
+                     int sms) {
+    const bool bf16 = dt == LA_DTYPE_BF16;
+    if (!strcmp(op, "la_forward_causal")) {
+        if (bf16 && D == M && (D == 64 || D == 128)) return causal_forward_tc_scratch(D, BH, N, sms);
+        return plan::ffma_causal_forward(BH, N, D, M, sms);
+    }
+    if (!strcmp(op, "la_backward_causal")) {
+        if (bf16 && D == 64 && M == 64)
+            return causal_backward_tc64_scratch(BH, N, sms, saved & LA_SAVED_OUT, saved & LA_SAVED_DEN,
+                                                saved & LA_SAVED_CKPT);
+        return plan::ffma_causal_backward(BH, N, D, M, sms);
+    }
+    if (!strcmp(op, "la_forward_noncausal")) {
+        if (!bf16 && D == 64 && M == 64) return noncausal_forward_tc_f32_scratch(BH, N, sms);
+        return plan::ffma_noncausal_forward(BH, N, D, M, sms);
+    }
+    if (!strcmp(op, "la_decode_step") || !strcmp(op, "la_forward_noncausal_noalloc")) return 0;
+    return SIZE_MAX;
+}
+
 }  // namespace la
 
 using namespace la;
 
 extern "C" {
+
+size_t la_workspace_bytes(const char* op, int B, int H, int N, int D, int M, la_dtype dtype,
+                          unsigned saved, int num_sms) {
+    static const char* fn = "la_workspace_bytes";
+    if (!op) return fail(LA_ERR_INVALID_ARG, "%s: op is NULL", fn), SIZE_MAX;
+    if (B < 0 || H < 0 || N < 0)
+        return fail(LA_ERR_INVALID_ARG, "%s: negative size B=%d H=%d N=%d", fn, B, H, N), SIZE_MAX;
+    if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16)
+        return fail(LA_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dtype), SIZE_MAX;
+    if (!head_ok(D) || !head_ok(M))
+        return fail(LA_ERR_UNSUPPORTED, "%s: D=%d M=%d, supported head sizes are 32, 64, 128", fn, D,
+                    M),
+               SIZE_MAX;
+    if ((unsigned long long)B * H >= (1ull << 31))
+        return fail(LA_ERR_INVALID_ARG, "%s: B*H too large", fn), SIZE_MAX;
+    const int BH = B * H;
+    if (!strcmp(op, "la_decode_step")) N = 1;
+    if (workspace_for(op, 1, 1, D, M, dtype, saved, 1) == SIZE_MAX)
+        return fail(LA_ERR_INVALID_ARG, "%s: unknown op \"%s\"", fn, op), SIZE_MAX;
+    if ((size_t)BH * N == 0) return 0;
+    if (num_sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, fn), SIZE_MAX;
+    }
+    return workspace_for(op, BH, N, D, M, dtype, saved, num_sms);
+}
+
+size_t la_scratch_peak_bytes(int reset) {
+    static const char* fn = "la_scratch_peak_bytes";
+    LaunchCtx ctx;
+    if (get_ctx(nullptr, &ctx) != LA_OK) return SIZE_MAX;
+    unsigned long long v = 0;
+    cudaError_t e = cudaMemPoolGetAttribute(ctx.pool, cudaMemPoolAttrUsedMemHigh, &v);
+    if (e != cudaSuccess) return cuda_fail(e, fn), SIZE_MAX;
+    if (reset) {
+        unsigned long long zero = 0;
+        if ((e = cudaMemPoolSetAttribute(ctx.pool, cudaMemPoolAttrUsedMemHigh, &zero)) != cudaSuccess)
+            return cuda_fail(e, fn), SIZE_MAX;
+    }
+    return (size_t)v;
+}
+
 
 la_status la_forward_causal(const void* Q, const void* K, const void* V, void* Out, int B, int H,
                             int N, int D, int M, la_dtype dtype, const float* S_init,

@@ -28,6 +28,13 @@ void set_error_message(const char* msg);
 // (the zero state) is never written or read.
 constexpr int kCkptChunks = 8;
 
+// Scratch bytes the tensor-core launchers take from the pool for one call
+// (what la_workspace_bytes reports; the launchers allocate exactly these).
+size_t causal_forward_tc_scratch(int D, int BH, int N, int num_sms);
+size_t causal_backward_tc64_scratch(int BH, int N, int num_sms, bool out_given, bool den_given,
+                                    bool ckpt_given);
+size_t noncausal_forward_tc_f32_scratch(int BH, int N, int num_sms);
+
 // Stream-ordered scratch from the library pool.  Returns cudaSuccess or the error.
 cudaError_t scratch_alloc(const LaunchCtx& c, void** p, size_t bytes);
 // One block whose bounded waits expire and set their bits in c.status_word.

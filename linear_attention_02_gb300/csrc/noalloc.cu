@@ -9,6 +9,7 @@
 // and read-out kernels as la_forward_noncausal, but takes its scratch (the
 // per-span states and the head totals) from g_noalloc_scratch, and it calls
 // no cudaMalloc, cudaFree or other allocating routine.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -25,7 +26,7 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDev = 64;
 struct NoAllocDevice {
-    bool ready = false;
+    std::atomic<bool> ready{false};  // set (release) once the fields below are filled
     int num_sms = 0;
     float* scratch = nullptr;  // device address of g_noalloc_scratch on this device
 };
@@ -51,9 +52,9 @@ la_status na_setup(NoAllocDevice** out) {
     if (e != cudaSuccess) return na_fail(LA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDev) return na_fail(LA_ERR_CUDA, "device ordinal %d out of range", dev);
     NoAllocDevice& d = g_na[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_na_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             int sms = 0;
             if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
                 return na_fail(LA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
@@ -62,7 +63,7 @@ la_status na_setup(NoAllocDevice** out) {
                 return na_fail(LA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
             d.num_sms = sms;
             d.scratch = static_cast<float*>(p);
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     *out = &d;

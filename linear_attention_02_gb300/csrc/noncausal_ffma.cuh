@@ -62,7 +62,7 @@ cudaError_t noncausal_forward(const LaunchCtx& c, const T* Q, const T* K, const 
     choose_spans(BH, N, C::L, c.num_sms, &spans, &span_len);
     float* ws = nullptr;
     const size_t agg_words = (size_t)BH * spans * C::W;
-    LA_TRY(scratch_alloc(c, (void**)&ws, sizeof(float) * (agg_words + (size_t)BH * C::W)));
+    LA_TRY(scratch_alloc(c, (void**)&ws, plan::ffma_noncausal_forward(BH, N, D, M, c.num_sms)));
     float* agg = ws;
     float* totals = ws + agg_words;
     cudaError_t e = cudaSuccess;

@@ -424,7 +424,21 @@ inline int spans_for(int BH, int chunks, int slots) {
     return best;
 }
 
+// State-kernel spans of a head and their length in tokens.
+inline void nc_spans(int BH, int N, int num_sms, int* spans, int* span_len) {
+    const int chunks = (N + L - 1) / L;
+    const int s = spans_for(BH, chunks, 2 * num_sms);
+    *span_len = ((chunks + s - 1) / s) * L;
+    *spans = (N + *span_len - 1) / *span_len;
+}
+
 }  // namespace tcn
+
+size_t noncausal_forward_tc_f32_scratch(int BH, int N, int num_sms) {
+    int spans = 1, len = 0;
+    tcn::nc_spans(BH, N, num_sms, &spans, &len);
+    return sizeof(float) * static_cast<size_t>(BH) * spans * tcn::W;
+}
 
 cudaError_t noncausal_forward_tc_f32(const LaunchCtx& c, const float* Q, const float* K,
                                      const float* V, float* O, int BH, int N) {
@@ -439,18 +453,16 @@ cudaError_t noncausal_forward_tc_f32(const LaunchCtx& c, const float* Q, const f
         (e = cudaFuncSetAttribute(kb, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)))
         return e;
-    const int chunks = (N + L - 1) / L;
-    const int slots = 2 * c.num_sms;  // two CTAs per SM (96 KB, 128 TMEM columns each)
     NcParams p;
     p.N = N;
-    p.spans = spans_for(BH, chunks, slots);
-    p.span_len = ((chunks + p.spans - 1) / p.spans) * L;
-    p.spans = (N + p.span_len - 1) / p.span_len;
+    nc_spans(BH, N, c.num_sms, &p.spans, &p.span_len);
+    const int chunks = (N + L - 1) / L;
+    const int slots = 2 * c.num_sms;  // two CTAs per SM (96 KB, 128 TMEM columns each)
     p.out_spans = spans_for(BH, chunks, slots);
     p.out_len = ((chunks + p.out_spans - 1) / p.out_spans) * L;
     p.out_spans = (N + p.out_len - 1) / p.out_len;
     p.status = c.status_word;
-    const size_t part_bytes = sizeof(float) * static_cast<size_t>(BH) * p.spans * W;
+    const size_t part_bytes = noncausal_forward_tc_f32_scratch(BH, N, c.num_sms);
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&p.part), part_bytes)) != cudaSuccess) return e;
     do {
         CUtensorMap mQ, mK, mV, mO;

@@ -82,8 +82,11 @@ def randn(shape, dtype: str, seed: int, scale: float = 1.0, device: str = "cpu")
 
 
 def qkv(B: int, H: int, N: int, D: int, M: int, dtype: str, seed: int, scale: float = 1.0,
-        with_grad: bool = False, device: str = "cpu") -> dict:
-    """Q, K [B,H,N,D], V [B,H,N,M] and optionally G [B,H,N,M], drawn in that order."""
+        with_grad: bool = False, device: str = "cpu", qk_mean: float = 0.0) -> dict:
+    """Q, K [B,H,N,D], V [B,H,N,M] and optionally G [B,H,N,M], drawn in that order.
+
+    Every tensor is N(0,1)*scale; Q and K are then moved by qk_mean (e.g. -4
+    puts nearly every entry of Q and K below zero)."""
     g = _gen(seed, device)
     out = {}
     shapes = [("Q", (B, H, N, D)), ("K", (B, H, N, D)), ("V", (B, H, N, M))]
@@ -93,6 +96,8 @@ def qkv(B: int, H: int, N: int, D: int, M: int, dtype: str, seed: int, scale: fl
         x = torch.randn(shp, generator=g, dtype=torch.float32, device=device)
         if scale != 1.0:
             x.mul_(scale)
+        if qk_mean != 0.0 and name in ("Q", "K"):
+            x.add_(qk_mean)
         out[name] = x.to(torch_dtype(dtype))
     return out
 
@@ -103,11 +108,15 @@ def step_seed(seed: int, step: int) -> int:
 
 
 def decode_step_qkv(B: int, H: int, D: int, M: int, dtype: str, seed: int, step: int,
-                    device: str = "cpu") -> dict:
-    """q, k [B,H,D] and v [B,H,M] of one decode step."""
+                    device: str = "cpu", scale: float = 1.0, qk_mean: float = 0.0) -> dict:
+    """q, k [B,H,D] and v [B,H,M] of one decode step (N(0,1)*scale, q and k moved by qk_mean)."""
     g = _gen(step_seed(seed, step), device)
     out = {}
     for name, shp in (("q", (B, H, D)), ("k", (B, H, D)), ("v", (B, H, M))):
         x = torch.randn(shp, generator=g, dtype=torch.float32, device=device)
+        if scale != 1.0:
+            x.mul_(scale)
+        if qk_mean != 0.0 and name in ("q", "k"):
+            x.add_(qk_mean)
         out[name] = x.to(torch_dtype(dtype))
     return out

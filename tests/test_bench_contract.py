@@ -58,3 +58,12 @@ def test_reference_arm_under_two_ranks_prints_once_from_rank_0():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_reference_arm_does_not_load_the_cuda_library():
+    code = ("import runpy, sys; sys.argv = ['bench.py', '--impl', 'reference', '--steps', '1', '--warmup', '0']; "
+            "runpy.run_path('bench.py', run_name='__main__'); "
+            "print('LOADED' if any('liblinattn' in ln for ln in open('/proc/self/maps')) else 'CLEAN')")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().splitlines()[-1] == "CLEAN"

@@ -3,15 +3,18 @@ not allocate device memory inside an op (their device memory is planned ahead
 by a host framework, or allocation is forbidden or too slow where they run).
 Its scratch is a fixed device array inside the library, shared by all calls.
 
-Checked through the C ABI (ctypes) against la_forward_noncausal, twice in a
-row with different inputs, so that scratch left behind by the first call
-cannot leak into the second.  This file is collected last on purpose."""
+Checked through the C ABI (ctypes) against la_forward_noncausal and against
+the fp64 oracle, twice in a row with different inputs, so that scratch left
+behind by the first call cannot leak into the second; and the device's free
+memory is checked unchanged across a call.  This file is collected last on
+purpose."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from linear_attention_02_gb300 import _native, synth
 
 pytestmark = pytest.mark.gpu
@@ -33,21 +36,36 @@ def _call(fn, x, out, shape, dt):
               DT[dt], ctypes.c_void_p(st))
 
 
+# (1, 127, 300, 128, 128): 127 heads leave room for one span per head in the
+# fixed scratch, so the call takes the branch that lengthens the spans.
 @pytest.mark.parametrize("dt,shape", [("f32", (8, 8, 4096, 64, 64)),
                                       ("bf16", (2, 3, 517, 128, 64)),
-                                      ("f32", (1, 2, 77, 32, 128))])
+                                      ("f32", (1, 2, 77, 32, 128)),
+                                      ("bf16", (1, 127, 300, 128, 128))])
 def test_noalloc_matches_allocating_entry_point(dt, shape):
     lib = _native.lib
     B, H, N, D, M = shape
     for call in range(2):
-        x = {k: v.cuda() for k, v in synth.qkv(B, H, N, D, M, dt, seed=500 + call).items()}
+        xc = synth.qkv(B, H, N, D, M, dt, seed=500 + call)
+        x = {k: v.cuda() for k, v in xc.items()}
         ref = torch.empty((B, H, N, M), dtype=x["V"].dtype, device="cuda")
         got = torch.full_like(ref, float("nan"))
         assert _call(lib.la_forward_noncausal, x, ref, shape, dt) == _native.LA_OK
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         assert _call(lib.la_forward_noncausal_noalloc, x, got, shape, dt) == _native.LA_OK, \
             lib.la_last_error_message()
         torch.cuda.synchronize()
+        if call == 1:  # the first call may commit the fixed array; later ones take nothing
+            assert torch.cuda.mem_get_info()[0] == free0
         assert _rel(got, ref) <= TOL[dt], f"call {call}"
+        # against the oracle on a few heads (all of them when small)
+        hs = list(range(min(B * H, 4)))
+        Q = xc["Q"].reshape(B * H, N, D)[hs]
+        K = xc["K"].reshape(B * H, N, D)[hs]
+        V = xc["V"].reshape(B * H, N, M)[hs]
+        want = oracle.noncausal_forward_assoc(Q, K, V)[0]
+        assert _rel(got.reshape(B * H, N, M)[hs], torch.from_numpy(want)) <= TOL[dt], f"call {call}"
 
 
 def test_noalloc_rejects_work_beyond_its_scratch():
