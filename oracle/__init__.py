@@ -63,9 +63,12 @@ def _load():
     lib.lao_causal_backward_cumsum.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I]
     lib.lao_causal_backward_quadratic.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
     lib.lao_decode_step.argtypes = [I, I, I, P, P, P, P, P, P]
+    lib.lao_noncausal_backward_assoc.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I]
+    lib.lao_noncausal_backward_quadratic.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
     for f in ("lao_causal_forward_quadratic", "lao_causal_forward_recurrent",
               "lao_noncausal_forward_quadratic", "lao_noncausal_forward_assoc",
-              "lao_causal_backward_cumsum", "lao_causal_backward_quadratic", "lao_decode_step"):
+              "lao_causal_backward_cumsum", "lao_causal_backward_quadratic", "lao_decode_step",
+              "lao_noncausal_backward_assoc", "lao_noncausal_backward_quadratic"):
         getattr(lib, f).restype = None
     _lib = lib
     return lib
@@ -169,6 +172,27 @@ def causal_backward_quadratic(Q, K, V, G):
     dQ, dK, dV = np.empty_like(Q), np.empty_like(K), np.empty_like(V)
     _load().lao_causal_backward_quadratic(nh, N, D, M, _p(Q), _p(K), _p(V), _p(G), _p(dQ), _p(dK),
                                           _p(dV))
+    return dQ, dK, dV
+
+
+def noncausal_backward_assoc(Q, K, V, G, nthreads: int = 0):
+    """Returns (dQ, dK, dV) of L = sum(G * O) for the non-causal output."""
+    Q, K, V, G = _f64(Q), _f64(K), _f64(V), _f64(G)
+    lead, nh, N = _heads(Q, Q.shape[-1])
+    D, M = Q.shape[-1], V.shape[-1]
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(K), np.empty_like(V)
+    _load().lao_noncausal_backward_assoc(nh, N, D, M, _p(Q), _p(K), _p(V), _p(G), _p(dQ), _p(dK),
+                                         _p(dV), int(nthreads))
+    return dQ, dK, dV
+
+
+def noncausal_backward_quadratic(Q, K, V, G):
+    Q, K, V, G = _f64(Q), _f64(K), _f64(V), _f64(G)
+    lead, nh, N = _heads(Q, Q.shape[-1])
+    D, M = Q.shape[-1], V.shape[-1]
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(K), np.empty_like(V)
+    _load().lao_noncausal_backward_quadratic(nh, N, D, M, _p(Q), _p(K), _p(V), _p(G), _p(dQ),
+                                             _p(dK), _p(dV))
     return dQ, dK, dV
 
 

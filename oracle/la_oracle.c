@@ -414,6 +414,165 @@ void lao_causal_backward_quadratic(int nh, int N, int D, int M, const double* Q,
     }
 }
 
+/* ----------------------------------------- non-causal backward, state form */
+
+typedef struct {
+    int N, D, M;
+    const double *Q, *K, *V, *G;
+    double *dQ, *dK, *dV;
+} ncb_ctx;
+
+/*
+ * Gradient of L = sum G * O for the non-causal form ("Transformers are RNNs"
+ * section 二, eq. linear): the numerator gradients of section 三（一）4
+ * (eqs. gq-gv) with the prefix state S_i and the suffix state R_i both taken
+ * over every token, and the denominator by the quotient rule as in the causal
+ * case:
+ *   S = sum_j kf_j V_j^T, Z = sum_j kf_j, den_i = qf_i.Z, O_i = qf_i^T S / den_i
+ *   gn_i = G_i / den_i,  gd_i = -(G_i . O_i) / den_i
+ *   dqf_i = S gn_i + Z gd_i
+ *   R = sum_i qf_i gn_i^T,  r = sum_i qf_i gd_i
+ *   dkf_j = R V_j + r,  dV_j = R^T kf_j
+ * then dQ = dqf * phi'(Q), dK = dkf * phi'(K).
+ */
+static void ncb_state_head(int h, void* p) {
+    ncb_ctx* c = (ncb_ctx*)p;
+    const int N = c->N, D = c->D, M = c->M;
+    const double* Qh = c->Q + (size_t)h * N * D;
+    const double* Kh = c->K + (size_t)h * N * D;
+    const double* Vh = c->V + (size_t)h * N * M;
+    const double* Gh = c->G + (size_t)h * N * M;
+    double* dQh = c->dQ + (size_t)h * N * D;
+    double* dKh = c->dK + (size_t)h * N * D;
+    double* dVh = c->dV + (size_t)h * N * M;
+    double* qf = phi_rows(Qh, N, D);
+    double* kf = phi_rows(Kh, N, D);
+    double* S = (double*)calloc((size_t)D * M, sizeof(double));
+    double* Z = (double*)calloc((size_t)D, sizeof(double));
+    double* R = (double*)calloc((size_t)D * M, sizeof(double));
+    double* r = (double*)calloc((size_t)D, sizeof(double));
+    double* gn = (double*)malloc(sizeof(double) * (size_t)M);
+    double* o = (double*)malloc(sizeof(double) * (size_t)M);
+    for (int j = 0; j < N; ++j) {
+        const double* kj = kf + (size_t)j * D;
+        for (int d = 0; d < D; ++d) {
+            for (int e = 0; e < M; ++e) S[(size_t)d * M + e] += kj[d] * Vh[(size_t)j * M + e];
+            Z[d] += kj[d];
+        }
+    }
+    for (int i = 0; i < N; ++i) {
+        const double* qi = qf + (size_t)i * D;
+        const double* gi = Gh + (size_t)i * M;
+        double den = dot(qi, Z, D);
+        for (int e = 0; e < M; ++e) {
+            double num = 0.0;
+            for (int d = 0; d < D; ++d) num += qi[d] * S[(size_t)d * M + e];
+            o[e] = num / den;
+        }
+        for (int e = 0; e < M; ++e) gn[e] = gi[e] / den;
+        double gd = -dot(gi, o, M) / den;
+        for (int d = 0; d < D; ++d) {
+            double acc = Z[d] * gd;
+            for (int e = 0; e < M; ++e) acc += S[(size_t)d * M + e] * gn[e];
+            dQh[(size_t)i * D + d] = acc * lao_dphi(Qh[(size_t)i * D + d]);
+            for (int e = 0; e < M; ++e) R[(size_t)d * M + e] += qi[d] * gn[e];
+            r[d] += qi[d] * gd;
+        }
+    }
+    for (int j = 0; j < N; ++j) {
+        const double* kj = kf + (size_t)j * D;
+        const double* vj = Vh + (size_t)j * M;
+        for (int d = 0; d < D; ++d) {
+            double acc = r[d];
+            for (int e = 0; e < M; ++e) acc += R[(size_t)d * M + e] * vj[e];
+            dKh[(size_t)j * D + d] = acc * lao_dphi(Kh[(size_t)j * D + d]);
+        }
+        for (int e = 0; e < M; ++e) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += R[(size_t)d * M + e] * kj[d];
+            dVh[(size_t)j * M + e] = acc;
+        }
+    }
+    free(qf);
+    free(kf);
+    free(S);
+    free(Z);
+    free(R);
+    free(r);
+    free(gn);
+    free(o);
+}
+
+void lao_noncausal_backward_assoc(int nh, int N, int D, int M, const double* Q,
+                                  const double* K, const double* V, const double* G,
+                                  double* dQ, double* dK, double* dV, int nthreads) {
+    ncb_ctx c = {N, D, M, Q, K, V, G, dQ, dK, dV};
+    for_heads(nh, nthreads, ncb_state_head, &c);
+}
+
+/*
+ * The same gradient from the unmasked quotient O_i = sum_j w_ij V_j / sum_j w_ij,
+ * w_ij = qf_i.kf_j, term by term:
+ *   dL/dw_ij = gn_i.V_j + gd_i   (every i, j)
+ *   dqf_i = sum_j dL/dw_ij kf_j,  dkf_j = sum_i dL/dw_ij qf_i,  dV_j = sum_i w_ij gn_i.
+ */
+void lao_noncausal_backward_quadratic(int nh, int N, int D, int M, const double* Q,
+                                      const double* K, const double* V, const double* G,
+                                      double* dQ, double* dK, double* dV) {
+    for (int h = 0; h < nh; ++h) {
+        const double* Qh = Q + (size_t)h * N * D;
+        const double* Kh = K + (size_t)h * N * D;
+        const double* Vh = V + (size_t)h * N * M;
+        const double* Gh = G + (size_t)h * N * M;
+        double* dQh = dQ + (size_t)h * N * D;
+        double* dKh = dK + (size_t)h * N * D;
+        double* dVh = dV + (size_t)h * N * M;
+        double* qf = phi_rows(Qh, N, D);
+        double* kf = phi_rows(Kh, N, D);
+        double* gn = (double*)malloc(sizeof(double) * (size_t)N * M);
+        double* gd = (double*)malloc(sizeof(double) * (size_t)N);
+        double* dqf = (double*)calloc((size_t)N * D, sizeof(double));
+        double* dkf = (double*)calloc((size_t)N * D, sizeof(double));
+        double* o = (double*)malloc(sizeof(double) * (size_t)M);
+        memset(dVh, 0, sizeof(double) * (size_t)N * M);
+        for (int i = 0; i < N; ++i) {
+            double den = 0.0;
+            for (int e = 0; e < M; ++e) o[e] = 0.0;
+            for (int j = 0; j < N; ++j) {
+                double wij = dot(qf + (size_t)i * D, kf + (size_t)j * D, D);
+                den += wij;
+                for (int e = 0; e < M; ++e) o[e] += wij * Vh[(size_t)j * M + e];
+            }
+            for (int e = 0; e < M; ++e) o[e] /= den;
+            const double* gi = Gh + (size_t)i * M;
+            for (int e = 0; e < M; ++e) gn[(size_t)i * M + e] = gi[e] / den;
+            gd[i] = -dot(gi, o, M) / den;
+        }
+        for (int i = 0; i < N; ++i) {
+            for (int j = 0; j < N; ++j) {
+                double dw = dot(gn + (size_t)i * M, Vh + (size_t)j * M, M) + gd[i];
+                double wij = dot(qf + (size_t)i * D, kf + (size_t)j * D, D);
+                for (int d = 0; d < D; ++d) {
+                    dqf[(size_t)i * D + d] += dw * kf[(size_t)j * D + d];
+                    dkf[(size_t)j * D + d] += dw * qf[(size_t)i * D + d];
+                }
+                for (int e = 0; e < M; ++e) dVh[(size_t)j * M + e] += wij * gn[(size_t)i * M + e];
+            }
+        }
+        for (size_t t = 0; t < (size_t)N * D; ++t) {
+            dQh[t] = dqf[t] * lao_dphi(Qh[t]);
+            dKh[t] = dkf[t] * lao_dphi(Kh[t]);
+        }
+        free(qf);
+        free(kf);
+        free(gn);
+        free(gd);
+        free(dqf);
+        free(dkf);
+        free(o);
+    }
+}
+
 /* ------------------------------------------------------------ decode step */
 
 /* RNN-mode inference ("Transformer与RNN的深层联结" section 2; "Transformers are

@@ -65,6 +65,18 @@ void lao_causal_backward_quadratic(int nh, int N, int D, int M, const double* Q,
                                    const double* K, const double* V, const double* G,
                                    double* dQ, double* dK, double* dV);
 
+/* Non-causal backward, state form: the gradients of section 三（一）4 with
+ * the prefix and suffix states taken over all tokens (S, Z and R, r are
+ * totals), the denominator by the quotient rule. */
+void lao_noncausal_backward_assoc(int nh, int N, int D, int M, const double* Q,
+                                  const double* K, const double* V, const double* G,
+                                  double* dQ, double* dK, double* dV, int nthreads);
+
+/* Non-causal backward, quadratic form (derivative of the unmasked quotient). */
+void lao_noncausal_backward_quadratic(int nh, int N, int D, int M, const double* Q,
+                                      const double* K, const double* V, const double* G,
+                                      double* dQ, double* dK, double* dV);
+
 /* One recurrent decode step for nh heads: S += phi(k) v^T, Z += phi(k), then
  * out = phi(q)^T S / phi(q).Z (update first, then read).  q,k [nh][D],
  * v, out [nh][M]; S, Z updated in place. */

@@ -298,3 +298,78 @@ def test_backward_invariants():
     np.testing.assert_allclose((fk * dfk).sum(axis=(1, 2)), 0.0, atol=1e-9)
     # row 1 of the causal output depends on V_1 only: its query gets no gradient
     np.testing.assert_allclose(dQ[:, 0], 0.0, atol=1e-13)
+
+
+# ------------------------------------------------ non-causal backward pins
+
+@pytest.mark.parametrize("case", ["noncausal_backward_2x1x1", "noncausal_backward_2x2x1"])
+def test_golden_noncausal_backward_both_forms(case):
+    g = _golden()[case]
+    Q, K, V, G = (np.array(g[k], float) for k in ("Q", "K", "V", "G"))
+    np.testing.assert_allclose(oracle.noncausal_forward_assoc(Q, K, V)[0], _arr(g["O"]), rtol=1e-14)
+    want = [_arr(g[k]) for k in ("dQ", "dK", "dV")]
+    for got in (oracle.noncausal_backward_assoc(Q, K, V, G), oracle.noncausal_backward_quadratic(Q, K, V, G)):
+        for a, b in zip(got, want):
+            np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("nh,N,D,M", SHAPES)
+def test_noncausal_backward_state_equals_quadratic(nh, N, D, M):
+    Q, K, V, G = (_rand((nh, N, x), s) for x, s in ((D, 70), (D, 71), (M, 72), (M, 73)))
+    a = oracle.noncausal_backward_assoc(Q, K, V, G)
+    b = oracle.noncausal_backward_quadratic(Q, K, V, G)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, rtol=1e-10, atol=1e-11)
+
+
+def test_noncausal_backward_finite_differences():
+    nh, N, D, M = 1, 6, 3, 2
+    Q, K, V, G = (_rand((nh, N, x), s) for x, s in ((D, 74), (D, 75), (M, 76), (M, 77)))
+    grads = oracle.noncausal_backward_assoc(Q, K, V, G)
+
+    def loss(q, k, v):
+        return float(np.sum(G * oracle.noncausal_forward_assoc(q, k, v)[0]))
+
+    h = 1e-6
+    for which, (X, dX) in enumerate(zip((Q, K, V), grads)):
+        fd = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            xp, xm = X.copy(), X.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p, args_m = [Q, K, V], [Q, K, V]
+            args_p[which], args_m[which] = xp, xm
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        np.testing.assert_allclose(dX, fd, rtol=1e-6, atol=1e-8)
+
+
+def test_noncausal_backward_matches_torch_autograd():
+    nh, N, D, M = 2, 23, 5, 3
+    arrays = [_rand((nh, N, x), s) for x, s in ((D, 78), (D, 79), (M, 80), (M, 81))]
+    Q, K, V, G = (torch.tensor(a, dtype=torch.float64) for a in arrays)
+    for t in (Q, K, V):
+        t.requires_grad_(True)
+    fq = torch.nn.functional.elu(Q, alpha=1.0) + 1.0
+    fk = torch.nn.functional.elu(K, alpha=1.0) + 1.0
+    w = fq @ fk.transpose(-1, -2)
+    O = (w @ V) / w.sum(-1, keepdim=True)
+    (O * G).sum().backward()
+    got = oracle.noncausal_backward_assoc(*arrays)
+    for a, b in zip(got, (Q.grad, K.grad, V.grad)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_noncausal_backward_invariants():
+    nh, N, D, M = 3, 41, 6, 4
+    Q, K, V, G = (_rand((nh, N, x), s) for x, s in ((D, 82), (D, 83), (M, 84), (M, 85)))
+    dQ, dK, dV = oracle.noncausal_backward_assoc(Q, K, V, G)
+    np.testing.assert_allclose(dV.sum(axis=1), G.sum(axis=1), rtol=1e-10, atol=1e-11)
+    fq, fk = _phi_np(Q), _phi_np(K)
+    dfq = dQ / np.where(Q > 0, 1.0, np.exp(np.minimum(Q, 0.0)))
+    dfk = dK / np.where(K > 0, 1.0, np.exp(np.minimum(K, 0.0)))
+    np.testing.assert_allclose((fq * dfq).sum(-1), 0.0, atol=1e-10)
+    np.testing.assert_allclose((fk * dfk).sum(axis=(1, 2)), 0.0, atol=1e-9)
+    # one token: the non-causal and causal gradients coincide (O_1 = V_1, so dQ = dK = 0, dV = G)
+    a = oracle.noncausal_backward_assoc(Q[:, :1], K[:, :1], V[:, :1], G[:, :1])
+    np.testing.assert_allclose(a[2], G[:, :1], rtol=1e-14)
+    np.testing.assert_allclose(a[0], 0.0, atol=1e-14)
