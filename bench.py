@@ -7,7 +7,7 @@ tokens/s counts (b, n) positions across all heads: B*N tokens per step.
 
 Also measured in the same run (the "paths" object): the causal forward alone,
 the long-sequence forward (B=1, H=16, N=65536, D=M=128), the non-causal fp32
-forward (B=8, H=8, N=4096, D=M=64), one decode step of 256 sequences x 16
+forward and backward (B=8, H=8, N=4096, D=M=64), one decode step of 256 sequences x 16
 heads (D=M=64, fp32 state) and the 2048-token prefill that hands the decode
 its state (the causal forward emitting the final S, Z of every head), each
 with its fraction of the HBM roofline.
@@ -420,7 +420,16 @@ def measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_
         f()
     ms = _time_events(torch, f, 20, stream)
     res["noncausal_f32/fwd"] = entry(ms, _bytes_fwd(w.B, w.H, w.N, w.D, w.M, 4), w.B * w.N)
-    del x, O
+    # the non-causal backward on the same shape, taking the forward's output
+    G = synth.randn((w.B, w.H, w.N, w.M), w.dtype, w.seed + 1, device="cuda")
+    dQ, dK, dV = torch.empty_like(x["Q"]), torch.empty_like(x["K"]), torch.empty_like(x["V"])
+    f = lambda: la.la_backward_noncausal(x["Q"], x["K"], x["V"], G, Out=O, dQ=dQ, dK=dK, dV=dV)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 20, stream)
+    res["noncausal_f32/bwd"] = entry(ms, _bytes_bwd(w.B, w.H, w.N, w.D, w.M, 4, with_out=True),
+                                     w.B * w.N)
+    del x, O, G, dQ, dK, dV
 
     w = synth.WORKLOADS["decode_bf16"]
     B, H, D, M = w.B, w.H, w.D, w.M

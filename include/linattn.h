@@ -124,6 +124,26 @@ la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void
                                void* stream);
 
 /*
+ * Non-causal backward: the gradient of L(Out) given dOut = dL/dOut for
+ * la_forward_noncausal's output.  The numerator gradients of "Transformers
+ * are RNNs" section 三（一）4 (eqs. gq-gv) with the prefix state of phi(Q) and
+ * the suffix state of phi(K) and V both summed over every token (the
+ * unmasked sums of section 二, eq. linear), the denominator by the quotient
+ * rule, then the chain rule through phi:
+ *   gn_i = dOut_i / den_i, gd_i = -(dOut_i . Out_i) / den_i, den_i = phi(Q_i).Z
+ *   dphi(Q_i) = S gn_i + Z gd_i;  R = sum_i phi(Q_i) gn_i^T, r = sum_i phi(Q_i) gd_i
+ *   dphi(K_j) = R V_j + r;  dV_j = R^T phi(K_j)
+ *   Q, K [B][H][N][D]; V, dOut [B][H][N][M] dtype   (read)
+ *   Out  [B][H][N][M] dtype, nullable               (read) the forward's output;
+ *        recomputed when NULL
+ *   dQ, dK [B][H][N][D]; dV [B][H][N][M] dtype      (written)
+ * Outputs may not alias inputs or each other.
+ */
+la_status la_backward_noncausal(const void* Q, const void* K, const void* V, const void* Out,
+                                const void* dOut, void* dQ, void* dK, void* dV,
+                                int B, int H, int N, int D, int M, la_dtype dtype, void* stream);
+
+/*
  * One recurrent decode step for B*H independent heads ("Transformers are
  * RNNs" section 四, the RNN form; "Transformer与RNN的深层联结" section 2,
  * RNN-mode inference): first S += phi(k) v^T and Z += phi(k), then
@@ -172,7 +192,7 @@ la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void*
  * gradient rows that its parallel split needs in a library-owned pool, and
  * this function says how many bytes of it one call holds at its peak.
  *   op       the entry point's name: "la_forward_causal", "la_backward_causal",
- *            "la_forward_noncausal", "la_decode_step" (0) or
+ *            "la_forward_noncausal", "la_backward_noncausal", "la_decode_step" (0) or
  *            "la_forward_noncausal_noalloc" (0: it uses its fixed array)
  *   B..M, dtype  the call's sizes and dtype (N is ignored for decode)
  *   saved    for "la_backward_causal": an OR of LA_SAVED_OUT, LA_SAVED_DEN and

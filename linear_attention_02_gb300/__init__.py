@@ -163,6 +163,28 @@ def la_forward_noncausal(Q, K, V, out=None, stream=None):
     return out
 
 
+def la_backward_noncausal(Q, K, V, dOut, Out=None, dQ=None, dK=None, dV=None, stream=None):
+    """Backward of la_forward_noncausal; returns (dQ, dK, dV).  Out is optional."""
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (dOut, "dOut")):
+        _need(t, n, Q.dtype, dev)
+    if K.shape != Q.shape or dOut.shape != V.shape:
+        raise ValueError("K must have the shape of Q and dOut the shape of V")
+    if Out is not None:
+        _need(Out, "Out", Q.dtype, dev)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t, n in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        _need(t, n, Q.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_backward_noncausal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Out), _ptr(dOut), _ptr(dQ),
+                                          _ptr(dK), _ptr(dV), B, H, N, D, M, _dtype(Q),
+                                          _stream_handle(stream)))
+    return dQ, dK, dV
+
+
 def la_forward_noncausal_noalloc(Q, K, V, out=None, stream=None):
     """la_forward_noncausal for callers that may not allocate device memory.
 

@@ -24,6 +24,7 @@ SIGNATURES = {
     "la_causal_ckpt_floats": [_I, _I, _I, _I, _I],
     "la_forward_noncausal": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_forward_noncausal_noalloc": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
+    "la_backward_noncausal": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "la_decode_step": [_P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _P],
     "la_workspace_bytes": [ctypes.c_char_p, _I, _I, _I, _I, _I, _I, ctypes.c_uint, _I],
     "la_scratch_peak_bytes": [_I],

@@ -198,6 +198,14 @@ struct FwdNoncausal {
                                               N);
     }
 };
+struct BwdNoncausal {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V,
+                           const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N) {
+        return noncausal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
+                                           (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
+    }
+};
 struct Decode {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* q, const void* k, const void* v,
@@ -253,6 +261,7 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
         if (!bf16 && D == 64 && M == 64) return noncausal_forward_tc_f32_scratch(BH, N, sms);
         return plan::ffma_noncausal_forward(BH, N, D, M, sms);
     }
+    if (!strcmp(op, "la_backward_noncausal")) return plan::ffma_noncausal_backward(BH, N, D, M, sms);
     if (!strcmp(op, "la_decode_step") || !strcmp(op, "la_forward_noncausal_noalloc")) return 0;
     return SIZE_MAX;
 }
@@ -372,6 +381,24 @@ la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     return finish(dispatch<FwdNoncausal>(dtype, D, M, &ctx, Q, K, V, Out, (int)((size_t)B * H), N),
+                  fn);
+}
+
+la_status la_backward_noncausal(const void* Q, const void* K, const void* V, const void* Out,
+                                const void* dOut, void* dQ, void* dK, void* dV, int B, int H, int N,
+                                int D, int M, la_dtype dtype, void* stream) {
+    static const char* fn = "la_backward_noncausal";
+    const void* p[] = {Q, K, V, dOut, dQ, dK, dV};
+    const char* nm[] = {"Q", "K", "V", "dOut", "dQ", "dK", "dV"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 7, &empty);
+    if (s != LA_OK) return s;
+    if ((s = check_optional(fn, Out, "Out"))) return s;
+    if (empty) return LA_OK;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    return finish(dispatch<BwdNoncausal>(dtype, D, M, &ctx, Q, K, V, Out, dOut, dQ, dK, dV,
+                                         (int)((size_t)B * H), N),
                   fn);
 }
 

@@ -76,6 +76,10 @@ cudaError_t noncausal_forward(const LaunchCtx& c, const T* Q, const T* K, const 
                               int BH, int N);
 
 template <typename T, int D, int M>
+cudaError_t noncausal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,
+                               const T* G, T* dQ, T* dK, T* dV, int BH, int N);
+
+template <typename T, int D, int M>
 cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
                         float* Z, float* out, int BH);
 

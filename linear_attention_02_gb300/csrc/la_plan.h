@@ -56,6 +56,12 @@ inline size_t ffma_noncausal_forward(int BH, int N, int D, int M, int num_sms) {
     return sizeof(float) * (static_cast<size_t>(BH) * spans + BH) * state_words(D, M);
 }
 
+// CUDA-core non-causal backward: state partials and totals, (R | r) partials and totals.
+inline size_t ffma_noncausal_backward(int BH, int N, int D, int M, int num_sms) {
+    const int spans = ffma_span_count(BH, N, D, M, num_sms);
+    return 2 * sizeof(float) * (static_cast<size_t>(BH) * spans + BH) * state_words(D, M);
+}
+
 // Tensor-core causal kernels: the chunks of all heads cut into equal ranges,
 // one per resident CTA (see tc_common.cuh, split_chunks).
 inline int tc_units(int BH, int chunks_per_head, int slots) {

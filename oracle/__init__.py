@@ -65,10 +65,12 @@ def _load():
     lib.lao_decode_step.argtypes = [I, I, I, P, P, P, P, P, P]
     lib.lao_noncausal_backward_assoc.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I]
     lib.lao_noncausal_backward_quadratic.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+    lib.lao_softmax_decode_step.argtypes = [I, I, I, I, P, P, P, P, P, P]
     for f in ("lao_causal_forward_quadratic", "lao_causal_forward_recurrent",
               "lao_noncausal_forward_quadratic", "lao_noncausal_forward_assoc",
               "lao_causal_backward_cumsum", "lao_causal_backward_quadratic", "lao_decode_step",
-              "lao_noncausal_backward_assoc", "lao_noncausal_backward_quadratic"):
+              "lao_noncausal_backward_assoc", "lao_noncausal_backward_quadratic",
+              "lao_softmax_decode_step"):
         getattr(lib, f).restype = None
     _lib = lib
     return lib
@@ -206,3 +208,15 @@ def decode_step(q, k, v, S, Z):
     out = np.empty(q.shape[:-1] + (M,))
     _load().lao_decode_step(nh, D, M, _p(q), _p(k), _p(v), _p(S), _p(Z), _p(out))
     return out, S, Z
+
+
+def softmax_decode_step(q, k, v, Kc, Vc):
+    """Softmax KV-cache decode: out [..., M] for q, k [..., D], v [..., M] and
+    caches Kc [..., T, D], Vc [..., T, M] of the T earlier positions."""
+    q, k, v, Kc, Vc = _f64(q), _f64(k), _f64(v), _f64(Kc), _f64(Vc)
+    D, M = q.shape[-1], v.shape[-1]
+    T = Kc.shape[-2]
+    nh = int(np.prod(q.shape[:-1])) if q.ndim > 1 else 1
+    out = np.empty(q.shape[:-1] + (M,))
+    _load().lao_softmax_decode_step(nh, T, D, M, _p(q), _p(k), _p(v), _p(Kc), _p(Vc), _p(out))
+    return out

@@ -602,3 +602,42 @@ void lao_decode_step(int nh, int D, int M, const double* q, const double* k,
     free(kf);
     free(qf);
 }
+
+/* ------------------------------------------- softmax KV-cache decode step */
+
+/* Standard Transformer inference with a KV cache ("Transformer与RNN的深层联结"
+ * section 2): the step's k, v are appended to the cache, then the query
+ * attends to every cached position with softmax(q K^T / sqrt(D)) V (the
+ * scaled dot-product of "Transformers are RNNs" section 一, eq. softmax).
+ * Kc [nh][T][D], Vc [nh][T][M] hold the T earlier positions and are not
+ * modified; the appended row is k [nh][D], v [nh][M].  The largest score is
+ * subtracted before the exponentials (the pages' overflow guard, which does
+ * not change the result). */
+void lao_softmax_decode_step(int nh, int T, int D, int M, const double* q, const double* k,
+                             const double* v, const double* Kc, const double* Vc, double* out) {
+    double* sc = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    for (int h = 0; h < nh; ++h) {
+        const double* qh = q + (size_t)h * D;
+        double mx = -INFINITY;
+        for (int j = 0; j <= T; ++j) {
+            const double* kj = j < T ? Kc + ((size_t)h * T + j) * D : k + (size_t)h * D;
+            sc[j] = dot(qh, kj, D) * inv_sqrt_d;
+            if (sc[j] > mx) mx = sc[j];
+        }
+        double den = 0.0;
+        for (int j = 0; j <= T; ++j) {
+            sc[j] = exp(sc[j] - mx);
+            den += sc[j];
+        }
+        for (int e = 0; e < M; ++e) {
+            double acc = 0.0;
+            for (int j = 0; j <= T; ++j) {
+                const double* vj = j < T ? Vc + ((size_t)h * T + j) * M : v + (size_t)h * M;
+                acc += sc[j] * vj[e];
+            }
+            out[(size_t)h * M + e] = acc / den;
+        }
+    }
+    free(sc);
+}

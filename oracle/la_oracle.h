@@ -83,6 +83,12 @@ void lao_noncausal_backward_quadratic(int nh, int N, int D, int M, const double*
 void lao_decode_step(int nh, int D, int M, const double* q, const double* k,
                      const double* v, double* S, double* Z, double* out);
 
+/* Softmax attention decode step with a KV cache: append (k, v) to the T
+ * cached positions, then out = softmax(q K^T / sqrt(D)) V over all T + 1.
+ * q, k [nh][D]; v, out [nh][M]; Kc [nh][T][D], Vc [nh][T][M] (read only). */
+void lao_softmax_decode_step(int nh, int T, int D, int M, const double* q, const double* k,
+                             const double* v, const double* Kc, const double* Vc, double* out);
+
 #ifdef __cplusplus
 }
 #endif

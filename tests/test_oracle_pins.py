@@ -373,3 +373,34 @@ def test_noncausal_backward_invariants():
     a = oracle.noncausal_backward_assoc(Q[:, :1], K[:, :1], V[:, :1], G[:, :1])
     np.testing.assert_allclose(a[2], G[:, :1], rtol=1e-14)
     np.testing.assert_allclose(a[0], 0.0, atol=1e-14)
+
+
+# --------------------------------------------- softmax KV-cache decode pins
+
+@pytest.mark.parametrize("case", ["a", "b"])
+def test_golden_softmax_decode(case):
+    g = _golden()["softmax_decode_T1"][case]
+    q, k, v, Kc, Vc = (np.array(g[n], float) for n in ("q", "k", "v", "Kc", "Vc"))
+    out = oracle.softmax_decode_step(q[None], k[None], v[None], Kc[None], Vc[None])[0]
+    np.testing.assert_allclose(out, _arr(g["out"]), rtol=1e-14)
+
+
+def test_softmax_decode_matches_library_softmax_and_special_cases():
+    nh, T, D, M = 3, 37, 8, 5
+    q, k, v = _rand((nh, D), 90), _rand((nh, D), 91), _rand((nh, M), 92)
+    Kc, Vc = _rand((nh, T, D), 93), _rand((nh, T, M), 94)
+    out = oracle.softmax_decode_step(q, k, v, Kc, Vc)
+    Kt = torch.tensor(np.concatenate([Kc, k[:, None]], 1))
+    Vt = torch.tensor(np.concatenate([Vc, v[:, None]], 1))
+    w = torch.softmax(torch.einsum("hd,htd->ht", torch.tensor(q), Kt) / math.sqrt(D), dim=-1)
+    np.testing.assert_allclose(out, torch.einsum("ht,htm->hm", w, Vt).numpy(), rtol=1e-12, atol=1e-13)
+    # empty cache: the only position is the new one
+    np.testing.assert_allclose(oracle.softmax_decode_step(q, k, v, Kc[:, :0], Vc[:, :0]), v, rtol=1e-15)
+    # every key equal: the mean of the values
+    Ke = np.broadcast_to(k[:, None], (nh, T, D)).copy()
+    np.testing.assert_allclose(oracle.softmax_decode_step(q, k, v, Ke, Vc),
+                               np.concatenate([Vc, v[:, None]], 1).mean(axis=1), rtol=1e-12)
+    # a common shift of every key moves every score equally: the output is unchanged
+    c = _rand((nh, 1, D), 95)
+    np.testing.assert_allclose(oracle.softmax_decode_step(q, k + c[:, 0], v, Kc + c, Vc), out,
+                               rtol=1e-11, atol=1e-12)
