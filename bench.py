@@ -8,8 +8,9 @@ tokens/s counts (b, n) positions across all heads: B*N tokens per step.
 Also measured in the same run (the "paths" object): the causal forward alone,
 the long-sequence forward (B=1, H=16, N=65536, D=M=128), the non-causal fp32
 forward and backward (B=8, H=8, N=4096, D=M=64), one decode step of 256 sequences x 16
-heads (D=M=64, fp32 state) and the 2048-token prefill that hands the decode
-its state (the causal forward emitting the final S, Z of every head), each
+heads (D=M=64, fp32 state), the softmax KV-cache decode step it replaces (the
+same heads with a full 4096-position cache) and the 2048-token prefill that
+hands the decode its state (the causal forward emitting the final S, Z of every head), each
 with its fraction of the HBM roofline.
 
 Timing: W untimed warm-up steps, then K steps between a barrier and a device
@@ -452,7 +453,25 @@ def measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_
     res["decode_bf16/step"] = entry(ms, _bytes_decode(B, H, D, M, 2), B,
                                     {"l2": "flushed before each step",
                                      "ms_l2_warm": round(ms_warm, 5)})
-    del S, Z, steps, out, flush_buf
+    lin_ms = ms
+    del S, Z, out
+
+    # the softmax KV-cache step on the same heads at the end of the decode run (a full
+    # cache of prefill + steps positions): what the recurrent step replaces
+    T_max = w.prefill + w.steps
+    Kc = synth.randn((B, H, T_max, D), w.dtype, w.seed + 2, device="cuda")
+    Vc = synth.randn((B, H, T_max, M), w.dtype, w.seed + 3, device="cuda")
+    out = torch.empty(B, H, M, device="cuda")
+    T = T_max - 1
+    f = lambda: la.la_softmax_decode_step(steps[0]["q"], steps[0]["k"], steps[0]["v"], Kc, Vc, T, out=out)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 10, stream, flush=lambda: flush_buf.fill_(1.0))
+    sd_bytes = B * H * (T * (D + M) * 2 + (D + M) * 2 + (2 * D + M) * 2 + M * 4)
+    res["softmax_kv_decode_bf16/step"] = entry(ms, sd_bytes, B, {
+        "cache_positions": T + 1, "l2": "flushed before each step",
+        "time_vs_recurrent_step": round(ms / lin_ms, 2)})
+    del Kc, Vc, out, steps, flush_buf
 
     # the prefill that hands the decode its state: the causal forward over every sequence's
     # prompt, emitting the final S, Z of each head (inputs larger than L2)

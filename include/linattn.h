@@ -158,6 +158,25 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
                          float* out, int B, int H, int D, int M, la_dtype dtype, void* stream);
 
 /*
+ * One decode step of standard softmax attention with a KV cache, the baseline
+ * the recurrent step is measured against ("Transformer与RNN的深层联结",
+ * section 2, standard Transformer inference: the step's k, v are appended to
+ * the cache, then out = softmax(q K^T / sqrt(D)) V over every cached position;
+ * the scaled dot product of "Transformers are RNNs", section 一, eq. softmax).
+ * Its cost grows with the cache; la_decode_step's does not.
+ *   q, k [B][H][D]; v [B][H][M] dtype               (read)
+ *   K_cache [B][H][T_max][D], V_cache [B][H][T_max][M] dtype
+ *           rows 0..T-1 read; row T written with k, v
+ *   T       positions already cached, 0 <= T < T_max (same for every head)
+ *   out     [B][H][M] fp32                          (written)
+ * Needs D == M (in {32, 64, 128}); LA_ERR_UNSUPPORTED otherwise.  Scratch:
+ * la_workspace_bytes("la_softmax_decode_step", B, H, T, D, M, ...).
+ */
+la_status la_softmax_decode_step(const void* q, const void* k, const void* v, void* K_cache,
+                                 void* V_cache, int T, int T_max, float* out, int B, int H, int D,
+                                 int M, la_dtype dtype, void* stream);
+
+/*
  * la_forward_noncausal with no device allocation.  The paper has no
  * counterpart: this is a service for callers that may not allocate device
  * memory inside an op -- a host framework that plans all device memory in
@@ -192,7 +211,8 @@ la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void*
  * gradient rows that its parallel split needs in a library-owned pool, and
  * this function says how many bytes of it one call holds at its peak.
  *   op       the entry point's name: "la_forward_causal", "la_backward_causal",
- *            "la_forward_noncausal", "la_backward_noncausal", "la_decode_step" (0) or
+ *            "la_forward_noncausal", "la_backward_noncausal", "la_decode_step" (0),
+ *            "la_softmax_decode_step" (N = the cache position T) or
  *            "la_forward_noncausal_noalloc" (0: it uses its fixed array)
  *   B..M, dtype  the call's sizes and dtype (N is ignored for decode)
  *   saved    for "la_backward_causal": an OR of LA_SAVED_OUT, LA_SAVED_DEN and

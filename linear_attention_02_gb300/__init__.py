@@ -253,6 +253,31 @@ LA_SAVED_OUT, LA_SAVED_DEN, LA_SAVED_CKPT = (_native.LA_SAVED_OUT, _native.LA_SA
                                              _native.LA_SAVED_CKPT)
 
 
+def la_softmax_decode_step(q, k, v, K_cache, V_cache, T, out=None, stream=None):
+    """Softmax attention decode step with a KV cache (the comparator of la_decode_step).
+
+    Writes k, v into row T of K_cache [B,H,T_max,D] / V_cache [B,H,T_max,M] and
+    returns out [B,H,M] fp32 = softmax(q K^T / sqrt(D)) V over rows 0..T."""
+    if q.dim() != 3 or v.dim() != 3 or K_cache.dim() != 4 or V_cache.dim() != 4:
+        raise ValueError("q, k [B,H,D], v [B,H,M], caches [B,H,T_max,D] / [B,H,T_max,M]")
+    B, H, D = q.shape
+    M = v.shape[2]
+    T_max = K_cache.shape[2]
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (K_cache, "K_cache"), (V_cache, "V_cache")):
+        _need(t, n, q.dtype, dev)
+    if tuple(K_cache.shape) != (B, H, T_max, D) or tuple(V_cache.shape) != (B, H, T_max, M):
+        raise ValueError("cache shapes do not match q and v")
+    if out is None:
+        out = torch.empty((B, H, M), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_softmax_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(K_cache), _ptr(V_cache),
+                                           int(T), T_max, _ptr(out), B, H, D, M, _dtype(q),
+                                           _stream_handle(stream)))
+    return out
+
+
 def la_check_device_status(stream=None):
     _check(_lib.la_check_device_status(_stream_handle(stream)))
 

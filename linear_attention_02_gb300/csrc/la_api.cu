@@ -262,6 +262,8 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
         return plan::ffma_noncausal_forward(BH, N, D, M, sms);
     }
     if (!strcmp(op, "la_backward_noncausal")) return plan::ffma_noncausal_backward(BH, N, D, M, sms);
+    if (!strcmp(op, "la_softmax_decode_step"))  // N is the cache position T: T + 1 positions
+        return D == M ? plan::softmax_decode_scratch(BH, N + 1, D, sms) : SIZE_MAX;
     if (!strcmp(op, "la_decode_step") || !strcmp(op, "la_forward_noncausal_noalloc")) return 0;
     return SIZE_MAX;
 }
@@ -287,10 +289,11 @@ size_t la_workspace_bytes(const char* op, int B, int H, int N, int D, int M, la_
     if ((unsigned long long)B * H >= (1ull << 31))
         return fail(LA_ERR_INVALID_ARG, "%s: B*H too large", fn), SIZE_MAX;
     const int BH = B * H;
-    if (!strcmp(op, "la_decode_step")) N = 1;
     if (workspace_for(op, 1, 1, D, M, dtype, saved, 1) == SIZE_MAX)
-        return fail(LA_ERR_INVALID_ARG, "%s: unknown op \"%s\"", fn, op), SIZE_MAX;
-    if ((size_t)BH * N == 0) return 0;
+        return fail(LA_ERR_INVALID_ARG, "%s: unknown op \"%s\" or unsupported shape", fn, op), SIZE_MAX;
+    if (!strcmp(op, "la_decode_step")) N = 1;
+    const bool cache_op = !strcmp(op, "la_softmax_decode_step");  // N = T may be 0
+    if (BH == 0 || (N == 0 && !cache_op)) return 0;
     if (num_sms <= 0) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -413,6 +416,40 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     return finish(dispatch<Decode>(dtype, D, M, &ctx, q, k, v, S, Z, out, (int)((size_t)B * H)), fn);
+}
+
+la_status la_softmax_decode_step(const void* q, const void* k, const void* v, void* K_cache,
+                                 void* V_cache, int T, int T_max, float* out, int B, int H, int D,
+                                 int M, la_dtype dtype, void* stream) {
+    static const char* fn = "la_softmax_decode_step";
+    const void* p[] = {q, k, v, K_cache, V_cache, out};
+    const char* nm[] = {"q", "k", "v", "K_cache", "V_cache", "out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, 1, D, M, dtype, p, nm, 6, &empty);
+    if (s != LA_OK) return s;
+    if (D != M)
+        return fail(LA_ERR_UNSUPPORTED, "%s: D=%d M=%d, the KV-cache step needs D == M", fn, D, M);
+    if (T < 0 || T >= T_max)
+        return fail(LA_ERR_INVALID_ARG, "%s: cache position T=%d must satisfy 0 <= T < T_max=%d", fn,
+                    T, T_max);
+    if ((unsigned long long)B * H * T_max * D >= (1ull << 40))
+        return fail(LA_ERR_INVALID_ARG, "%s: cache too large", fn);
+    if (empty) return LA_OK;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    const int BH = B * H;
+    cudaError_t e = cudaErrorInvalidValue;
+#define LA_SD_CASE(Ty, d)                                                                       \
+    if (D == d)                                                                                 \
+        e = softmax_decode_step<Ty, d>(ctx, (const Ty*)q, (const Ty*)k, (const Ty*)v, (Ty*)K_cache, \
+                                       (Ty*)V_cache, T, T_max, out, BH);
+    if (dtype == LA_DTYPE_F32) {
+        LA_SD_CASE(float, 32) else LA_SD_CASE(float, 64) else LA_SD_CASE(float, 128)
+    } else {
+        LA_SD_CASE(__nv_bfloat16, 32) else LA_SD_CASE(__nv_bfloat16, 64) else LA_SD_CASE(__nv_bfloat16, 128)
+    }
+#undef LA_SD_CASE
+    return finish(e, fn);
 }
 
 la_status la_selftest_expired_waits(void* stream) {

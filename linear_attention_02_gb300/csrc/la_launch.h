@@ -79,6 +79,12 @@ template <typename T, int D, int M>
 cudaError_t noncausal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,
                                const T* G, T* dQ, T* dK, T* dV, int BH, int N);
 
+// Softmax attention decode step with a KV cache (M = D): appends k, v at
+// position T_len of the caches, then attends over positions 0..T_len.
+template <typename T, int D>
+cudaError_t softmax_decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, T* Kc,
+                                T* Vc, int T_len, int T_max, float* out, int BH);
+
 template <typename T, int D, int M>
 cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
                         float* Z, float* out, int BH);

@@ -62,6 +62,22 @@ inline size_t ffma_noncausal_backward(int BH, int N, int D, int M, int num_sms) 
     return 2 * sizeof(float) * (static_cast<size_t>(BH) * spans + BH) * state_words(D, M);
 }
 
+// Softmax KV-cache decode: positions of a head cut into ranges so that the grid
+// is about eight waves of eight 256-thread CTAs per SM, at least 256 positions a range.
+inline void softmax_decode_split(int BH, int total, int num_sms, int* splits, int* split_len) {
+    int s = (64 * num_sms + std::max(BH, 1) - 1) / std::max(BH, 1);
+    s = std::max(1, std::min(s, (total + 255) / 256));
+    *split_len = (total + s - 1) / s;
+    *splits = (total + *split_len - 1) / *split_len;
+}
+
+// Its per-range partials: running maximum, weight sum and D weighted-value sums.
+inline size_t softmax_decode_scratch(int BH, int total, int D, int num_sms) {
+    int splits = 1, len = 1;
+    softmax_decode_split(BH, total, num_sms, &splits, &len);
+    return sizeof(float) * static_cast<size_t>(BH) * splits * (D + 2);
+}
+
 // Tensor-core causal kernels: the chunks of all heads cut into equal ranges,
 // one per resident CTA (see tc_common.cuh, split_chunks).
 inline int tc_units(int BH, int chunks_per_head, int slots) {
