@@ -66,11 +66,15 @@ def _load():
     lib.lao_noncausal_backward_assoc.argtypes = [I, I, I, I, P, P, P, P, P, P, P, I]
     lib.lao_noncausal_backward_quadratic.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
     lib.lao_softmax_decode_step.argtypes = [I, I, I, I, P, P, P, P, P, P]
+    lib.lao_retention_forward_recurrent.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P]
+    lib.lao_retention_forward_quadratic.argtypes = [I, I, I, I, I, P, P, P, P, P, P]
+    lib.lao_retention_decode_step.argtypes = [I, I, I, P, P, P, P, P, P]
     for f in ("lao_causal_forward_quadratic", "lao_causal_forward_recurrent",
               "lao_noncausal_forward_quadratic", "lao_noncausal_forward_assoc",
               "lao_causal_backward_cumsum", "lao_causal_backward_quadratic", "lao_decode_step",
               "lao_noncausal_backward_assoc", "lao_noncausal_backward_quadratic",
-              "lao_softmax_decode_step"):
+              "lao_softmax_decode_step", "lao_retention_forward_recurrent",
+              "lao_retention_forward_quadratic", "lao_retention_decode_step"):
         getattr(lib, f).restype = None
     _lib = lib
     return lib
@@ -220,3 +224,46 @@ def softmax_decode_step(q, k, v, Kc, Vc):
     out = np.empty(q.shape[:-1] + (M,))
     _load().lao_softmax_decode_step(nh, T, D, M, _p(q), _p(k), _p(v), _p(Kc), _p(Vc), _p(out))
     return out
+
+
+def _decays(Q, gamma_head, gates):
+    gh = None if gamma_head is None else _f64(gamma_head).reshape(-1)
+    gt = None if gates is None else _f64(gates)
+    return gh, gt
+
+
+def retention_forward_recurrent(Q, K, V, gamma_head=None, gates=None, S0=None):
+    """Retention over [B, H, N, *] inputs; returns (O, S_N).  gamma_head: [H];
+    gates: [B, H, N]; neither: decay 1."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N, D = Q.shape
+    M = V.shape[-1]
+    gh, gt = _decays(Q, gamma_head, gates)
+    S0 = None if S0 is None else _f64(S0)
+    O = np.empty((B, H, N, M))
+    S = np.empty((B, H, D, M))
+    _load().lao_retention_forward_recurrent(B * H, H, N, D, M, _p(Q), _p(K), _p(V), _p(gh), _p(gt),
+                                            _p(S0), _p(O), _p(S))
+    return O, S
+
+
+def retention_forward_quadratic(Q, K, V, gamma_head=None, gates=None):
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N, D = Q.shape
+    M = V.shape[-1]
+    gh, gt = _decays(Q, gamma_head, gates)
+    O = np.empty((B, H, N, M))
+    _load().lao_retention_forward_quadratic(B * H, H, N, D, M, _p(Q), _p(K), _p(V), _p(gh), _p(gt),
+                                            _p(O))
+    return O
+
+
+def retention_decode_step(q, k, v, gamma, S):
+    """One step for every head: returns (out, S_new); gamma has one decay per head."""
+    q, k, v, S = _f64(q), _f64(k), _f64(v), _f64(S).copy()
+    D, M = q.shape[-1], v.shape[-1]
+    nh = int(np.prod(q.shape[:-1]))
+    g = np.ascontiguousarray(np.broadcast_to(np.asarray(gamma, dtype=np.float64), q.shape[:-1]))
+    out = np.empty(q.shape[:-1] + (M,))
+    _load().lao_retention_decode_step(nh, D, M, _p(q), _p(k), _p(v), _p(g), _p(S), _p(out))
+    return out, S

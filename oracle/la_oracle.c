@@ -641,3 +641,92 @@ void lao_softmax_decode_step(int nh, int T, int D, int M, const double* q, const
     }
     free(sc);
 }
+
+/* ----------------------------------------------------- retention (decay) */
+
+/* Decay of token t of head h: gates[h][t] when given (gated retention),
+ * else gamma_head[h % H] (RetNet, one decay per head), else 1 (linear
+ * attention without reflection).  `h` counts B*H heads, head index h % H. */
+static double decay_of(int h, int t, int N, int H, const double* gamma_head, const double* gates) {
+    if (gates) return gates[(size_t)h * N + t];
+    if (gamma_head) return gamma_head[h % H];
+    return 1.0;
+}
+
+/* "Transformer and Variants" section 1.3.2 (linear attention as an RNN without
+ * the reflection term) and section 1.3.4 (RetNet, gated retention), in the
+ * S = sum k v^T convention used throughout (S is the page's H transposed):
+ *   S_t = gamma_t S_{t-1} + k_t v_t^T,   y_t = S_t^T q_t
+ * raw q and k (no feature map) and no normaliser.  S0 (nullable) is the state
+ * before token 0, S_out (nullable) receives the state after the last token. */
+void lao_retention_forward_recurrent(int nh, int H, int N, int D, int M, const double* Q,
+                                     const double* K, const double* V, const double* gamma_head,
+                                     const double* gates, const double* S0, double* O,
+                                     double* S_out) {
+    double* S = (double*)malloc(sizeof(double) * (size_t)D * M);
+    for (int h = 0; h < nh; ++h) {
+        const double* Qh = Q + (size_t)h * N * D;
+        const double* Kh = K + (size_t)h * N * D;
+        const double* Vh = V + (size_t)h * N * M;
+        double* Oh = O + (size_t)h * N * M;
+        if (S0) memcpy(S, S0 + (size_t)h * D * M, sizeof(double) * (size_t)D * M);
+        else memset(S, 0, sizeof(double) * (size_t)D * M);
+        for (int t = 0; t < N; ++t) {
+            const double g = decay_of(h, t, N, H, gamma_head, gates);
+            for (int d = 0; d < D; ++d)
+                for (int e = 0; e < M; ++e)
+                    S[(size_t)d * M + e] = g * S[(size_t)d * M + e] +
+                                           Kh[(size_t)t * D + d] * Vh[(size_t)t * M + e];
+            for (int e = 0; e < M; ++e) {
+                double y = 0.0;
+                for (int d = 0; d < D; ++d) y += S[(size_t)d * M + e] * Qh[(size_t)t * D + d];
+                Oh[(size_t)t * M + e] = y;
+            }
+        }
+        if (S_out) memcpy(S_out + (size_t)h * D * M, S, sizeof(double) * (size_t)D * M);
+    }
+    free(S);
+}
+
+/* The same output unrolled (section 1.3.1's expansion of y_t as a sum over
+ * j <= t, with the decays of the later tokens multiplied in):
+ *   y_t = sum_{j<=t} (prod_{l=j+1..t} gamma_l) (k_j . q_t) v_j
+ * (no initial state). */
+void lao_retention_forward_quadratic(int nh, int H, int N, int D, int M, const double* Q,
+                                     const double* K, const double* V, const double* gamma_head,
+                                     const double* gates, double* O) {
+    for (int h = 0; h < nh; ++h) {
+        const double* Qh = Q + (size_t)h * N * D;
+        const double* Kh = K + (size_t)h * N * D;
+        const double* Vh = V + (size_t)h * N * M;
+        double* Oh = O + (size_t)h * N * M;
+        for (int t = 0; t < N; ++t) {
+            for (int e = 0; e < M; ++e) Oh[(size_t)t * M + e] = 0.0;
+            double prod = 1.0; /* prod_{l=j+1..t} gamma_l, built as j walks down from t */
+            for (int j = t; j >= 0; --j) {
+                const double a = prod * dot(Kh + (size_t)j * D, Qh + (size_t)t * D, D);
+                for (int e = 0; e < M; ++e) Oh[(size_t)t * M + e] += a * Vh[(size_t)j * M + e];
+                prod *= decay_of(h, j, N, H, gamma_head, gates);
+            }
+        }
+    }
+}
+
+/* One decode step of the retention recurrence: S = gamma S + k v^T, then
+ * out = S^T q.  gamma [nh] (the step's decay of each head), q, k [nh][D],
+ * v, out [nh][M]; S [nh][D][M] updated in place. */
+void lao_retention_decode_step(int nh, int D, int M, const double* q, const double* k,
+                               const double* v, const double* gamma, double* S, double* out) {
+    for (int h = 0; h < nh; ++h) {
+        double* Sh = S + (size_t)h * D * M;
+        for (int d = 0; d < D; ++d)
+            for (int e = 0; e < M; ++e)
+                Sh[(size_t)d * M + e] = gamma[h] * Sh[(size_t)d * M + e] +
+                                        k[(size_t)h * D + d] * v[(size_t)h * M + e];
+        for (int e = 0; e < M; ++e) {
+            double y = 0.0;
+            for (int d = 0; d < D; ++d) y += Sh[(size_t)d * M + e] * q[(size_t)h * D + d];
+            out[(size_t)h * M + e] = y;
+        }
+    }
+}

@@ -89,6 +89,22 @@ void lao_decode_step(int nh, int D, int M, const double* q, const double* k,
 void lao_softmax_decode_step(int nh, int T, int D, int M, const double* q, const double* k,
                              const double* v, const double* Kc, const double* Vc, double* out);
 
+/* Retention ("Transformer and Variants" sections 1.3.2 and 1.3.4): S_t =
+ * gamma_t S_{t-1} + k_t v_t^T, y_t = S_t^T q_t, raw q, k, no normaliser.
+ * gamma_t = gates[h][t] if gates, else gamma_head[h % H] if gamma_head, else 1
+ * (h over nh = B*H heads).  Recurrent form (with optional S0 / S_out) and the
+ * unrolled sum over j <= t. */
+void lao_retention_forward_recurrent(int nh, int H, int N, int D, int M, const double* Q,
+                                     const double* K, const double* V, const double* gamma_head,
+                                     const double* gates, const double* S0, double* O,
+                                     double* S_out);
+void lao_retention_forward_quadratic(int nh, int H, int N, int D, int M, const double* Q,
+                                     const double* K, const double* V, const double* gamma_head,
+                                     const double* gates, double* O);
+/* One retention decode step per head: S = gamma S + k v^T, out = S^T q. */
+void lao_retention_decode_step(int nh, int D, int M, const double* q, const double* k,
+                               const double* v, const double* gamma, double* S, double* out);
+
 #ifdef __cplusplus
 }
 #endif

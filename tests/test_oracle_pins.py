@@ -404,3 +404,88 @@ def test_softmax_decode_matches_library_softmax_and_special_cases():
     c = _rand((nh, 1, D), 95)
     np.testing.assert_allclose(oracle.softmax_decode_step(q, k + c[:, 0], v, Kc + c, Vc), out,
                                rtol=1e-11, atol=1e-12)
+
+
+# ------------------------------------------------------- retention pins
+
+def _ret_case(name):
+    g = _golden()[name]
+    q, k, v = (np.array(g[n], float) for n in ("q", "k", "v"))
+    if q.ndim == 1:
+        q, k, v = q[:, None], k[:, None], v[:, None]
+    return g, q[None, None], k[None, None], v[None, None]
+
+
+def test_golden_retention_scalar():
+    g, Q, K, V = _ret_case("retention_3x1x1")
+    gam = np.array([_eval_expr(g["gamma"])])
+    gates = _arr(g["gates"])[None, None]
+    for kw, want in (({}, "y_decay1"), ({"gamma_head": gam}, "y_retnet"), ({"gates": gates}, "y_gated")):
+        w = _arr(g[want])
+        np.testing.assert_allclose(oracle.retention_forward_recurrent(Q, K, V, **kw)[0][0, 0, :, 0], w,
+                                   rtol=1e-14)
+        np.testing.assert_allclose(oracle.retention_forward_quadratic(Q, K, V, **kw)[0, 0, :, 0], w,
+                                   rtol=1e-14)
+
+
+def test_golden_retention_orientation():
+    g, Q, K, V = _ret_case("retention_2x2x2")
+    O, S = oracle.retention_forward_recurrent(Q, K, V)
+    np.testing.assert_allclose(O[0, 0], _arr(g["y_decay1"]), rtol=1e-14)
+    np.testing.assert_allclose(S[0, 0], _arr(g["S_decay1"]), rtol=1e-14)
+    O, S = oracle.retention_forward_recurrent(Q, K, V, gamma_head=np.array([0.5]))
+    np.testing.assert_allclose(O[0, 0], _arr(g["y_half"]), rtol=1e-14)
+    np.testing.assert_allclose(S[0, 0], _arr(g["S_half"]), rtol=1e-14)
+    # decode continues: the second token as a decode step after the first
+    _, S1 = oracle.retention_forward_recurrent(Q[:, :, :1], K[:, :, :1], V[:, :, :1])
+    out, S2 = oracle.retention_decode_step(Q[0, 0, 1], K[0, 0, 1], V[0, 0, 1], np.array(0.5), S1[0, 0])
+    np.testing.assert_allclose(out, _arr(g["y_half"])[1], rtol=1e-14)
+    np.testing.assert_allclose(S2, _arr(g["S_half"]), rtol=1e-14)
+
+
+def test_retention_against_library_masks():
+    B, H, N, D, M = 2, 3, 29, 5, 4
+    Q, K, V = _rand((B, H, N, D), 110), _rand((B, H, N, D), 111), _rand((B, H, N, M), 112)
+    A = np.einsum("bhid,bhjd->bhij", Q, K)
+    # decay 1: y = tril(Q K^T) V
+    np.testing.assert_allclose(oracle.retention_forward_recurrent(Q, K, V)[0],
+                               np.tril(A) @ V, rtol=1e-11, atol=1e-12)
+    # RetNet: y = (tril(Q K^T) * gamma^(i-j)) V, one gamma per head
+    gam = np.array([0.9, 0.5, 0.99])
+    i = np.arange(N)
+    Gm = np.where(i[:, None] >= i[None, :], gam[:, None, None] ** np.maximum(i[:, None] - i[None, :], 0), 0.0)
+    want = (A * Gm[None]) @ V
+    np.testing.assert_allclose(oracle.retention_forward_recurrent(Q, K, V, gamma_head=gam)[0], want,
+                               rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(oracle.retention_forward_quadratic(Q, K, V, gamma_head=gam), want,
+                               rtol=1e-10, atol=1e-12)
+
+
+def test_retention_gated_forms_and_special_cases():
+    B, H, N, D, M = 2, 2, 33, 4, 3
+    Q, K, V = _rand((B, H, N, D), 113), _rand((B, H, N, D), 114), _rand((B, H, N, M), 115)
+    gates = np.random.default_rng(116).uniform(0.5, 1.0, (B, H, N))
+    a = oracle.retention_forward_recurrent(Q, K, V, gates=gates)[0]
+    np.testing.assert_allclose(a, oracle.retention_forward_quadratic(Q, K, V, gates=gates), rtol=1e-10,
+                               atol=1e-12)
+    # gates equal to a per-head constant are RetNet
+    gam = np.array([0.8, 0.95])
+    np.testing.assert_allclose(
+        oracle.retention_forward_recurrent(Q, K, V, gates=np.broadcast_to(gam[None, :, None], (B, H, N)))[0],
+        oracle.retention_forward_recurrent(Q, K, V, gamma_head=gam)[0], rtol=1e-13)
+    # zero decay forgets everything: y_t = (q_t . k_t) v_t
+    y0 = oracle.retention_forward_recurrent(Q, K, V, gates=np.zeros((B, H, N)))[0]
+    np.testing.assert_allclose(y0, np.einsum("bhnd,bhnd->bhn", Q, K)[..., None] * V, rtol=1e-12)
+    # a carried-in state splits the sequence
+    cut = 14
+    O, S = oracle.retention_forward_recurrent(Q, K, V, gates=gates)
+    Oa, Sa = oracle.retention_forward_recurrent(Q[:, :, :cut], K[:, :, :cut], V[:, :, :cut], gates=gates[:, :, :cut])
+    Ob, Sb = oracle.retention_forward_recurrent(Q[:, :, cut:], K[:, :, cut:], V[:, :, cut:],
+                                                gates=gates[:, :, cut:], S0=Sa)
+    np.testing.assert_allclose(np.concatenate([Oa, Ob], 2), O, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(Sb, S, rtol=1e-12, atol=1e-13)
+    # decode steps continue the forward
+    _, Sd = oracle.retention_forward_recurrent(Q[:, :, :cut], K[:, :, :cut], V[:, :, :cut], gates=gates[:, :, :cut])
+    for t in range(cut, N):
+        out, Sd = oracle.retention_decode_step(Q[:, :, t], K[:, :, t], V[:, :, t], gates[:, :, t], Sd)
+        np.testing.assert_allclose(out, O[:, :, t], rtol=1e-11, atol=1e-12)
