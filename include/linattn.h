@@ -158,6 +158,42 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
                          float* out, int B, int H, int D, int M, la_dtype dtype, void* stream);
 
 /*
+ * Linear attention with decay ("retention"), as "Transformer and Variants"
+ * (by-xin.github.io) writes it: section 1.3.2 (linear attention as an RNN
+ * without the reflection term, no softmax and no normaliser) and section
+ * 1.3.4 (RetNet: a decay gamma per head; gated retention: a decay gamma_t per
+ * token), with the state in the S = sum k v^T convention (the page's H
+ * transposed):
+ *     S_t = gamma_t S_{t-1} + k_t v_t^T,   Out_t = S_t^T q_t
+ * Raw Q and K (no feature map).
+ *   Q, K [B][H][N][D]; V [B][H][N][M] dtype (read);  Out [B][H][N][M] dtype (written)
+ *   gamma_head [H] fp32, nullable: RetNet's decay of each head
+ *   gates      [B][H][N] fp32, nullable: gated retention's decay of every token
+ *              (the page's sigmoid(W_gamma x_t), computed by the caller)
+ *   neither: decay 1 (the unnormalised form); both: LA_ERR_INVALID_ARG.
+ *   Decays lie in (0, 1]; one below 2^-64 acts as 2^-64.
+ *   S_init [B][H][D][M] fp32, nullable (read): state before token 0 (0 if NULL)
+ *   S_final [B][H][D][M] fp32, nullable (written): state after token N-1
+ */
+la_status la_forward_retention(const void* Q, const void* K, const void* V, void* Out, int B,
+                               int H, int N, int D, int M, la_dtype dtype, const float* gamma_head,
+                               const float* gates, const float* S_init, float* S_final,
+                               void* stream);
+
+/*
+ * One retention decode step for B*H heads: S = gamma S + k v^T, then
+ * out = S^T q ("Transformer and Variants" section 1.3.4, RNN form).
+ *   q, k [B][H][D]; v [B][H][M] dtype      (read)
+ *   gamma_head [H] fp32, nullable; gate [B][H] fp32, nullable (this step's
+ *   decay of each head); neither: decay 1
+ *   S [B][H][D][M] fp32                    (read and updated in place)
+ *   out [B][H][M] fp32                     (written)
+ */
+la_status la_retention_decode_step(const void* q, const void* k, const void* v,
+                                   const float* gamma_head, const float* gate, float* S, float* out,
+                                   int B, int H, int D, int M, la_dtype dtype, void* stream);
+
+/*
  * One decode step of standard softmax attention with a KV cache, the baseline
  * the recurrent step is measured against ("Transformer与RNN的深层联结",
  * section 2, standard Transformer inference: the step's k, v are appended to
@@ -212,7 +248,8 @@ la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void*
  * this function says how many bytes of it one call holds at its peak.
  *   op       the entry point's name: "la_forward_causal", "la_backward_causal",
  *            "la_forward_noncausal", "la_backward_noncausal", "la_decode_step" (0),
- *            "la_softmax_decode_step" (N = the cache position T) or
+ *            "la_softmax_decode_step" (N = the cache position T),
+ *            "la_forward_retention", "la_retention_decode_step" (0) or
  *            "la_forward_noncausal_noalloc" (0: it uses its fixed array)
  *   B..M, dtype  the call's sizes and dtype (N is ignored for decode)
  *   saved    for "la_backward_causal": an OR of LA_SAVED_OUT, LA_SAVED_DEN and

@@ -253,6 +253,68 @@ LA_SAVED_OUT, LA_SAVED_DEN, LA_SAVED_CKPT = (_native.LA_SAVED_OUT, _native.LA_SA
                                              _native.LA_SAVED_CKPT)
 
 
+def _decay_args(gamma_head, gates, shape, dev, name):
+    if gamma_head is not None and gates is not None:
+        raise ValueError(f"give gamma_head or {name}, not both")
+    if gamma_head is not None:
+        _need(gamma_head, "gamma_head", torch.float32, dev)
+        if tuple(gamma_head.shape) != (shape[1],):
+            raise ValueError(f"gamma_head must be [H] = {(shape[1],)}")
+    if gates is not None:
+        _need(gates, name, torch.float32, dev)
+        if tuple(gates.shape) != tuple(shape):
+            raise ValueError(f"{name} must be {tuple(shape)}, got {tuple(gates.shape)}")
+
+
+def la_forward_retention(Q, K, V, gamma_head=None, gates=None, out=None, S_init=None,
+                         return_state=False, stream=None):
+    """Linear attention with decay: S_t = gamma_t S_{t-1} + k_t v_t^T, Out_t = S_t^T q_t.
+
+    gamma_head [H] (RetNet), gates [B,H,N] (gated retention) or neither (decay 1).
+    Returns Out, or (Out, S_final) with return_state."""
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, Q.dtype, dev)
+    if K.shape != Q.shape:
+        raise ValueError("K must have the shape of Q")
+    _decay_args(gamma_head, gates, (B, H, N), dev, "gates")
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=Q.dtype, device=dev)
+    _need(out, "out", Q.dtype, dev)
+    if S_init is not None:
+        _need(S_init, "S_init", torch.float32, dev)
+    S_f = torch.empty((B, H, D, M), dtype=torch.float32, device=dev) if return_state else None
+    with torch.cuda.device(dev):
+        _check(_lib.la_forward_retention(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D, M,
+                                         _dtype(Q), _ptr(gamma_head), _ptr(gates), _ptr(S_init),
+                                         _ptr(S_f), _stream_handle(stream)))
+    return (out, S_f) if return_state else out
+
+
+def la_retention_decode_step(q, k, v, S, gamma_head=None, gate=None, out=None, stream=None):
+    """One retention step: S = gamma S + k v^T (in place), returns out = S^T q [B,H,M] fp32."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q/k must be [B,H,D] and v [B,H,M]")
+    B, H, D = q.shape
+    M = v.shape[2]
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, dev)
+    _need(S, "S", torch.float32, dev)
+    if tuple(S.shape) != (B, H, D, M):
+        raise ValueError("S must be [B,H,D,M]")
+    _decay_args(gamma_head, gate, (B, H), dev, "gate")
+    if out is None:
+        out = torch.empty((B, H, M), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_retention_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma_head), _ptr(gate),
+                                             _ptr(S), _ptr(out), B, H, D, M, _dtype(q),
+                                             _stream_handle(stream)))
+    return out
+
+
 def la_softmax_decode_step(q, k, v, K_cache, V_cache, T, out=None, stream=None):
     """Softmax attention decode step with a KV cache (the comparator of la_decode_step).
 

@@ -206,6 +206,23 @@ struct BwdNoncausal {
                                            (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
     }
 };
+struct FwdRetention {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
+                           const float* gh, const float* gt, int BH, int H, int N, const float* Si,
+                           float* Sf) {
+        return retention_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, gh, gt,
+                                          BH, H, N, Si, Sf);
+    }
+};
+struct RetentionStep {
+    template <typename T, int D, int M>
+    static cudaError_t run(const LaunchCtx* c, const void* q, const void* k, const void* v,
+                           const float* gh, const float* gt, float* S, float* out, int BH, int H) {
+        return retention_step<T, D, M>(*c, (const T*)q, (const T*)k, (const T*)v, gh, gt, S, out, BH,
+                                       H);
+    }
+};
 struct Decode {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* q, const void* k, const void* v,
@@ -262,6 +279,8 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
         return plan::ffma_noncausal_forward(BH, N, D, M, sms);
     }
     if (!strcmp(op, "la_backward_noncausal")) return plan::ffma_noncausal_backward(BH, N, D, M, sms);
+    if (!strcmp(op, "la_forward_retention")) return plan::ffma_retention_forward(BH, N, D, M, sms);
+    if (!strcmp(op, "la_retention_decode_step")) return 0;
     if (!strcmp(op, "la_softmax_decode_step"))  // N is the cache position T: T + 1 positions
         return D == M ? plan::softmax_decode_scratch(BH, N + 1, D, sms) : SIZE_MAX;
     if (!strcmp(op, "la_decode_step") || !strcmp(op, "la_forward_noncausal_noalloc")) return 0;
@@ -416,6 +435,56 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
     LaunchCtx ctx;
     if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
     return finish(dispatch<Decode>(dtype, D, M, &ctx, q, k, v, S, Z, out, (int)((size_t)B * H)), fn);
+}
+
+la_status la_forward_retention(const void* Q, const void* K, const void* V, void* Out, int B,
+                               int H, int N, int D, int M, la_dtype dtype, const float* gamma_head,
+                               const float* gates, const float* S_init, float* S_final,
+                               void* stream) {
+    static const char* fn = "la_forward_retention";
+    const void* p[] = {Q, K, V, Out};
+    const char* nm[] = {"Q", "K", "V", "Out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 4, &empty);
+    if (s != LA_OK) return s;
+    if (gamma_head && gates)
+        return fail(LA_ERR_INVALID_ARG, "%s: give gamma_head or gates, not both", fn);
+    if ((s = check_optional(fn, S_init, "S_init")) || (s = check_optional(fn, S_final, "S_final")))
+        return s;
+    if (((uintptr_t)gamma_head | (uintptr_t)gates) & 3u)
+        return fail(LA_ERR_INVALID_ARG, "%s: gamma_head / gates not 4-byte aligned", fn);
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    const size_t bh = (size_t)B * H;
+    if (empty) {
+        if (!S_final || bh == 0) return LA_OK;
+        const size_t sb = bh * D * M * sizeof(float);
+        return finish(S_init ? cudaMemcpyAsync(S_final, S_init, sb, cudaMemcpyDeviceToDevice, ctx.stream)
+                             : cudaMemsetAsync(S_final, 0, sb, ctx.stream),
+                      fn);
+    }
+    return finish(dispatch<FwdRetention>(dtype, D, M, &ctx, Q, K, V, Out, gamma_head, gates, (int)bh,
+                                         H, N, S_init, S_final),
+                  fn);
+}
+
+la_status la_retention_decode_step(const void* q, const void* k, const void* v,
+                                   const float* gamma_head, const float* gate, float* S, float* out,
+                                   int B, int H, int D, int M, la_dtype dtype, void* stream) {
+    static const char* fn = "la_retention_decode_step";
+    const void* p[] = {q, k, v, S, out};
+    const char* nm[] = {"q", "k", "v", "S", "out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, 1, D, M, dtype, p, nm, 5, &empty);
+    if (s != LA_OK || empty) return s;
+    if (gamma_head && gate) return fail(LA_ERR_INVALID_ARG, "%s: give gamma_head or gate, not both", fn);
+    if (((uintptr_t)gamma_head | (uintptr_t)gate) & 3u)
+        return fail(LA_ERR_INVALID_ARG, "%s: gamma_head / gate not 4-byte aligned", fn);
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    return finish(dispatch<RetentionStep>(dtype, D, M, &ctx, q, k, v, gamma_head, gate, S, out,
+                                          (int)((size_t)B * H), H),
+                  fn);
 }
 
 la_status la_softmax_decode_step(const void* q, const void* k, const void* v, void* K_cache,

@@ -85,6 +85,19 @@ template <typename T, int D>
 cudaError_t softmax_decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, T* Kc,
                                 T* Vc, int T_len, int T_max, float* out, int BH);
 
+// Retention (decayed, unnormalised linear attention) forward on the CUDA cores:
+// gamma_head [H] or gates [BH][N] (per token) or neither (decay 1).
+template <typename T, int D, int M>
+cudaError_t retention_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O,
+                              const float* gamma_head, const float* gates, int BH, int H, int N,
+                              const float* S_init, float* S_final);
+
+// One retention decode step: S = gamma S + k v^T, out = S^T q.
+template <typename T, int D, int M>
+cudaError_t retention_step(const LaunchCtx& c, const T* q, const T* k, const T* v,
+                           const float* gamma_head, const float* gate, float* S, float* out, int BH,
+                           int H);
+
 template <typename T, int D, int M>
 cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
                         float* Z, float* out, int BH);

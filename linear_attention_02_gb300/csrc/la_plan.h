@@ -78,6 +78,14 @@ inline size_t softmax_decode_scratch(int BH, int total, int D, int num_sms) {
     return sizeof(float) * static_cast<size_t>(BH) * splits * (D + 2);
 }
 
+// CUDA-core retention forward: per-span aggregates (D x M, no normaliser) and
+// per-span total log2 decays, only when a head has several spans.
+inline size_t ffma_retention_forward(int BH, int N, int D, int M, int num_sms) {
+    const int spans = ffma_span_count(BH, N, D, M, num_sms);
+    return spans > 1 ? sizeof(float) * static_cast<size_t>(BH) * spans * (static_cast<size_t>(D) * M + 1)
+                     : 0;
+}
+
 // Tensor-core causal kernels: the chunks of all heads cut into equal ranges,
 // one per resident CTA (see tc_common.cuh, split_chunks).
 inline int tc_units(int BH, int chunks_per_head, int slots) {

@@ -112,12 +112,16 @@ softmax_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
 
-    for (int jb = j0 + warp * RPW + slot; jb < j1; jb += kSdUnroll * STEP) {
+    // The loop bound is the warp's (wb), the same for all of its lanes, so every
+    // lane takes part in every shuffle below; rows at or past j1 are skipped
+    // after the shuffle.
+    for (int wb = j0 + warp * RPW; wb < j1; wb += kSdUnroll * STEP) {
+        const int jb = wb + slot;
         uint4 kr[kSdUnroll], vr[kSdUnroll];
 #pragma unroll
         for (int u = 0; u < kSdUnroll; ++u) {  // every load of this step first
             const int j = jb + u * STEP;
-            if (j < T_len) {
+            if (j < T_len && j < j1) {
                 kr[u] = __ldcs(K4 + static_cast<size_t>(j) * ROW4);
                 vr[u] = __ldcs(V4 + static_cast<size_t>(j) * ROW4);
             } else {

@@ -120,3 +120,10 @@ def decode_step_qkv(B: int, H: int, D: int, M: int, dtype: str, seed: int, step:
             x.add_(qk_mean)
         out[name] = x.to(torch_dtype(dtype))
     return out
+
+
+def decays(shape, seed: int, lo: float = 0.85, hi: float = 1.0, device: str = "cpu") -> torch.Tensor:
+    """fp32 decays drawn uniformly in [lo, hi): one per head (RetNet's gamma) or
+    one per token (gated retention's gamma_t)."""
+    g = _gen(seed, device)
+    return torch.rand(tuple(shape), generator=g, dtype=torch.float32, device=device).mul_(hi - lo).add_(lo)
