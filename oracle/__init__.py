@@ -69,12 +69,15 @@ def _load():
     lib.lao_retention_forward_recurrent.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P]
     lib.lao_retention_forward_quadratic.argtypes = [I, I, I, I, I, P, P, P, P, P, P]
     lib.lao_retention_decode_step.argtypes = [I, I, I, P, P, P, P, P, P]
+    lib.lao_poly_forward_quadratic.argtypes = [I, I, I, I, P, P, P, P, I]
+    lib.lao_poly_forward_state.argtypes = [I, I, I, I, P, P, P, P, I]
     for f in ("lao_causal_forward_quadratic", "lao_causal_forward_recurrent",
               "lao_noncausal_forward_quadratic", "lao_noncausal_forward_assoc",
               "lao_causal_backward_cumsum", "lao_causal_backward_quadratic", "lao_decode_step",
               "lao_noncausal_backward_assoc", "lao_noncausal_backward_quadratic",
               "lao_softmax_decode_step", "lao_retention_forward_recurrent",
-              "lao_retention_forward_quadratic", "lao_retention_decode_step"):
+              "lao_retention_forward_quadratic", "lao_retention_decode_step",
+              "lao_poly_forward_quadratic", "lao_poly_forward_state"):
         getattr(lib, f).restype = None
     _lib = lib
     return lib
@@ -267,3 +270,22 @@ def retention_decode_step(q, k, v, gamma, S):
     out = np.empty(q.shape[:-1] + (M,))
     _load().lao_retention_decode_step(nh, D, M, _p(q), _p(k), _p(v), _p(g), _p(S), _p(out))
     return out, S
+
+
+def _poly(fn, Q, K, V, causal):
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    lead, nh, N = _heads(Q, Q.shape[-1])
+    D, M = Q.shape[-1], V.shape[-1]
+    O = np.empty(lead + (N, M))
+    fn(nh, N, D, M, _p(Q), _p(K), _p(V), _p(O), 1 if causal else 0)
+    return O
+
+
+def poly_forward_quadratic(Q, K, V, causal=True):
+    """Attention with similarity (Q_i . K_j)^2, written out directly."""
+    return _poly(_load().lao_poly_forward_quadratic, Q, K, V, causal)
+
+
+def poly_forward_state(Q, K, V, causal=True):
+    """The same through the explicit degree-2 feature map (C = D^2 state)."""
+    return _poly(_load().lao_poly_forward_state, Q, K, V, causal)

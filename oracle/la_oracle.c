@@ -730,3 +730,83 @@ void lao_retention_decode_step(int nh, int D, int M, const double* q, const doub
         }
     }
 }
+
+/* ------------------------------------- degree-2 polynomial feature map */
+
+/* "【论文解读】Transformers are RNNs" section 二 (3): the homogeneous
+ * polynomial kernel k(x, y) = (x^T y)^2 as the similarity of the general
+ * attention form (eq. common), causal (j <= i, eq. mask) or over all j:
+ *   V'_i = sum_j (Q_i . K_j)^2 V_j / sum_j (Q_i . K_j)^2
+ * written out directly, O(N^2 D) per head. */
+void lao_poly_forward_quadratic(int nh, int N, int D, int M, const double* Q, const double* K,
+                                const double* V, double* O, int causal) {
+    double* num = (double*)malloc(sizeof(double) * (size_t)M);
+    for (int h = 0; h < nh; ++h) {
+        const double* Qh = Q + (size_t)h * N * D;
+        const double* Kh = K + (size_t)h * N * D;
+        const double* Vh = V + (size_t)h * N * M;
+        double* Oh = O + (size_t)h * N * M;
+        for (int i = 0; i < N; ++i) {
+            const int jmax = causal ? i : N - 1;
+            double den = 0.0;
+            memset(num, 0, sizeof(double) * (size_t)M);
+            for (int j = 0; j <= jmax; ++j) {
+                const double d = dot(Qh + (size_t)i * D, Kh + (size_t)j * D, D);
+                const double w = d * d;
+                den += w;
+                for (int e = 0; e < M; ++e) num[e] += w * Vh[(size_t)j * M + e];
+            }
+            for (int e = 0; e < M; ++e) Oh[(size_t)i * M + e] = num[e] / den;
+        }
+    }
+    free(num);
+}
+
+/* The same through the explicit feature map of that section: phi(x) has the
+ * C = D^2 entries x_a x_b (index a D + b), so phi(x) . phi(y) = (x . y)^2, and
+ * the linear form keeps S = sum_j phi(K_j) V_j^T (C x M) and Z = sum_j phi(K_j)
+ * -- causal: the running sums of section 三 read after each token's update;
+ * otherwise the totals.  O(N D^2 M) per head. */
+void lao_poly_forward_state(int nh, int N, int D, int M, const double* Q, const double* K,
+                            const double* V, double* O, int causal) {
+    const int C = D * D;
+    double* S = (double*)malloc(sizeof(double) * (size_t)C * M);
+    double* Z = (double*)malloc(sizeof(double) * (size_t)C);
+    double* f = (double*)malloc(sizeof(double) * (size_t)C);
+    for (int h = 0; h < nh; ++h) {
+        const double* Qh = Q + (size_t)h * N * D;
+        const double* Kh = K + (size_t)h * N * D;
+        const double* Vh = V + (size_t)h * N * M;
+        double* Oh = O + (size_t)h * N * M;
+        memset(S, 0, sizeof(double) * (size_t)C * M);
+        memset(Z, 0, sizeof(double) * (size_t)C);
+        for (int pass = causal ? 1 : 0; pass < 2; ++pass) {
+            /* non-causal: pass 0 forms the totals, pass 1 reads them */
+            for (int t = 0; t < N; ++t) {
+                if (causal || pass == 0) {
+                    const double* k = Kh + (size_t)t * D;
+                    for (int a = 0; a < D; ++a)
+                        for (int b = 0; b < D; ++b) f[a * D + b] = k[a] * k[b];
+                    for (int c = 0; c < C; ++c) {
+                        for (int e = 0; e < M; ++e) S[(size_t)c * M + e] += f[c] * Vh[(size_t)t * M + e];
+                        Z[c] += f[c];
+                    }
+                }
+                if (pass == 1) {
+                    const double* q = Qh + (size_t)t * D;
+                    for (int a = 0; a < D; ++a)
+                        for (int b = 0; b < D; ++b) f[a * D + b] = q[a] * q[b];
+                    const double den = dot(f, Z, C);
+                    for (int e = 0; e < M; ++e) {
+                        double num = 0.0;
+                        for (int c = 0; c < C; ++c) num += f[c] * S[(size_t)c * M + e];
+                        Oh[(size_t)t * M + e] = num / den;
+                    }
+                }
+            }
+        }
+    }
+    free(S);
+    free(Z);
+    free(f);
+}

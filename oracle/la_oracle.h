@@ -105,6 +105,15 @@ void lao_retention_forward_quadratic(int nh, int H, int N, int D, int M, const d
 void lao_retention_decode_step(int nh, int D, int M, const double* q, const double* k,
                                const double* v, const double* gamma, double* S, double* out);
 
+/* Degree-2 polynomial similarity (x^T y)^2 ("Transformers are RNNs" section
+ * 二 (3)): the quadratic form, and the linear form through the explicit
+ * feature map phi(x) = (x_a x_b), C = D^2 (state S: C x M, Z: C).  causal != 0
+ * keeps j <= i. */
+void lao_poly_forward_quadratic(int nh, int N, int D, int M, const double* Q, const double* K,
+                                const double* V, double* O, int causal);
+void lao_poly_forward_state(int nh, int N, int D, int M, const double* Q, const double* K,
+                            const double* V, double* O, int causal);
+
 #ifdef __cplusplus
 }
 #endif

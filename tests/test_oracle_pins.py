@@ -489,3 +489,42 @@ def test_retention_gated_forms_and_special_cases():
     for t in range(cut, N):
         out, Sd = oracle.retention_decode_step(Q[:, :, t], K[:, :, t], V[:, :, t], gates[:, :, t], Sd)
         np.testing.assert_allclose(out, O[:, :, t], rtol=1e-11, atol=1e-12)
+
+
+# ------------------------------------------- degree-2 polynomial kernel pins
+
+def test_golden_poly_both_forms():
+    g = _golden()["poly_2x2x1"]
+    Q, K, V = (np.array(g[k], float) for k in ("Q", "K", "V"))
+    for causal, key in ((True, "causal_O"), (False, "noncausal_O")):
+        want = _arr(g[key])
+        np.testing.assert_allclose(oracle.poly_forward_quadratic(Q, K, V, causal), want, rtol=1e-14)
+        np.testing.assert_allclose(oracle.poly_forward_state(Q, K, V, causal), want, rtol=1e-14)
+
+
+@pytest.mark.parametrize("nh,N,D,M", [(1, 9, 2, 3), (2, 30, 4, 5), (3, 17, 8, 2)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_poly_forms_agree_and_match_library(nh, N, D, M, causal):
+    Q, K, V = _rand((nh, N, D), 130), _rand((nh, N, D), 131), _rand((nh, N, M), 132)
+    a = oracle.poly_forward_quadratic(Q, K, V, causal)
+    b = oracle.poly_forward_state(Q, K, V, causal)
+    np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-11)
+    W = np.einsum("hid,hjd->hij", Q, K) ** 2
+    if causal:
+        W = np.tril(W)
+    np.testing.assert_allclose(a, (W @ V) / W.sum(-1, keepdims=True), rtol=1e-11, atol=1e-12)
+
+
+def test_poly_invariants():
+    nh, N, D, M = 2, 40, 4, 3
+    Q, K, V = _rand((nh, N, D), 133), _rand((nh, N, D), 134), _rand((nh, N, M), 135)
+    O = oracle.poly_forward_state(Q, K, V)
+    np.testing.assert_allclose(O[:, 0], V[:, 0], rtol=1e-13)       # row 1 sees only V_1
+    sgn = np.where(np.random.default_rng(136).random((nh, N, 1)) < 0.5, -1.0, 1.0)
+    np.testing.assert_allclose(oracle.poly_forward_state(Q * sgn, -K, V), O, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(oracle.poly_forward_state(3.0 * Q, 0.5 * K, V), O, rtol=1e-11, atol=1e-12)
+    lo, hi = np.minimum.accumulate(V, axis=1), np.maximum.accumulate(V, axis=1)
+    assert np.all(O >= lo - 1e-12) and np.all(O <= hi + 1e-12)
+    Ke = np.broadcast_to(K[:, :1], K.shape).copy()
+    np.testing.assert_allclose(oracle.poly_forward_quadratic(Q, Ke, V),
+                               np.cumsum(V, 1) / np.arange(1, N + 1)[None, :, None], rtol=1e-12)
