@@ -9,8 +9,10 @@ Also measured in the same run (the "paths" object): the causal forward alone,
 the long-sequence forward (B=1, H=16, N=65536, D=M=128), the non-causal fp32
 forward and backward (B=8, H=8, N=4096, D=M=64), one decode step of 256 sequences x 16
 heads (D=M=64, fp32 state), the softmax KV-cache decode step it replaces (the
-same heads with a full 4096-position cache) and the 2048-token prefill that
-hands the decode its state (the causal forward emitting the final S, Z of every head), each
+same heads with a full 4096-position cache), gated retention (forward on the
+training shape, one decode step), the degree-2 polynomial feature map (causal,
+B=4 H=16 N=4096 D=32 M=64, against the FP32 FMA rate) and the 2048-token prefill that hands the
+decode its state (the causal forward emitting the final S, Z of every head), each
 with its fraction of the HBM roofline.
 
 Timing: W untimed warm-up steps, then K steps between a barrier and a device
@@ -189,6 +191,17 @@ def _bytes_bwd(B, H, N, D, M, esz, with_out=True, den=False):
 
 def _bytes_decode(B, H, D, M, esz):
     return B * H * (2 * D * M * 4 + 2 * D * 4 + (2 * D + M) * esz + M * 4)
+
+
+def _fp32_fma_tflops(torch):
+    """FP32 FMA peak of this GPU: SMs x 128 FMA lanes x 2 flops x the maximum SM clock."""
+    pr = torch.cuda.get_device_properties(torch.cuda.current_device())
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    return pr.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
 
 
 def _time_events(torch, fn, reps, stream, flush=None):
@@ -472,6 +485,51 @@ def measure_paths(torch, la, synth, stream, hbm, fwd_ms, bwd_ms, fwd_bytes, bwd_
         "cache_positions": T + 1, "l2": "flushed before each step",
         "time_vs_recurrent_step": round(ms / lin_ms, 2)})
     del Kc, Vc, out, steps, flush_buf
+
+    # retention (decayed, unnormalised linear attention): gated decays on the training
+    # workload's shape, and one gated decode step of the decode workload's heads
+    wt = synth.WORKLOADS[HEADLINE]
+    x = synth.qkv(wt.B, wt.H, wt.N, wt.D, wt.M, wt.dtype, wt.seed, wt.scale, device="cuda")
+    gates = synth.decays((wt.B, wt.H, wt.N), wt.seed + 5, 0.85, 1.0, device="cuda")
+    O = torch.empty_like(x["V"])
+    f = lambda: la.la_forward_retention(x["Q"], x["K"], x["V"], gates=gates, out=O)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 10, stream)
+    res["retention_gated_bf16/fwd"] = entry(
+        ms, _bytes_fwd(wt.B, wt.H, wt.N, wt.D, wt.M, 2) + wt.B * wt.H * wt.N * 4, wt.B * wt.N)
+    del x, O, gates
+    Sr = torch.randn(B, H, D, M, device="cuda")
+    sq = synth.decode_step_qkv(B, H, D, M, w.dtype, w.seed, 0, device="cuda")
+    gate = synth.decays((B, H), w.seed + 6, 0.85, 1.0, device="cuda")
+    out = torch.empty(B, H, M, device="cuda")
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, device="cuda")
+    f = lambda: la.la_retention_decode_step(sq["q"], sq["k"], sq["v"], Sr, gate=gate, out=out)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 50, stream, flush=lambda: flush_buf.fill_(1.0))
+    res["retention_gated_bf16/decode_step"] = entry(
+        ms, B * H * (2 * D * M * 4 + (2 * D + M) * 2 + 4 + M * 4), B, {"l2": "flushed before each step"})
+    del Sr, sq, gate, out, flush_buf
+
+    # the degree-2 polynomial feature map (C = D^2 = 1024 features), causal, bf16:
+    # ALU-bound, measured against the fp32 FMA rate (2 flops per FMA)
+    Bp, Hp, Np, Dp, Mp = 4, 16, 4096, 32, 64
+    x = synth.qkv(Bp, Hp, Np, Dp, Mp, "bf16", 1007, device="cuda")
+    O = torch.empty_like(x["V"])
+    f = lambda: la.la_forward_poly2(x["Q"], x["K"], x["V"], causal=True, out=O)
+    for _ in range(3):
+        f()
+    ms = _time_events(torch, f, 10, stream)
+    flops = Bp * Hp * Np * 4 * Dp * Dp * (Mp + 1)  # phi(Q) [S | Z] and phi(K)^T [V | 1] per token
+    fma_peak = _fp32_fma_tflops(torch)
+    d = entry(ms, _bytes_fwd(Bp, Hp, Np, Dp, Mp, 2), Bp * Np)
+    d.update({"bound": "alu", "algorithmic_tflops": round(flops / (ms / 1e3) / 1e12, 2),
+              "alu_peak_tflops": round(fma_peak, 1),
+              "alu_frac": round(flops / (ms / 1e3) / 1e12 / fma_peak, 4),
+              "workload": f"B={Bp} H={Hp} N={Np} D={Dp} M={Mp} bf16, causal"})
+    res["poly2_causal_bf16/fwd"] = d
+    del x, O
 
     # the prefill that hands the decode its state: the causal forward over every sequence's
     # prompt, emitting the final S, Z of each head (inputs larger than L2)

@@ -158,6 +158,20 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
                          float* out, int B, int H, int D, int M, la_dtype dtype, void* stream);
 
 /*
+ * Attention with the degree-2 polynomial similarity sim(q, k) = (q^T k)^2 in
+ * its linear form ("【论文解读】Transformers are RNNs", section 二 (3): the
+ * explicit feature map phi(x) = (x_a x_b), C = D^2 features, cost O(N D^2 M)):
+ *     V'_i = phi(Q_i)^T S / phi(Q_i)^T Z,  S = sum_j phi(K_j) V_j^T,  Z = sum_j phi(K_j)
+ * over j <= i when causal != 0 (section 三), else over all j.  Raw Q and K
+ * (no elu).  Q, K [B][H][N][D]; V [B][H][N][M] dtype (read); Out [B][H][N][M]
+ * dtype (written).  Built for D = 32 and M in {32, 64} (LA_ERR_UNSUPPORTED
+ * otherwise).  A row whose query is orthogonal to every key it sees has a zero
+ * denominator and no defined output.
+ */
+la_status la_forward_poly2(const void* Q, const void* K, const void* V, void* Out, int B, int H,
+                           int N, int D, int M, la_dtype dtype, int causal, void* stream);
+
+/*
  * Linear attention with decay ("retention"), as "Transformer and Variants"
  * (by-xin.github.io) writes it: section 1.3.2 (linear attention as an RNN
  * without the reflection term, no softmax and no normaliser) and section
@@ -249,7 +263,8 @@ la_status la_forward_noncausal_noalloc(const void* Q, const void* K, const void*
  *   op       the entry point's name: "la_forward_causal", "la_backward_causal",
  *            "la_forward_noncausal", "la_backward_noncausal", "la_decode_step" (0),
  *            "la_softmax_decode_step" (N = the cache position T),
- *            "la_forward_retention", "la_retention_decode_step" (0) or
+ *            "la_forward_retention", "la_retention_decode_step" (0),
+ *            "la_forward_poly2" or
  *            "la_forward_noncausal_noalloc" (0: it uses its fixed array)
  *   B..M, dtype  the call's sizes and dtype (N is ignored for decode)
  *   saved    for "la_backward_causal": an OR of LA_SAVED_OUT, LA_SAVED_DEN and

@@ -253,6 +253,23 @@ LA_SAVED_OUT, LA_SAVED_DEN, LA_SAVED_CKPT = (_native.LA_SAVED_OUT, _native.LA_SA
                                              _native.LA_SAVED_CKPT)
 
 
+def la_forward_poly2(Q, K, V, causal=True, out=None, stream=None):
+    """Attention with similarity (Q_i . K_j)^2 through its degree-2 feature map (D = 32)."""
+    B, H, N, D, M = _dims(Q, V)
+    dev = Q.device
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, Q.dtype, dev)
+    if K.shape != Q.shape:
+        raise ValueError("K must have the shape of Q")
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=Q.dtype, device=dev)
+    _need(out, "out", Q.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(_lib.la_forward_poly2(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, N, D, M, _dtype(Q),
+                                     1 if causal else 0, _stream_handle(stream)))
+    return out
+
+
 def _decay_args(gamma_head, gates, shape, dev, name):
     if gamma_head is not None and gates is not None:
         raise ValueError(f"give gamma_head or {name}, not both")

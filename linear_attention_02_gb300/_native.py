@@ -28,6 +28,7 @@ SIGNATURES = {
     "la_decode_step": [_P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _P],
     "la_workspace_bytes": [ctypes.c_char_p, _I, _I, _I, _I, _I, _I, ctypes.c_uint, _I],
     "la_scratch_peak_bytes": [_I],
+    "la_forward_poly2": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
     "la_forward_retention": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _P],
     "la_retention_decode_step": [_P, _P, _P, _F, _F, _F, _F, _I, _I, _I, _I, _I, _P],
     "la_softmax_decode_step": [_P, _P, _P, _P, _P, _I, _I, _F, _I, _I, _I, _I, _I, _P],

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "liblinattn.so")
 
-SOURCES = ["la_api.cu", "ffma_f32.cu", "ffma_bf16.cu", "ncbwd_ffma.cu", "ret_ffma.cu", "decode.cu", "softmax_decode.cu", "noalloc.cu",
+SOURCES = ["la_api.cu", "ffma_f32.cu", "ffma_bf16.cu", "ncbwd_ffma.cu", "ret_ffma.cu", "poly_ffma.cu", "decode.cu", "softmax_decode.cu", "noalloc.cu",
            "causal_tc.cu", "causal_bwd_tc.cu", "noncausal_tc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -279,6 +279,8 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
         return plan::ffma_noncausal_forward(BH, N, D, M, sms);
     }
     if (!strcmp(op, "la_backward_noncausal")) return plan::ffma_noncausal_backward(BH, N, D, M, sms);
+    if (!strcmp(op, "la_forward_poly2"))
+        return D == 32 && (M == 32 || M == 64) ? plan::poly2_scratch(BH, N, M, sms) : SIZE_MAX;
     if (!strcmp(op, "la_forward_retention")) return plan::ffma_retention_forward(BH, N, D, M, sms);
     if (!strcmp(op, "la_retention_decode_step")) return 0;
     if (!strcmp(op, "la_softmax_decode_step"))  // N is the cache position T: T + 1 positions
@@ -485,6 +487,36 @@ la_status la_retention_decode_step(const void* q, const void* k, const void* v,
     return finish(dispatch<RetentionStep>(dtype, D, M, &ctx, q, k, v, gamma_head, gate, S, out,
                                           (int)((size_t)B * H), H),
                   fn);
+}
+
+la_status la_forward_poly2(const void* Q, const void* K, const void* V, void* Out, int B, int H,
+                           int N, int D, int M, la_dtype dtype, int causal, void* stream) {
+    static const char* fn = "la_forward_poly2";
+    const void* p[] = {Q, K, V, Out};
+    const char* nm[] = {"Q", "K", "V", "Out"};
+    bool empty = false;
+    la_status s = check_common(fn, B, H, N, D, M, dtype, p, nm, 4, &empty);
+    if (s != LA_OK) return s;
+    if (D != 32 || (M != 32 && M != 64))
+        return fail(LA_ERR_UNSUPPORTED, "%s: D=%d M=%d, the degree-2 feature map is built for D = 32, "
+                    "M in {32, 64}", fn, D, M);
+    if (empty) return LA_OK;
+    LaunchCtx ctx;
+    if ((s = get_ctx((cudaStream_t)stream, &ctx)) != LA_OK) return s;
+    const int BH = B * H;
+    const bool c = causal != 0;
+    cudaError_t e;
+    if (dtype == LA_DTYPE_F32)
+        e = M == 32 ? poly2_forward<float, 32>(ctx, (const float*)Q, (const float*)K, (const float*)V,
+                                               (float*)Out, BH, N, c)
+                    : poly2_forward<float, 64>(ctx, (const float*)Q, (const float*)K, (const float*)V,
+                                               (float*)Out, BH, N, c);
+    else
+        e = M == 32 ? poly2_forward<__nv_bfloat16, 32>(ctx, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
+                                                       (const __nv_bfloat16*)V, (__nv_bfloat16*)Out, BH, N, c)
+                    : poly2_forward<__nv_bfloat16, 64>(ctx, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
+                                                       (const __nv_bfloat16*)V, (__nv_bfloat16*)Out, BH, N, c);
+    return finish(e, fn);
 }
 
 la_status la_softmax_decode_step(const void* q, const void* k, const void* v, void* K_cache,

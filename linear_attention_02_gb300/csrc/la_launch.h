@@ -98,6 +98,12 @@ cudaError_t retention_step(const LaunchCtx& c, const T* q, const T* k, const T* 
                            const float* gamma_head, const float* gate, float* S, float* out, int BH,
                            int H);
 
+// Attention with the degree-2 polynomial similarity (q . k)^2 through its
+// explicit feature map, D = 32, causal or over all tokens.
+template <typename T, int M>
+cudaError_t poly2_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O, int BH,
+                          int N, bool causal);
+
 template <typename T, int D, int M>
 cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
                         float* Z, float* out, int BH);

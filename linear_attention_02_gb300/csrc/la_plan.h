@@ -86,6 +86,29 @@ inline size_t ffma_retention_forward(int BH, int N, int D, int M, int num_sms) {
                      : 0;
 }
 
+// Degree-2 polynomial feature map (D = 32): the D (D + 1) / 2 = 528 features
+// split into kPolySlices slices; a grid of heads x spans x slices of about two
+// waves of one CTA per SM.
+constexpr int kPolySlices = 3;
+constexpr int kPolyFeatures = 32 * 33 / 2;
+constexpr int kPolyChunk = 64;
+inline void poly_spans(int BH, int N, int num_sms, int* spans, int* span_len) {
+    const int chunks = (N + kPolyChunk - 1) / kPolyChunk;
+    int s = (2 * num_sms + kPolySlices * std::max(BH, 1) - 1) / (kPolySlices * std::max(BH, 1));
+    s = std::max(1, std::min(s, std::max(chunks, 1)));
+    const int per = (chunks + s - 1) / s;
+    *span_len = std::max(per, 1) * kPolyChunk;
+    *spans = std::max(1, (N + *span_len - 1) / *span_len);
+}
+// The span aggregates of every slice ([BH][spans][features][M + 1]) and the
+// fp32 numerator and denominator accumulator [BH][N][M + 1].
+inline size_t poly2_scratch(int BH, int N, int M, int num_sms) {
+    int spans = 1, len = 1;
+    poly_spans(BH, N, num_sms, &spans, &len);
+    const size_t agg = sizeof(float) * static_cast<size_t>(BH) * spans * kPolyFeatures * (M + 1);
+    return up256(agg) + sizeof(float) * static_cast<size_t>(BH) * N * (M + 1);
+}
+
 // Tensor-core causal kernels: the chunks of all heads cut into equal ranges,
 // one per resident CTA (see tc_common.cuh, split_chunks).
 inline int tc_units(int BH, int chunks_per_head, int slots) {
