@@ -31,6 +31,19 @@
 // head boundary.  Units are taken from an atomic ticket after TMEM is
 // allocated, so a CTA only ever waits for CTAs that started (and hold their
 // TMEM) before it.
+//
+// The same kernel, instantiated with RET, runs linear attention with decay
+// ("retention", "Transformer and Variants" sections 1.3.2 and 1.3.4):
+// S_t = gamma_t S_{t-1} + k_t v_t^T, y_t = S_t^T q_t, raw q and k, no
+// normaliser.  With a_i the running sum of log2(gamma) over the chunk's tokens
+// 0 .. i and A = a_127:
+//   y_c   = (tril(Q_c K_c^T) * 2^(a_i - a_j)) V_c + diag(2^a) Q_c S_{c-1}
+//   S_c   = 2^A S_{c-1} + (diag(2^(A - a)) K_c)^T V_c
+// so P is scaled as it is masked, the Q and K tiles are scaled by rows after
+// P is taken, and the fp32 state in TMEM is scaled before the update; every
+// power of two has a non-positive exponent.  A published piece carries its
+// total log2 decay, and the look-back decays each earlier aggregate by the
+// pieces after it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,7 +58,7 @@
 namespace la {
 namespace tcf {
 
-template <int D, int M>
+template <int D, int M, bool RET = false>
 struct Layout {
     static constexpr int DA = D / 64;  // atom columns of a phi(Q)/phi(K) tile
     static constexpr int MA = M / 64;  // atom columns of a V / output tile
@@ -71,7 +84,8 @@ struct Layout {
     static constexpr uint32_t KV2_V = D == 64 ? S : S + DA * kAtom;
     static constexpr uint32_t BARS = S + (MA + 1) * S_ATOM > KV2_V + MA * kAtom ? S + (MA + 1) * S_ATOM
                                                                                  : KV2_V + MA * kAtom;
-    static constexpr uint32_t BYTES = BARS + 64;
+    static constexpr uint32_t DEC = BARS + 64;  // retention: a_i of the chunk (128 floats), warp sums
+    static constexpr uint32_t BYTES = BARS + 64 + (RET ? 528 : 0);
     // tensor memory columns: P (fp32, then masked and packed in place to bf16 pairs, the A
     // operand of P [V | 1]: columns 0 .. 63 for one warpgroup, 0 .. 31 and 64 .. 95 for two),
     // O_ext after the packed P, S_ext after O_ext
@@ -105,14 +119,62 @@ struct FwdParams {
     float* den;            // [BH][N] or null: the normaliser of every token
     float* ckpt;           // [BH][ckpt_slots(CH)][W] or null: states before every 8th chunk
     unsigned* status;      // device error word
+    // retention only
+    const float* gates;       // [BH][N] per-token decays, or null
+    const float* gamma_head;  // [H] per-head decays, or null (neither: decay 1)
+    int H;                    // heads per batch entry
+    float* lam;               // [units] total log2 decay of each published piece
 };
 
-template <int D, int M>
-__global__ void __launch_bounds__(Layout<D, M>::THREADS, Layout<D, M>::PER_SM)
+// log2 of a decay, kept finite: a decay below 2^-64 counts as 2^-64.
+__device__ __forceinline__ float log2_decay(float g) { return fmaxf(log2f(g), -64.f); }
+
+// dec[i] = sum of log2(decay) over tokens c0 .. c0 + i of head h (rows past the
+// head's end add nothing).  Threads 0 .. 127 scan; every thread of the CTA
+// calls it, and it ends with the scan complete for all of them.
+__device__ __forceinline__ void decay_scan(float* dec, const FwdParams& p, int h, int c0, int valid) {
+    const int t = threadIdx.x;
+    float* wsum = dec + L;
+    float l = 0.f;
+    if (t < L) {
+        if (t < valid)
+            l = log2_decay(p.gates ? p.gates[static_cast<size_t>(h) * p.N + c0 + t]
+                                   : (p.gamma_head ? p.gamma_head[h % p.H] : 1.f));
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float x = __shfl_up_sync(0xffffffffu, l, o);
+            if ((t & 31) >= o) l += x;
+        }
+        if ((t & 31) == 31) wsum[t >> 5] = l;
+    }
+    __syncthreads();
+    if (t < L) {
+        for (int w = 0; w < (t >> 5); ++w) l += wsum[w];
+        dec[t] = l;
+    }
+    __syncthreads();
+}
+
+// Row `row` of a K-major 128-row bf16 tile, atom `a`, times f (rounded to bf16).
+__device__ __forceinline__ void scale_row_atom(uint8_t* tile, int a, int row, float f) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4* q = reinterpret_cast<uint4*>(tile + a * kAtom + swz(row, c));
+        uint4 u = *q;
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = pack_bf16(__uint_as_float(w[k] << 16) * f, __uint_as_float(w[k] & 0xFFFF0000u) * f);
+        *q = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <int D, int M, bool RET>
+__global__ void __launch_bounds__(Layout<D, M, RET>::THREADS, Layout<D, M, RET>::PER_SM)
 causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                      const FwdParams p) {
-    using Lay = Layout<D, M>;
+    using Lay = Layout<D, M, RET>;
     constexpr int DA = Lay::DA, MA = Lay::MA, NE = Lay::NE, W = Lay::W, NT = Lay::THREADS;
     constexpr int HALF = M / Lay::GROUPS;   // columns of a state/output row per warpgroup
     constexpr int PCOLS = L / Lay::GROUPS;  // columns of P per warpgroup
@@ -123,6 +185,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     constexpr uint32_t ID_O = idesc_bf16(128, NE, false, true);
 
     extern __shared__ __align__(1024) uint8_t sm[];
+    float* const dec = reinterpret_cast<float*>(sm + Lay::DEC);  // retention: the chunk's a_i
     const int t = threadIdx.x, warp = t >> 5;
     const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup
     const int row = 32 * q + (t & 31);      // tile row / TMEM lane owned by this thread
@@ -204,19 +267,42 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int d = row;
         for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 16) {
             float v[16];
+            if constexpr (RET) {  // each aggregate decayed by the pieces after it, then S_init
+                float f = 1.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                v[i] = p.S_init ? p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i] : 0.f;
-            for (int sp = sp0; sp < sp1; ++sp) {
-                const float4* a =
-                    reinterpret_cast<const float4*>(p.agg + static_cast<size_t>(sp) * W + d * M + j0);
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                for (int sp = sp1 - 1; sp >= sp0; --sp) {
+                    const float4* a =
+                        reinterpret_cast<const float4*>(p.agg + static_cast<size_t>(sp) * W + d * M + j0);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 x = __ldcg(a + u);
-                    v[4 * u] += x.x;
-                    v[4 * u + 1] += x.y;
-                    v[4 * u + 2] += x.z;
-                    v[4 * u + 3] += x.w;
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 x = __ldcg(a + u);
+                        v[4 * u] = fmaf(f, x.x, v[4 * u]);
+                        v[4 * u + 1] = fmaf(f, x.y, v[4 * u + 1]);
+                        v[4 * u + 2] = fmaf(f, x.z, v[4 * u + 2]);
+                        v[4 * u + 3] = fmaf(f, x.w, v[4 * u + 3]);
+                    }
+                    f *= exp2f(__ldcg(p.lam + sp));
+                }
+                if (p.S_init)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[i] = fmaf(f, p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i], v[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = p.S_init ? p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i] : 0.f;
+                for (int sp = sp0; sp < sp1; ++sp) {
+                    const float4* a =
+                        reinterpret_cast<const float4*>(p.agg + static_cast<size_t>(sp) * W + d * M + j0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 x = __ldcg(a + u);
+                        v[4 * u] += x.x;
+                        v[4 * u + 1] += x.y;
+                        v[4 * u + 2] += x.z;
+                        v[4 * u + 3] += x.w;
+                    }
                 }
             }
             tmem_st16(tm + lane + Lay::T_S + j0, v);
@@ -271,6 +357,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int c_last = (ur.end - 1 - h * p.CH) * L;  // the first chunk summed
         if (t == 0)
             for (int b = 0; b < KV_BUFS - 1 && b < n1; ++b) load_kv(c_last - b * L, b);
+        float run = 0.f;  // retention: log2 decay of the piece's chunks already summed (the later ones)
         for (int i1 = 0; i1 < n1; ++i1) {
             const int c0 = c_last - i1 * L;
             const int b = i1 % KV_BUFS;
@@ -288,7 +375,15 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             if (t == 0 && i1 + KV_BUFS - 1 < n1)
                 load_kv(c0 - (KV_BUFS - 1) * L, (i1 + KV_BUFS - 1) % KV_BUFS);
-            phi_tile<true, NT>(sm + k_buf(b), DA, min(L, p.N - c0));
+            if constexpr (RET) {  // K rows decayed to the end of the piece
+                decay_scan(dec, p, h, c0, min(L, p.N - c0));
+                const float A = dec[L - 1];
+                const float f = exp2f(run + A - dec[row]);
+                for (int a = g; a < DA; a += Lay::GROUPS) scale_row_atom(sm + k_buf(b), a, row, f);
+                run += A;
+            } else {
+                phi_tile<true, NT>(sm + k_buf(b), DA, min(L, p.N - c0));
+            }
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
@@ -325,6 +420,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 out[D * M + d] = z[0];
             }
         }
+        if (RET && t == 0) p.lam[unit] = run;
         __threadfence();
         fence_before_sync();
         __syncthreads();
@@ -362,8 +458,12 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const int valid = min(L, p.N - c0);
         if (t == 0 && !mbar_wait(tma_bar, (got0++) & 1u, kWaitLimit)) fail(kErrWait);
         __syncthreads();
-        phi_tile<false, NT>(sm + Lay::Q, DA, valid);
-        phi_tile<true, NT>(sm + Lay::K, DA, valid);
+        if constexpr (RET) {
+            decay_scan(dec, p, h, c0, valid);
+        } else {
+            phi_tile<false, NT>(sm + Lay::Q, DA, valid);
+            phi_tile<true, NT>(sm + Lay::K, DA, valid);
+        }
         fence_proxy_async();
         fence_before_sync();
         __syncthreads();
@@ -377,7 +477,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                          k > 0 ? 1u : 0u);
             }
             mma_commit(mma_bar);
-            mma_state_update(sK, sV, true);  // under the P epilogue; tracked by the next commit
+            if (!RET) mma_state_update(sK, sV, true);  // under the P epilogue; tracked by the next commit
             tma_store_wait_read();           // the staging tile (P area) is free again
         }
         wait_bar(mma_bar, mma_phase);
@@ -394,19 +494,48 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 } else {
                     float v[64];
                     tmem_ld64(tm + lane + Lay::T_P + j0, v);
+                    if constexpr (RET) {  // decay 2^(a_i - a_j) of key j seen from query i
+                        const float ai = dec[row];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int j = j0 + 2 * u;
-                        pk[u] = pack_bf16(j <= row ? v[2 * u] : 0.f, j + 1 <= row ? v[2 * u + 1] : 0.f);
+                        for (int u = 0; u < 32; ++u) {
+                            const int j = j0 + 2 * u;
+                            pk[u] = pack_bf16(j <= row ? v[2 * u] * exp2f(ai - dec[j]) : 0.f,
+                                              j + 1 <= row ? v[2 * u + 1] * exp2f(ai - dec[j + 1]) : 0.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            const int j = j0 + 2 * u;
+                            pk[u] = pack_bf16(j <= row ? v[2 * u] : 0.f, j + 1 <= row ? v[2 * u + 1] : 0.f);
+                        }
                     }
                 }
                 tmem_st32u(tm + lane + Lay::T_P + g * PCOLS + 32 * jb, pk);
+            }
+        }
+        if constexpr (RET) {  // P is taken: Q rows by 2^(a_i), K rows by 2^(A - a_j), the state by 2^A
+            const float A = dec[L - 1], ai = dec[row];
+            for (int a = g; a < DA; a += Lay::GROUPS) {
+                scale_row_atom(sm + Lay::Q, a, row, exp2f(ai));
+                scale_row_atom(sm + Lay::K, a, row, exp2f(A - ai));
+            }
+            if (q < D / 32) {
+                const float f = exp2f(A);
+                for (int j0 = g * HALF; j0 < (g + 1) * HALF + (g == 0 ? 16 : 0); j0 += 16) {
+                    const int col = j0 < (g + 1) * HALF ? j0 : M;  // then the normaliser block
+                    float v[16];
+                    tmem_ld16(tm + lane + Lay::T_S + col, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] *= f;
+                    tmem_st16(tm + lane + Lay::T_S + col, v);
+                }
             }
         }
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
         if (t == 0) {
+            if (RET) mma_state_update(sK, sV, true);  // with the decayed K rows
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)  // O_ext = phi(Q) [S | Z]
                 mma_bf16(tm + Lay::T_O, sdesc(sQ + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
@@ -436,7 +565,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                             reinterpret_cast<float4*>(so + j0)[u] =
                                 make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
                     }
-                    if (g == 0) {
+                    if (g == 0 && p.Z_final) {
                         float z[16];
                         tmem_ld16(tm + lane + Lay::T_S + M, z);
                         p.Z_final[static_cast<size_t>(h) * D + d] = z[0];
@@ -478,7 +607,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         {   // V' = O_ext[:, :M] / O_ext[:, M] -> bf16 staging tile (P area)
             float dv[16];
             tmem_ld16(tm + lane + Lay::T_O + M, dv);
-            const float inv = 1.f / dv[0];
+            const float inv = RET ? 1.f : 1.f / dv[0];  // retention has no normaliser
             if (p.den && g == 0 && row < valid) p.den[static_cast<size_t>(h) * p.N + c0 + row] = dv[0];
             for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                 float v[32];
@@ -521,15 +650,24 @@ size_t causal_forward_tc_scratch(int D, int BH, int N, int num_sms) {
     return sizeof(float) * units * plan::state_words(D, D) + sizeof(unsigned) * (units + 1) + 256;
 }
 
-template <int D, int M>
-cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                              const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
-                              const float* S_init, const float* Z_init, float* S_final,
-                              float* Z_final, float* Den, float* Ckpt) {
+size_t retention_forward_tc_scratch(int D, int BH, int N, int num_sms) {
     using namespace tcf;
-    using Lay = Layout<D, M>;
+    const int per_sm = D == 64 ? Layout<64, 64, true>::PER_SM : Layout<128, 128, true>::PER_SM;
     const int chunks = (N + L - 1) / L;
-    auto kern = causal_fwd_tc_kernel<D, M>;
+    const size_t units = static_cast<size_t>(plan::tc_units(BH, chunks, per_sm * num_sms));
+    // the causal forward's aggregates and flags, plus one total log2 decay per unit
+    return sizeof(float) * units * (plan::state_words(D, D) + 1) + sizeof(unsigned) * (units + 1) + 256;
+}
+
+namespace tcf {
+
+// Launches the forward kernel (RET: retention) with the split and scratch of `p`'s sizes.
+template <int D, int M, bool RET>
+cudaError_t launch_forward(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                           const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N, FwdParams p) {
+    using Lay = Layout<D, M, RET>;
+    const int chunks = (N + L - 1) / L;
+    auto kern = causal_fwd_tc_kernel<D, M, RET>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Lay::BYTES));
     if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
@@ -550,10 +688,11 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
 
     const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * Lay::W;
     const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
+    const size_t bytes = RET ? retention_forward_tc_scratch(D, BH, N, c.num_sms)
+                             : causal_forward_tc_scratch(D, BH, N, c.num_sms);
     char* ws = nullptr;
-    e = scratch_alloc(c, reinterpret_cast<void**>(&ws), causal_forward_tc_scratch(D, BH, N, c.num_sms));
+    e = scratch_alloc(c, reinterpret_cast<void**>(&ws), bytes);
     if (e != cudaSuccess) return e;
-    FwdParams p;
     p.N = N;
     p.BH = BH;
     p.CH = chunks;
@@ -561,12 +700,7 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     p.agg = reinterpret_cast<float*>(ws);
     p.flags = reinterpret_cast<unsigned*>(ws + agg_bytes);
     p.ticket = p.flags + units;
-    p.S_init = S_init;
-    p.Z_init = Z_init;
-    p.S_final = S_final;
-    p.Z_final = Z_final;
-    p.den = Den;
-    p.ckpt = Ckpt;
+    p.lam = RET ? reinterpret_cast<float*>(ws + agg_bytes + flag_bytes) : nullptr;
     p.status = c.status_word;
     do {
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
@@ -582,6 +716,45 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
     return e;
 }
 
+}  // namespace tcf
+
+template <int D, int M>
+cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                              const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N,
+                              const float* S_init, const float* Z_init, float* S_final,
+                              float* Z_final, float* Den, float* Ckpt) {
+    tcf::FwdParams p{};
+    p.S_init = S_init;
+    p.Z_init = Z_init;
+    p.S_final = S_final;
+    p.Z_final = Z_final;
+    p.den = Den;
+    p.ckpt = Ckpt;
+    return tcf::launch_forward<D, M, false>(c, Q, K, V, O, BH, N, p);
+}
+
+template <int D, int M>
+cudaError_t retention_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                 const __nv_bfloat16* V, __nv_bfloat16* O, const float* gamma_head,
+                                 const float* gates, int BH, int H, int N, const float* S_init,
+                                 float* S_final) {
+    tcf::FwdParams p{};
+    p.S_init = S_init;
+    p.S_final = S_final;
+    p.gates = gates;
+    p.gamma_head = gamma_head;
+    p.H = H;
+    return tcf::launch_forward<D, M, true>(c, Q, K, V, O, BH, N, p);
+}
+
+template cudaError_t retention_forward_tc<64, 64>(const LaunchCtx&, const __nv_bfloat16*,
+                                                  const __nv_bfloat16*, const __nv_bfloat16*,
+                                                  __nv_bfloat16*, const float*, const float*, int,
+                                                  int, int, const float*, float*);
+template cudaError_t retention_forward_tc<128, 128>(const LaunchCtx&, const __nv_bfloat16*,
+                                                    const __nv_bfloat16*, const __nv_bfloat16*,
+                                                    __nv_bfloat16*, const float*, const float*, int,
+                                                    int, int, const float*, float*);
 template cudaError_t causal_forward_tc<64, 64>(const LaunchCtx&, const __nv_bfloat16*,
                                                const __nv_bfloat16*, const __nv_bfloat16*,
                                                __nv_bfloat16*, int, int, const float*, const float*,

@@ -211,8 +211,12 @@ struct FwdRetention {
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V, void* O,
                            const float* gh, const float* gt, int BH, int H, int N, const float* Si,
                            float* Sf) {
-        return retention_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, gh, gt,
-                                          BH, H, N, Si, Sf);
+        if constexpr (UseTensorCores<T, D, M>::value)
+            return retention_forward_tc<D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, gh,
+                                              gt, BH, H, N, Si, Sf);
+        else
+            return retention_forward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (T*)O, gh,
+                                              gt, BH, H, N, Si, Sf);
     }
 };
 struct RetentionStep {
@@ -281,7 +285,9 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
     if (!strcmp(op, "la_backward_noncausal")) return plan::ffma_noncausal_backward(BH, N, D, M, sms);
     if (!strcmp(op, "la_forward_poly2"))
         return D == 32 && (M == 32 || M == 64) ? plan::poly2_scratch(BH, N, M, sms) : SIZE_MAX;
-    if (!strcmp(op, "la_forward_retention")) return plan::ffma_retention_forward(BH, N, D, M, sms);
+    if (!strcmp(op, "la_forward_retention"))
+        return bf16 && D == M && (D == 64 || D == 128) ? retention_forward_tc_scratch(D, BH, N, sms)
+                                                       : plan::ffma_retention_forward(BH, N, D, M, sms);
     if (!strcmp(op, "la_retention_decode_step")) return 0;
     if (!strcmp(op, "la_softmax_decode_step"))  // N is the cache position T: T + 1 positions
         return D == M ? plan::softmax_decode_scratch(BH, N + 1, D, sms) : SIZE_MAX;

@@ -54,6 +54,14 @@ cudaError_t causal_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const 
                               const float* S_init, const float* Z_init, float* S_final,
                               float* Z_final, float* Den, float* Ckpt);
 
+// Tensor-core retention forward (decay, no normaliser) for bf16 storage with D = M in {64, 128}.
+template <int D, int M>
+cudaError_t retention_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                 const __nv_bfloat16* V, __nv_bfloat16* O, const float* gamma_head,
+                                 const float* gates, int BH, int H, int N, const float* S_init,
+                                 float* S_final);
+size_t retention_forward_tc_scratch(int D, int BH, int N, int num_sms);
+
 // Tensor-core causal backward for bf16 storage with D = M = 64; Den (the
 // forward's normaliser per token) and Ckpt (its state checkpoints) may be null.
 cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,

@@ -116,3 +116,31 @@ def test_retention_rejects_both_decays():
     with pytest.raises(ValueError):
         la.la_forward_retention(x, x, x, gamma_head=torch.ones(2, device="cuda"),
                                 gates=torch.ones(1, 2, 8, device="cuda"))
+
+
+# bf16 with D = M in {64, 128} runs the tensor-core kernel: the chunks of all heads cut
+# into equal ranges, so a range can hold the tail of one head and the start of
+# another, or stop inside a head (its aggregate then carries the piece's total decay)
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(8, 40, 300, 64, 64), (1, 2, 5000, 128, 128), (2, 3, 8300, 64, 64),
+                                   (1, 1, 128, 64, 64), (2, 3, 129, 64, 64)])
+def test_retention_tensor_core_ranges(kind, shape):
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=126 + N)
+    kw = _decay_kw(kind, B, H, N, seed=127)
+    S0 = torch.randn(B, H, D, M) * 0.1
+    O, S = la.la_forward_retention(x["Q"].cuda(), x["K"].cuda(), x["V"].cuda(),
+                                   **{k: v.cuda() for k, v in kw.items()}, S_init=S0.cuda(),
+                                   return_state=True)
+    la.la_check_device_status()
+    idx = list(range(min(B * H, 6)))
+    hs = [x[n].reshape(B * H, N, -1)[idx][None] for n in ("Q", "K", "V")]
+    okw = {}
+    if kind == "retnet":
+        okw["gamma_head"] = kw["gamma_head"].repeat(B)[idx]
+    elif kind == "gated":
+        okw["gates"] = kw["gates"].reshape(B * H, N)[idx][None]
+    Ro, Rs = oracle.retention_forward_recurrent(*hs, S0=S0.reshape(B * H, D, M)[idx][None], **okw)
+    assert rel_err(O.reshape(B * H, N, M)[idx], Ro[0]) <= TOL["bf16"]
+    assert rel_err(S.reshape(B * H, D, M)[idx], Rs[0]) <= TOL["bf16"]
