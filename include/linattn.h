@@ -290,6 +290,21 @@ size_t la_workspace_bytes(const char* op, int B, int H, int N, int D, int M, la_
  */
 size_t la_scratch_peak_bytes(int reset);
 
+/*
+ * Test hook for the failure path of the real kernels, off unless called: the
+ * next library call on this process that launches the tensor-core causal
+ * forward or backward has unit `unit` of its work split skip its look-back
+ * publication (the flag that later units of the same head wait for), and
+ * gives every look-back wait of that launch `spin_limit` polls (about 0.3 us
+ * each) instead of the default.  The units waiting on the missing flag give
+ * up, set the look-back bit (0x2) in the device error word, drain their copies
+ * in flight, free their tensor memory and end, so the call returns without a
+ * hang; its outputs are then undefined, and la_check_device_status reports
+ * LA_ERR_TIMEOUT.  The setting is consumed by that one call.  LA_ERR_INVALID_ARG
+ * for unit < 0 or spin_limit == 0.
+ */
+la_status la_debug_withhold_publication(int unit, unsigned spin_limit);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word set by bounded device-side waits.  LA_ERR_TIMEOUT if one gave up since
  * the last check, LA_ERR_CUDA if the stream reported an error, else LA_OK. */

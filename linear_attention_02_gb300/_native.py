@@ -32,6 +32,7 @@ SIGNATURES = {
     "la_forward_retention": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _P],
     "la_retention_decode_step": [_P, _P, _P, _F, _F, _F, _F, _I, _I, _I, _I, _I, _P],
     "la_softmax_decode_step": [_P, _P, _P, _P, _P, _I, _I, _F, _I, _I, _I, _I, _I, _P],
+    "la_debug_withhold_publication": [_I, ctypes.c_uint],
     "la_check_device_status": [_P],
     "la_selftest_expired_waits": [_P],
     "la_status_string": [_I],

@@ -111,6 +111,8 @@ struct BwdParams {
                           // kernel, when den is null
     const float* ckpt;    // the forward's state checkpoints (see kCkptChunks), or null
     unsigned* status;
+    int withhold;         // test hook: a unit that does not publish its aggregate (-1: none)
+    unsigned spin_limit;  // flag polls before a look-back gives up
 };
 
 constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);     // K-major x K-major
@@ -626,14 +628,14 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             __threadfence();
             fence_before_sync();
             bar_sync(kBarE, kBT);
-            if (t == 0) st_release(p.flags + unit, 1u);
+            if (t == 0 && unit != p.withhold) st_release(p.flags + unit, 1u);
         }
         bool bad = false;
         if (t == 0 && ur.look) {
             for (int sp = ur.u_first; sp < unit && !bad; ++sp) {
                 uint32_t n = 0;
                 while (ld_acquire(p.flags + sp) == 0u) {
-                    if (++n > kSpinLimit) {
+                    if (++n > p.spin_limit) {
                         atomicOr(p.status, kErrLookback);
                         bad = true;
                         break;
@@ -1174,6 +1176,8 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     p.den = Den;
     p.den_out = nullptr;
     p.ckpt = Ckpt;
+    p.withhold = c.withhold_unit;
+    p.spin_limit = c.spin_limit ? c.spin_limit : kSpinLimit;
     p.status = c.status_word;
     do {
         if (!O) {  // the output is needed for gd: recompute it

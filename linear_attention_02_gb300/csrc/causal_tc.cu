@@ -124,6 +124,8 @@ struct FwdParams {
     const float* gamma_head;  // [H] per-head decays, or null (neither: decay 1)
     int H;                    // heads per batch entry
     float* lam;               // [units] total log2 decay of each published piece
+    int withhold;             // test hook: a unit that does not publish (-1: none)
+    unsigned spin_limit;      // flag polls before a look-back gives up
 };
 
 // log2 of a decay, kept finite: a decay below 2^-64 counts as 2^-64.
@@ -424,7 +426,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __threadfence();
         fence_before_sync();
         __syncthreads();
-        if (t == 0) st_release(p.flags + unit, 1u);
+        if (t == 0 && unit != p.withhold) st_release(p.flags + unit, 1u);
     }
 
     // phase 2's first copy goes out now, under the look-back (it touches no state tile or TMEM)
@@ -435,7 +437,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int sp = ur.u_first; sp < unit && !sh[1]; ++sp) {
             uint32_t n = 0;
             while (ld_acquire(p.flags + sp) == 0u) {
-                if (++n > kSpinLimit) {
+                if (++n > p.spin_limit) {
                     fail(kErrLookback);
                     break;
                 }
@@ -530,6 +532,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     tmem_st16(tm + lane + Lay::T_S + col, v);
                 }
             }
+            fence_proxy_async();  // the rescaled Q and K rows, for the products below
         }
         fence_before_sync();
         __syncthreads();
@@ -701,6 +704,8 @@ cudaError_t launch_forward(const LaunchCtx& c, const __nv_bfloat16* Q, const __n
     p.flags = reinterpret_cast<unsigned*>(ws + agg_bytes);
     p.ticket = p.flags + units;
     p.lam = RET ? reinterpret_cast<float*>(ws + agg_bytes + flag_bytes) : nullptr;
+    p.withhold = c.withhold_unit;
+    p.spin_limit = c.spin_limit ? c.spin_limit : kSpinLimit;
     p.status = c.status_word;
     do {
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;

@@ -22,6 +22,8 @@ namespace la {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_withhold_unit{-1};     // test hook, consumed by the next call
+std::atomic<unsigned> g_spin_limit{0};
 thread_local char g_msg[512] = "";
 
 la_status fail(la_status s, const char* fmt, ...) {
@@ -79,6 +81,8 @@ la_status get_ctx(cudaStream_t stream, LaunchCtx* ctx) {
         }
     }
     ctx->stream = stream;
+    ctx->withhold_unit = g_withhold_unit.exchange(-1);
+    ctx->spin_limit = g_spin_limit.exchange(0u);
     ctx->num_sms = d.num_sms;
     ctx->pool = d.pool;
     ctx->status_word = d.status_word;
@@ -564,6 +568,15 @@ la_status la_selftest_expired_waits(void* stream) {
     la_status s = get_ctx((cudaStream_t)stream, &ctx);
     if (s != LA_OK) return s;
     return finish(selftest_expired_waits(ctx), "la_selftest_expired_waits");
+}
+
+la_status la_debug_withhold_publication(int unit, unsigned spin_limit) {
+    if (unit < 0 || spin_limit == 0)
+        return fail(LA_ERR_INVALID_ARG, "la_debug_withhold_publication: unit %d, spin limit %u", unit,
+                    spin_limit);
+    g_spin_limit.store(spin_limit);
+    g_withhold_unit.store(unit);
+    return LA_OK;
 }
 
 la_status la_check_device_status(void* stream) {

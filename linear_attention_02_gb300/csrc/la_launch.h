@@ -14,6 +14,10 @@ struct LaunchCtx {
     int num_sms;
     cudaMemPool_t pool;          // library-owned pool for stream-ordered scratch
     unsigned int* status_word;   // device error word for bounded waits
+    // test hook (la_debug_withhold_publication): the unit whose look-back flag the next
+    // tensor-core causal launch leaves unset (-1: none), and its flag-poll limit (0: default)
+    int withhold_unit;
+    unsigned spin_limit;
 };
 
 // Counts one kernel launch (la_kernel_launch_count).
