@@ -20,14 +20,13 @@
 //     nearest state checkpoint plus a short aggregate pass, or, without
 //     checkpoints, from phase 1 / look-back as in the forward (later pieces
 //     start a head from zero); then per chunk: den (from the forward, or from
-//     P and qf.Z by MMA), gn, gd (gd written to scratch), [dP | dqf] by one MMA,
+//     P and qf.Z by MMA), gn, gd (written to scratch), [dP | dqf] by one MMA,
 //     dqf += dP kf with dP read from TMEM, dQ out; the first piece's sum
 //     qf^T g (its share of R) is published for the suffix kernel when earlier
 //     units of its head exist;
 //   suffix kernel -- walks its chunks in reverse; the last piece starts from
 //     the shares of the later units of its head (all complete, the prefix
-//     kernel has finished), earlier pieces from zero: gn = G / den formed in
-//     place from the G tile, P^T and dP^T by MMA,
+//     kernel has finished), earlier pieces from zero: P^T and dP^T by MMA,
 //     masked and packed in TMEM, dV = P^T gn + kf R and dkf = dP^T qf +
 //     [V | 1][R | r]^T with P^T, dP^T read from TMEM, R += qf^T g.
 // Each CTA has eight compute warps (the epilogues), one MMA warp (every MMA,
@@ -107,8 +106,6 @@ struct BwdParams {
     unsigned* ticket;
     float* gd;            // [BH][N]
     const float* den;     // [BH][N] the forward's normaliser per token, or null (recomputed)
-    float* den_out;       // [BH][N] the prefix kernel's recomputed normaliser for the suffix
-                          // kernel, when den is null
     const float* ckpt;    // the forward's state checkpoints (see kCkptChunks), or null
     unsigned* status;
     int withhold;         // test hook: a unit that does not publish its aggregate (-1: none)
@@ -356,7 +353,6 @@ constexpr int kEM = kBT + 32;             // compute warps + MMA warp
 constexpr uint32_t kBarE = 3, kBarT = 2, kBarEM = 1, kBarME = 4;
 constexpr uint32_t kBarEM2 = 5;  // the second compute -> MMA warp hand-over of a chunk
 constexpr uint32_t kBarEM3 = 6;  // the third
-constexpr uint32_t kBarEM4 = 7;  // suffix kernel: gn formed in the g tile (before the other three)
 
 // Hand-over among the compute warps when they issue MMAs themselves (phase 1):
 // their shared-memory writes become visible to the tensor core and TMA, and
@@ -482,8 +478,8 @@ struct TmaBook {
 __global__ void __launch_bounds__(kCT, 1)
 bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmdQ,
-                     const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmGn,
+                     const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
     using Lay = LayF;
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
@@ -701,6 +697,7 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     r_phase ^= 1u;
                     mbar_arrive(&bars->freeb[b ^ 1]);
                 }
+                tma_store_wait_read_but_last();  // the g tile is read out (the dQ store may go on)
             }
             __syncwarp();
             hand_to_compute();  // G, O in; the g tile free: the compute warps start on gn, gd
@@ -726,6 +723,8 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     book.load(sm + Lay::G, &tmG, tma_bar, 0, cn0, hn);
                     book.load(sm + Lay::O, &tmO, tma_bar, 0, cn0, hn);
                 }
+                tma_store_3d(&tmGn, sm + Lay::GH, 0, c0, bh);
+                tma_store_commit();
 #pragma unroll
                 for (int k = 0; k < NE / 16; ++k)  // [dP | dqf] = g [V | 1 ; S | Z]^T
                     mma_bf16(tm + Lay::T_P, kmaj(sGh, k, kAtom), kmaj(sV, k, Lay::VS_K), ID_PQ, k > 0);
@@ -738,8 +737,8 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             __syncwarp();
             take_from_compute(kBarEM2);  // dP is masked and packed in TMEM
             if (lead) {
-                tma_store_wait_read();  // the previous dQ store is read out: the staging tile is
-                                        // free once this chunk's MMA3 commits
+                tma_store_wait_read_but_last();  // the previous dQ store is read out: the staging
+                                                 // tile is free once this chunk's MMA3 commits
 #pragma unroll
                 for (int k = 0; k < L / 16; ++k)  // dqf += dP kf, dP read from TMEM
                     mma_bf16_ts(tm + Lay::T_DQ, tm + Lay::T_P + packed_a_col(k), mnmaj(sK, k, kAtom),
@@ -808,7 +807,6 @@ bwd_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     *reinterpret_cast<uint4*>(sm + Lay::GH + kAtom + swz(row, 1)) =
                         make_uint4(0u, 0u, 0u, 0u);
                     if (ok) p.gd[static_cast<size_t>(bh) * p.N + c0 + row] = gd;
-                    if (ok && p.den_out) p.den_out[static_cast<size_t>(bh) * p.N + c0 + row] = den;
                 }
             }
             hand_to_mma();
@@ -847,7 +845,7 @@ cleanup:
 
 __global__ void __launch_bounds__(kCT, 1)
 bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmGn,
                      const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                      const BwdParams p) {
     using Lay = LayR;
@@ -924,11 +922,11 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         };
         float gdn[4];
         gd_rows(ur.end - 1, gdn);
-        if (lead) {  // V and G of the first chunk; Q and K come from the transform warps
+        if (lead) {  // V and g of the first chunk; Q and K come from the transform warps
             const int c0 = (ur.end - 1 - ur.hB * p.CH) * L;
             book.expect(tma_bar, 2 * kAtom);
             book.load(sm + Lay::V, &tmV, tma_bar, 0, c0, ur.hB);
-            book.load(sm + Lay::GH, &tmG, tma_bar, 0, c0, ur.hB);
+            book.load(sm + Lay::GH, &tmGn, tma_bar, 0, c0, ur.hB);
         }
         for (int gc = ur.end - 1; gc >= ur.start; --gc) {
             const int bh = gc / p.CH, cc = gc - bh * p.CH;
@@ -959,15 +957,14 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 for (int k = 0; k < D / 16; ++k)  // P^T = kf qf^T (needs no V or g)
                     mma_bf16(tm + Lay::T_P, kmaj(sK, k, kAtom), kmaj(sQ, k, kAtom), ID_P, k > 0);
                 mma_commit(&bars->cb[0]);
-                poll(tma_bar, tma_phase, bars, p.status);  // V, G
+            }
+            __syncwarp();
+            hand_to_compute();
+            if (lead) {
+                poll(tma_bar, tma_phase, bars, p.status);  // V, gn
                 tma_phase ^= 1u;
                 book.pending = false;
                 if (more) book.expect(tma_bar, 2 * kAtom);
-            }
-            __syncwarp();
-            hand_to_compute();           // P^T issued, V and G in: the compute warps form gn
-            take_from_compute(kBarEM4);  // gn = G / den is in the g tile
-            if (lead) {
 #pragma unroll
                 for (int k = 0; k < NE / 16; ++k)  // dP^T = [V | 1] g^T
                     mma_bf16(tm + Lay::T_DP, kmaj(sV, k, kAtom), kmaj(sGh, k, kAtom), ID_P, k > 0);
@@ -1007,7 +1004,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 r_phase ^= 1u;
                 if (more) {
                     book.load(sm + Lay::V, &tmV, tma_bar, 0, cn0, hn);
-                    book.load(sm + Lay::GH, &tmG, tma_bar, 0, cn0, hn);
+                    book.load(sm + Lay::GH, &tmGn, tma_bar, 0, cn0, hn);
                 }
             }
             __syncwarp();
@@ -1025,13 +1022,6 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             bar_sync(kBarE, kBT);
             fence_after_sync();
         };
-        // this thread's row of the normaliser, one chunk ahead (0 past the end of a head)
-        const float* den_src = p.den ? p.den : p.den_out;
-        auto den_row = [&](int gc) {
-            const int h = gc / p.CH, c0 = (gc - h * p.CH) * L;
-            return row < p.N - c0 ? __ldg(den_src + static_cast<size_t>(h) * p.N + c0 + row) : 0.f;
-        };
-        float den_next = den_row(ur.end - 1);
         for (int gc = ur.end - 1; gc >= ur.start; --gc) {
             const int bh = gc / p.CH, cc = gc - bh * p.CH;
             const bool more = gc > ur.start;
@@ -1039,19 +1029,7 @@ bwd_suffix_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const uint32_t ph = static_cast<uint32_t>(ur.end - 1 - gc) & 1u;  // this chunk's phase
             uint8_t* const tK = sm + (b ? Lay::K1 : Lay::K0);
             (void)bh;
-            const float den = den_next;
-            if (more) den_next = den_row(gc - 1);
             take_from_mma();
-            {   // gn = G / den in place (rows past the end of the head hold zeros and stay zero)
-                const float inv = den != 0.f ? 1.f / den : 0.f;
-                float gv[32];
-                read_row32(sm + Lay::GH, row, 4 * g, gv);
-                uint32_t pk[16];
-#pragma unroll
-                for (int u2 = 0; u2 < 16; ++u2) pk[u2] = pack_bf16(gv[2 * u2] * inv, gv[2 * u2 + 1] * inv);
-                store_row32(sm + Lay::GH, kAtom, row, 32 * g, pk);
-            }
-            hand_to_mma(kBarEM4);
             wait_on(&bars->cb[0], ph);  // P^T
             masked_half_t_to_tmem(tm + lane + Lay::T_P, row, q, g);   // P^T, masked, bf16 in TMEM
             hand_to_mma();              // the dV products start
@@ -1096,17 +1074,17 @@ size_t causal_backward_tc64_scratch(int BH, int N, int num_sms, bool out_given, 
     const int chunks = (N + L - 1) / L;
     const size_t units = static_cast<size_t>(plan::tc_units(BH, chunks, num_sms));
     const size_t agg = sizeof(float) * units * W, flags = sizeof(unsigned) * (units + 1);
-    const size_t o = sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
-    const size_t rowf = sizeof(float) * static_cast<size_t>(BH) * N;  // one fp32 word per token
+    const size_t gn = sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
+    const size_t gd = sizeof(float) * static_cast<size_t>(BH) * N;
     using plan::up256;
-    // S and R shares, flags, gd rows, and the normaliser rows when the call does not pass them
-    size_t total = 2 * up256(agg) + up256(flags) + up256(rowf) + (den_given ? 0 : up256(rowf));
-    if (!out_given) {  // Out recomputed: its tile, its checkpoints and the forward's own scratch,
-                       // live at the same time (the normaliser slot above takes its den)
-        total += up256(o);
+    size_t total = 2 * up256(agg) + up256(flags) + up256(gn) + up256(gd);
+    if (!out_given) {  // Out recomputed: its tile, its normaliser, its checkpoints and the
+                       // forward's own scratch, live at the same time
+        total += up256(gn) + up256(gd);
         if (!ckpt_given) total += up256(sizeof(float) * static_cast<size_t>(BH) * ckpt_slots(chunks) * W);
         total += causal_forward_tc_scratch(64, BH, N, num_sms);
     }
+    (void)den_given;  // the layout reserves the normaliser whenever Out is recomputed
     return total;
 }
 
@@ -1137,15 +1115,14 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
 
     const size_t agg_bytes = sizeof(float) * static_cast<size_t>(units) * W;
     const size_t flag_bytes = sizeof(unsigned) * (static_cast<size_t>(units) + 1);
+    const size_t gn_bytes = sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
     const size_t gd_bytes = sizeof(float) * static_cast<size_t>(BH) * N;
-    const size_t o_bytes = O ? 0 : sizeof(__nv_bfloat16) * static_cast<size_t>(BH) * N * M;
-    // the normaliser rows when the call does not pass them: the recomputed forward's, or the
-    // prefix kernel's for the suffix kernel
-    const size_t den_bytes = Den ? 0 : gd_bytes;
-    const size_t ck_bytes =  // the recomputed forward's checkpoints
+    const size_t o_bytes = O ? 0 : gn_bytes;
+    const size_t den_bytes = O ? 0 : gd_bytes;  // the recomputed forward's normaliser
+    const size_t ck_bytes =  // and its checkpoints
         O || Ckpt ? 0 : sizeof(float) * static_cast<size_t>(BH) * ckpt_slots(chunks) * W;
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gd_bytes) + up(o_bytes) +
+    const size_t total = 2 * up(agg_bytes) + up(flag_bytes) + up(gn_bytes) + up(gd_bytes) + up(o_bytes) +
                          up(den_bytes) + up(ck_bytes);
     char* ws = nullptr;
     if (total != causal_backward_tc64_scratch(BH, N, c.num_sms, O != nullptr, Den != nullptr,
@@ -1166,15 +1143,16 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
     p.flags = reinterpret_cast<unsigned*>(q);
     p.ticket = p.flags + units;
     q += up(flag_bytes);
+    __nv_bfloat16* gn = reinterpret_cast<__nv_bfloat16*>(q);
+    q += up(gn_bytes);
     p.gd = reinterpret_cast<float*>(q);
     q += up(gd_bytes);
     __nv_bfloat16* Ow = O ? nullptr : reinterpret_cast<__nv_bfloat16*>(q);
     q += up(o_bytes);
-    float* Dw = Den ? nullptr : reinterpret_cast<float*>(q);
+    float* Dw = O ? nullptr : reinterpret_cast<float*>(q);
     q += up(den_bytes);
     float* Cw = ck_bytes ? reinterpret_cast<float*>(q) : nullptr;
     p.den = Den;
-    p.den_out = nullptr;
     p.ckpt = Ckpt;
     p.withhold = c.withhold_unit;
     p.spin_limit = c.spin_limit ? c.spin_limit : kSpinLimit;
@@ -1187,19 +1165,17 @@ cudaError_t causal_backward_tc64(const LaunchCtx& c, const __nv_bfloat16* Q, con
             O = Ow;
             if (!Den) p.den = Dw;
             if (!Ckpt) p.ckpt = Cw;
-        } else if (!Den) {  // the prefix kernel recomputes the normaliser and keeps it for the suffix
-            p.den_out = Dw;
         }
         if ((e = cudaMemsetAsync(p.flags, 0, flag_bytes, c.stream)) != cudaSuccess) break;
-        CUtensorMap mQ, mK, mV, mG, mO, mdQ, mdK, mdV;
+        CUtensorMap mQ, mK, mV, mG, mO, mGn, mdQ, mdK, mdV;
         if ((e = make_map(&mQ, Q, BH, N, D)) || (e = make_map(&mK, K, BH, N, D)) ||
             (e = make_map(&mV, V, BH, N, M)) || (e = make_map(&mG, G, BH, N, M)) ||
-            (e = make_map(&mO, O, BH, N, M)) ||
+            (e = make_map(&mO, O, BH, N, M)) || (e = make_map(&mGn, gn, BH, N, M)) ||
             (e = make_map(&mdQ, dQ, BH, N, D)) || (e = make_map(&mdK, dK, BH, N, D)) ||
             (e = make_map(&mdV, dV, BH, N, M)))
             break;
-        kf<<<units, kCT, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mdQ, p);
-        kr<<<units, kCT, LayR::BYTES, c.stream>>>(mQ, mK, mV, mG, mdK, mdV, p);
+        kf<<<units, kCT, LayF::BYTES, c.stream>>>(mQ, mK, mV, mG, mO, mGn, mdQ, p);
+        kr<<<units, kCT, LayR::BYTES, c.stream>>>(mQ, mK, mV, mGn, mdK, mdV, p);
         note_launch(2);
         e = cudaGetLastError();
     } while (0);

@@ -87,12 +87,11 @@ def _run(e_ops, m_ops, degraded, seed):
 
 
 def suffix_protocol(n, ids):
-    em, em2, em3, em4 = ids
+    em, em2, em3 = ids
 
     def e():
         for i in range(n):
             yield ("sync", "ME")
-            yield ("arrive", em4)      # G scaled to gn in the g tile
             yield ("wait", "PT", i)
             yield ("arrive", em)
             yield ("wait", "dPT", i)
@@ -105,8 +104,7 @@ def suffix_protocol(n, ids):
     def m():
         for i in range(n):
             yield ("commit", "PT")
-            yield ("arrive", "ME")     # P^T issued, V and G landed
-            yield ("sync", em4)
+            yield ("arrive", "ME")
             yield ("commit", "dPT")
             yield ("sync", em)
             yield ("commit", "dV")
@@ -120,7 +118,7 @@ def suffix_protocol(n, ids):
 
 
 def prefix_protocol(n, ids):
-    em, em2, em3 = ids[:3]
+    em, em2, em3 = ids
 
     def e():
         for i in range(n):
@@ -148,7 +146,7 @@ def prefix_protocol(n, ids):
     return e(), m()
 
 
-KERNEL_IDS = ("EM", "EM2", "EM3", "EM4")
+KERNEL_IDS = ("EM", "EM2", "EM3")
 
 
 @pytest.mark.parametrize("protocol", [suffix_protocol, prefix_protocol])
@@ -161,5 +159,5 @@ def test_protocol_is_safe_under_any_schedule(protocol, degraded):
 
 @pytest.mark.parametrize("protocol", [suffix_protocol, prefix_protocol])
 def test_model_finds_the_hazard_of_one_shared_barrier(protocol):
-    results = {_run(*protocol(n, ("EM", "EM", "EM", "EM")), True, seed) for n in (2, 3) for seed in range(300)}
+    results = {_run(*protocol(n, ("EM", "EM", "EM")), True, seed) for n in (2, 3) for seed in range(300)}
     assert "double arrival" in results

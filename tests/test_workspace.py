@@ -31,21 +31,18 @@ def test_training_forward_bytes():
 
 def test_training_backward_bytes():
     # one CTA per SM -> 152 slots; ranges of ceil(4096 / 152) = 27 chunks -> 152
-    # units.  Two state arrays (S and R shares), flags and fp32 gd rows [64][8192];
-    # each part rounded up to 256 bytes.
+    # units.  Two state arrays (S and R shares), flags, bf16 gn rows [64][8192][64],
+    # fp32 gd rows [64][8192]; each part rounded up to 256 bytes.
     up = lambda x: (x + 255) // 256 * 256
     agg = 4 * 152 * (64 * 64 + 64)
-    want = 2 * up(agg) + up(4 * 153) + up(4 * 64 * 8192)
+    want = 2 * up(agg) + up(4 * 153) + up(2 * 64 * 8192 * 64) + up(4 * 64 * 8192)
     assert _ws("la_backward_causal", 4, 16, 8192, 64, 64, BF16, SAVED_ALL) == want
-    # without the normaliser: its rows [64][8192] (the prefix kernel keeps them for the suffix)
-    assert _ws("la_backward_causal", 4, 16, 8192, 64, 64, BF16,
-               _native.LA_SAVED_OUT | _native.LA_SAVED_CKPT) == want + up(4 * 64 * 8192)
     # without Out the call recomputes the forward: its output tile, normaliser,
     # checkpoints (8 slots per head) and the forward's own scratch on top
     fwd = _ws("la_forward_causal", 4, 16, 8192, 64, 64, BF16)
     ck = 4 * 64 * 8 * (64 * 64 + 64)
     assert _ws("la_backward_causal", 4, 16, 8192, 64, 64, BF16, 0) == \
-        want + up(4 * 64 * 8192) + up(2 * 64 * 8192 * 64) + up(ck) + fwd
+        want + up(2 * 64 * 8192 * 64) + up(4 * 64 * 8192) + up(ck) + fwd
 
 
 def test_noncausal_and_decode_bytes():
