@@ -206,8 +206,12 @@ struct BwdNoncausal {
     template <typename T, int D, int M>
     static cudaError_t run(const LaunchCtx* c, const void* Q, const void* K, const void* V,
                            const void* O, const void* G, void* dQ, void* dK, void* dV, int BH, int N) {
-        return noncausal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
-                                           (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
+        if constexpr (std::is_same<T, float>::value && D == 64 && M == 64)
+            return noncausal_backward_tc_f32(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
+                                             (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
+        else
+            return noncausal_backward<T, D, M>(*c, (const T*)Q, (const T*)K, (const T*)V, (const T*)O,
+                                               (const T*)G, (T*)dQ, (T*)dK, (T*)dV, BH, N);
     }
 };
 struct FwdRetention {
@@ -286,7 +290,9 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
         if (!bf16 && D == 64 && M == 64) return noncausal_forward_tc_f32_scratch(BH, N, sms);
         return plan::ffma_noncausal_forward(BH, N, D, M, sms);
     }
-    if (!strcmp(op, "la_backward_noncausal")) return plan::ffma_noncausal_backward(BH, N, D, M, sms);
+    if (!strcmp(op, "la_backward_noncausal"))
+        return !bf16 && D == 64 && M == 64 ? noncausal_backward_tc_f32_scratch(BH, N, sms)
+                                           : plan::ffma_noncausal_backward(BH, N, D, M, sms);
     if (!strcmp(op, "la_forward_poly2"))
         return D == 32 && (M == 32 || M == 64) ? plan::poly2_scratch(BH, N, M, sms) : SIZE_MAX;
     if (!strcmp(op, "la_forward_retention"))

@@ -87,6 +87,12 @@ template <typename T, int D, int M>
 cudaError_t noncausal_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O,
                               int BH, int N);
 
+// Tensor-core non-causal backward for fp32 storage with D = M = 64 (O nullable).
+cudaError_t noncausal_backward_tc_f32(const LaunchCtx& c, const float* Q, const float* K,
+                                      const float* V, const float* O, const float* G, float* dQ,
+                                      float* dK, float* dV, int BH, int N);
+size_t noncausal_backward_tc_f32_scratch(int BH, int N, int num_sms);
+
 template <typename T, int D, int M>
 cudaError_t noncausal_backward(const LaunchCtx& c, const T* Q, const T* K, const T* V, const T* O,
                                const T* G, T* dQ, T* dK, T* dV, int BH, int N);

@@ -26,6 +26,7 @@
 #include <algorithm>
 
 #include "la_launch.h"
+#include "la_plan.h"
 #include "tc_common.cuh"
 
 namespace la {
@@ -405,6 +406,476 @@ cleanup:
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
 }
 
+// ---------------------------------------------------------------- backward
+//
+// Gradient of the non-causal form for fp32 storage at D = M = 64 ("Transformers
+// are RNNs" section 二, eq. linear; the gradients of section 三（一）4 with the
+// prefix and suffix sums over all tokens; the denominator by the quotient rule):
+//   gn_i = G_i / den_i,  gd_i = -(G_i . O_i) / den_i,  g = [gn | gd 0 .. 0]
+//   dqf = g [S | Z]^T                 (query side, with S, Z from the state kernel)
+//   [R | r] = sum_i qf_i^T g_i        (query side, per-span partials)
+//   dkf = [V | 1] [R | r]^T,  dV = kf R   (key side)
+// on the same split-bf16 products as the forward (hi hi + hi lo + lo hi).
+
+constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, false);  // g [S | Z]^T, K-major x K-major
+constexpr uint32_t ID_DV = idesc_bf16(128, M, false, true);   // kf R, K-major x MN-major
+
+// K-major descriptor for K step k of a tile whose 64-column atoms are `atom` bytes apart.
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int k, uint32_t atom) {
+    return sdesc(base + (k >> 2) * atom + 32 * (k & 3), 16, 1024);
+}
+// MN-major descriptor for K step k (16 rows) of a tile whose atoms are `lbo` bytes apart.
+__device__ __forceinline__ uint64_t mdesc(uint32_t base, int k, uint32_t lbo) {
+    return sdesc(base + 2048 * k, lbo, 1024);
+}
+
+// query-side kernel shared memory: Q (fp32, then phi(Q) hi | lo), G (fp32, then gn
+// hi | lo), O (fp32 when given, then the gd atoms hi | lo), the state tiles
+// [S_hi | Z_hi | S_lo | Z_lo] and the fp32 dQ staging tile; the gn and gd atoms
+// are 2 kAtom apart, the column stride of the 80-wide g operand.
+struct LayQ {
+    static constexpr uint32_t Q = 0, G = 2 * kAtom, O = 4 * kAtom, S = 6 * kAtom, OUT = 8 * kAtom;
+    static constexpr uint32_t GSTEP = O - G;
+    static constexpr uint32_t BARS = 10 * kAtom;
+    static constexpr uint32_t XCH = BARS + 64;  // [2][128] fp32 partial row sums
+    static constexpr uint32_t BYTES = XCH + 1024;
+    static constexpr uint32_t T_O = 0, T_DQ = 80, T_R = 144, T_COLS = 256;
+};
+// key-side kernel shared memory: K (fp32, then phi(K) hi | lo), V (fp32, then
+// hi | lo), the ones atom (2 kAtom after V_hi: the column stride of [V_hi | 1]),
+// the tiles [R_hi | r_hi | R_lo | r_lo] and the fp32 dK and dV staging tiles.
+struct LayK {
+    static constexpr uint32_t K = 0, V = 2 * kAtom, ONES = 4 * kAtom, R = 5 * kAtom;
+    static constexpr uint32_t DK = 7 * kAtom, DV = 9 * kAtom;
+    static constexpr uint32_t BARS = 11 * kAtom;
+    static constexpr uint32_t BYTES = BARS + 64;
+    static constexpr uint32_t T_DK = 0, T_DV = 64, T_COLS = 128;
+};
+static_assert(LayQ::BYTES <= 227 * 1024 && LayK::BYTES <= 227 * 1024, "shared memory");
+
+struct NcbParams {
+    int N;
+    int s_spans;          // state partials per head (the state kernel's spans)
+    int q_spans, q_len;   // query-side spans (the (R | r) partials' layout)
+    int k_spans, k_len;   // key-side spans
+    const float* spart;   // [BH][s_spans][W]
+    float* rpart;         // [BH][q_spans][W]
+    unsigned* status;
+};
+
+// Sum of the partials sp < n of row d (this warpgroup's 32 columns into v[], the
+// extension word returned), read from [.. ][n][W] at `base`.
+__device__ __forceinline__ float sum_partials(const float* base, int n, int d, int g, float (&v)[32]) {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) v[u] = 0.f;
+    float z = 0.f;
+    for (int sp = 0; sp < n; ++sp) {
+        const float4* a = reinterpret_cast<const float4*>(base + static_cast<size_t>(sp) * W + d * M + 32 * g);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float4 x = __ldcg(a + u);
+            v[4 * u] += x.x;
+            v[4 * u + 1] += x.y;
+            v[4 * u + 2] += x.z;
+            v[4 * u + 3] += x.w;
+        }
+        z += __ldcg(base + static_cast<size_t>(sp) * W + D * M + d);
+    }
+    return z;
+}
+
+// Row d, columns 32 g .. 32 g + 31 of a state as bf16 hi (at `hi`) and lo (at
+// `lo`) swizzled 64-row atoms.
+__device__ __forceinline__ void put_state_row(uint8_t* hi, uint8_t* lo, int d, int g, const float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float h0, l0, h1, l1;
+            split_bf16(v[8 * c + 2 * u], h0, l0);
+            split_bf16(v[8 * c + 2 * u + 1], h1, l1);
+            h[u] = pack_bf16(h0, h1);
+            l[u] = pack_bf16(l0, l1);
+        }
+        *reinterpret_cast<uint4*>(hi + swz(d, 4 * g + c)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(lo + swz(d, 4 * g + c)) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// An extension row: x in column 0, zeros in columns 1 .. 15 (hi and lo atoms).
+__device__ __forceinline__ void put_ext_row(uint8_t* hi, uint8_t* lo, int r, float x) {
+    float h, l;
+    split_bf16(x, h, l);
+    *reinterpret_cast<uint4*>(hi + swz(r, 0)) = make_uint4(pack_bf16(h, 0.f), 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(hi + swz(r, 1)) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(lo + swz(r, 0)) = make_uint4(pack_bf16(l, 0.f), 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(lo + swz(r, 1)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// phi'(x) = min(phi(x), 1) for 32 columns of row r of a split phi tile (hi at
+// `hi`, lo one atom after): phi = hi + lo.
+__device__ __forceinline__ void dphi_row(const uint8_t* hi, int r, int g, float (&f)[32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 a = *reinterpret_cast<const uint4*>(hi + swz(r, 4 * g + c));
+        const uint4 b = *reinterpret_cast<const uint4*>(hi + kAtom + swz(r, 4 * g + c));
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            f[8 * c + 2 * u] = fminf(__uint_as_float(wa[u] << 16) + __uint_as_float(wb[u] << 16), 1.f);
+            f[8 * c + 2 * u + 1] =
+                fminf(__uint_as_float(wa[u] & 0xFFFF0000u) + __uint_as_float(wb[u] & 0xFFFF0000u), 1.f);
+        }
+    }
+}
+
+template <bool HAS_O>
+__global__ void __launch_bounds__(NT, 1)
+ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmdQ,
+                    const NcbParams p) {
+    using Lay = LayQ;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int t = threadIdx.x, warp = t >> 5;
+    if (smem_u32(sm) & 1023u) {
+        if (t == 0) atomicOr(p.status, kErrAlign);
+        return;
+    }
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+    uint64_t* mma_bar = tma_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
+    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    float* xch = reinterpret_cast<float*>(sm + Lay::XCH);
+    if (t == 0) {
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        fence_mbar_init();
+        sh[1] = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    const int unit = blockIdx.x;
+    const int bh = unit / p.q_spans, s = unit - bh * p.q_spans;
+    const int n0 = s * p.q_len, n1 = min(p.N, n0 + p.q_len);
+    const int nch = (n1 - n0 + L - 1) / L;
+    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
+    const int row = 32 * q + (t & 31);
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t sQ = smem_u32(sm + Lay::Q), sG = smem_u32(sm + Lay::G), sS = smem_u32(sm + Lay::S);
+    uint32_t tma_phase = 0, mma_phase = 0;
+
+    auto fail = [&](unsigned code) {
+        atomicOr(p.status, code);
+        sh[1] = 1;
+    };
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        __syncthreads();
+        phase ^= 1u;
+    };
+    auto load = [&](int c0) {  // thread 0 only
+        mbar_arrive_expect_tx(tma_bar, (HAS_O ? 6 : 4) * kAtom);
+        for (int a = 0; a < 2; ++a) {
+            tma_load_3d(sm + Lay::Q + a * kAtom, &tmQ, tma_bar, 32 * a, c0, bh);
+            tma_load_3d(sm + Lay::G + a * kAtom, &tmG, tma_bar, 32 * a, c0, bh);
+            if (HAS_O) tma_load_3d(sm + Lay::O + a * kAtom, &tmO, tma_bar, 32 * a, c0, bh);
+        }
+    };
+    if (t == 0) load(n0);
+
+    if (q < D / 32) {  // [S | Z] of the head, split: row d, this warpgroup's 32 columns
+        float v[32];
+        const float z = sum_partials(p.spart + static_cast<size_t>(bh) * p.s_spans * W, p.s_spans, row, g, v);
+        put_state_row(sm + Lay::S, sm + Lay::S + 2 * S_ATOM, row, g, v);
+        if (g == 0) {  // Z, sixteen copies (the den column of qf [S | Z] reads the first)
+            float zh, zl;
+            split_bf16(z, zh, zl);
+            const uint32_t ph = pack_bf16(zh, zh), pl = pack_bf16(zl, zl);
+            for (int c = 0; c < 2; ++c) {
+                *reinterpret_cast<uint4*>(sm + Lay::S + S_ATOM + swz(row, c)) = make_uint4(ph, ph, ph, ph);
+                *reinterpret_cast<uint4*>(sm + Lay::S + 3 * S_ATOM + swz(row, c)) = make_uint4(pl, pl, pl, pl);
+            }
+        }
+    }
+
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = n0 + c * L;
+        const int valid = min(L, n1 - c0);
+        wait_bar(tma_bar, tma_phase);
+        split_tile<true, false>(sm + Lay::Q, L);  // phi(Q) hi | lo (rows past N are 0: phi(0) = 1
+                                                  // there, but their g rows are 0)
+        if (t == 0) tma_store_wait_read();        // the dQ staging tile is free again
+        sync_tc();
+        if (sh[1]) goto cleanup;
+        if (t == 0) {  // O_ext = qf [S | Z]
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                mma_bf16(tm + Lay::T_O, sdesc(sQ + 32 * k, 16, 1024), sdesc(sS + 2048 * k, S_ATOM, 1024), ID_O,
+                         k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                mma_bf16(tm + Lay::T_O, sdesc(sQ + 32 * k, 16, 1024),
+                         sdesc(sS + 2 * S_ATOM + 2048 * k, S_ATOM, 1024), ID_O, 1u);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                mma_bf16(tm + Lay::T_O, sdesc(sQ + kAtom + 32 * k, 16, 1024), sdesc(sS + 2048 * k, S_ATOM, 1024),
+                         ID_O, 1u);
+            mma_commit(mma_bar);
+        }
+        float gv[32], ov[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // this thread's 32 columns of G (and O) from the fp32 tiles
+            const float4 a = *reinterpret_cast<const float4*>(sm + Lay::G + f32_off(row, 32 * g + 4 * u));
+            gv[4 * u] = a.x;
+            gv[4 * u + 1] = a.y;
+            gv[4 * u + 2] = a.z;
+            gv[4 * u + 3] = a.w;
+            if (HAS_O) {
+                const float4 b = *reinterpret_cast<const float4*>(sm + Lay::O + f32_off(row, 32 * g + 4 * u));
+                ov[4 * u] = b.x;
+                ov[4 * u + 1] = b.y;
+                ov[4 * u + 2] = b.z;
+                ov[4 * u + 3] = b.w;
+            }
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        float den;
+        {
+            float dz[16];
+            tmem_ld16(tm + lane + Lay::T_O + M, dz);
+            den = dz[0];
+        }
+        const float inv = row < valid ? 1.f / den : 0.f;
+        if (!HAS_O) {  // O = num / den
+            tmem_ld32(tm + lane + Lay::T_O + 32 * g, ov);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) ov[u] *= inv;
+        }
+        float go = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) go = fmaf(gv[u], ov[u], go);
+        xch[g * 128 + row] = go;
+        __syncthreads();  // every G and O row is read: the tiles take g from here on
+        const float gd = -(xch[row] + xch[128 + row]) * inv;
+        {   // gn = G / den, split, into the G tile's atoms
+#pragma unroll
+            for (int u = 0; u < 32; ++u) gv[u] *= inv;
+            put_state_row(sm + Lay::G, sm + Lay::G + kAtom, row, g, gv);
+            if (g == 0) put_ext_row(sm + Lay::O, sm + Lay::O + kAtom, row, gd);
+        }
+        sync_tc();
+        if (t == 0) {
+            const uint32_t sGl = sG + kAtom;
+            // dqf = g [S | Z]^T: g_hi [S | Z]_hi + g_hi [S | Z]_lo + g_lo [S | Z]_hi
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)
+                mma_bf16(tm + Lay::T_DQ, kdesc(sG, k, Lay::GSTEP), kdesc(sS, k, S_ATOM), ID_DQ, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)
+                mma_bf16(tm + Lay::T_DQ, kdesc(sG, k, Lay::GSTEP), kdesc(sS + 2 * S_ATOM, k, S_ATOM), ID_DQ, 1u);
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)
+                mma_bf16(tm + Lay::T_DQ, kdesc(sGl, k, Lay::GSTEP), kdesc(sS, k, S_ATOM), ID_DQ, 1u);
+            // [R | r] += qf^T g (the D = 64 rows pad to 128 through the A operand's atom stride)
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)
+                mma_bf16(tm + Lay::T_R, mdesc(sQ, k, kAtom), mdesc(sG, k, Lay::GSTEP), ID_S,
+                         (c > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)
+                mma_bf16(tm + Lay::T_R, mdesc(sQ, k, kAtom), mdesc(sGl, k, Lay::GSTEP), ID_S, 1u);
+#pragma unroll
+            for (int k = 0; k < L / 16; ++k)
+                mma_bf16(tm + Lay::T_R, mdesc(sQ + kAtom, k, kAtom), mdesc(sG, k, Lay::GSTEP), ID_S, 1u);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        {   // dQ = dqf * phi'(Q) -> fp32 staging tile
+            float v[32], f[32];
+            tmem_ld32(tm + lane + Lay::T_DQ + 32 * g, v);
+            dphi_row(sm + Lay::Q, row, g, f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(sm + Lay::OUT + f32_off(row, 32 * g + 4 * u)) =
+                    make_float4(v[4 * u] * f[4 * u], v[4 * u + 1] * f[4 * u + 1], v[4 * u + 2] * f[4 * u + 2],
+                                v[4 * u + 3] * f[4 * u + 3]);
+        }
+        sync_tc();
+        if (t == 0) {
+            tma_store_3d(&tmdQ, sm + Lay::OUT, 0, c0, bh);
+            tma_store_3d(&tmdQ, sm + Lay::OUT + kAtom, 32, c0, bh);
+            tma_store_commit();
+            if (c + 1 < nch) load(c0 + L);  // every input tile is consumed
+        }
+    }
+    if (q < D / 32) {  // publish this span's [R | r]
+        float* out = p.rpart + (static_cast<size_t>(bh) * p.q_spans + s) * W;
+        float v[32];
+        tmem_ld32(tm + lane + Lay::T_R + 32 * g, v);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            reinterpret_cast<float4*>(out + row * M + 32 * g)[u] =
+                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        if (g == 0) {
+            float z[16];
+            tmem_ld16(tm + lane + Lay::T_R + M, z);
+            out[D * M + row] = z[0];
+        }
+    }
+
+cleanup:  // the only early exit follows a copy wait: no copy of this CTA is in flight
+    if (t == 0) tma_store_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                  const NcbParams p) {
+    using Lay = LayK;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int t = threadIdx.x, warp = t >> 5;
+    if (smem_u32(sm) & 1023u) {
+        if (t == 0) atomicOr(p.status, kErrAlign);
+        return;
+    }
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
+    uint64_t* mma_bar = tma_bar + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
+    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    if (t == 0) {
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        fence_mbar_init();
+        sh[1] = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, Lay::T_COLS);
+        tmem_relinquish();
+    }
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += NT)
+        reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
+            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    const int unit = blockIdx.x;
+    const int bh = unit / p.k_spans, s = unit - bh * p.k_spans;
+    const int n0 = s * p.k_len, n1 = min(p.N, n0 + p.k_len);
+    const int nch = (n1 - n0 + L - 1) / L;
+    const int q = warp & 3, g = warp >> 2;
+    const int row = 32 * q + (t & 31);
+    const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sR = smem_u32(sm + Lay::R);
+    constexpr uint32_t VSTEP = Lay::ONES - Lay::V;  // [V_hi | 1]: the ones atom 2 kAtom after V_hi
+    uint32_t tma_phase = 0, mma_phase = 0;
+
+    auto fail = [&](unsigned code) {
+        atomicOr(p.status, code);
+        sh[1] = 1;
+    };
+    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
+        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
+        __syncthreads();
+        phase ^= 1u;
+    };
+    auto load = [&](int c0) {  // thread 0 only
+        mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
+        for (int a = 0; a < 2; ++a) {
+            tma_load_3d(sm + Lay::K + a * kAtom, &tmK, tma_bar, 32 * a, c0, bh);
+            tma_load_3d(sm + Lay::V + a * kAtom, &tmV, tma_bar, 32 * a, c0, bh);
+        }
+    };
+    if (t == 0) load(n0);
+
+    if (q < D / 32) {  // [R | r] of the head (the query side's partials), split
+        float v[32];
+        const float r = sum_partials(p.rpart + static_cast<size_t>(bh) * p.q_spans * W, p.q_spans, row, g, v);
+        put_state_row(sm + Lay::R, sm + Lay::R + 2 * S_ATOM, row, g, v);
+        if (g == 0) put_ext_row(sm + Lay::R + S_ATOM, sm + Lay::R + 3 * S_ATOM, row, r);
+    }
+
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = n0 + c * L;
+        wait_bar(tma_bar, tma_phase);
+        split_tile<true, false>(sm + Lay::K, L);   // phi(K) hi | lo
+        split_tile<false, false>(sm + Lay::V, L);  // V hi | lo
+        if (t == 0) tma_store_wait_read();         // the staging tiles are free again
+        sync_tc();
+        if (sh[1]) goto cleanup;
+        if (t == 0) {
+            const uint32_t sVl = sV + kAtom, sKl = sK + kAtom, sRl = sR + 2 * S_ATOM;
+            // dkf = [V | 1] [R | r]^T: [V_hi | 1][R | r]_hi + [V_hi | 1][R | r]_lo + V_lo R_hi
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)
+                mma_bf16(tm + Lay::T_DK, kdesc(sV, k, VSTEP), kdesc(sR, k, S_ATOM), ID_DQ, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < NE / 16; ++k)
+                mma_bf16(tm + Lay::T_DK, kdesc(sV, k, VSTEP), kdesc(sRl, k, S_ATOM), ID_DQ, 1u);
+#pragma unroll
+            for (int k = 0; k < M / 16; ++k)
+                mma_bf16(tm + Lay::T_DK, kdesc(sVl, k, VSTEP), kdesc(sR, k, S_ATOM), ID_DQ, 1u);
+            // dV = kf R: kf_hi R_hi + kf_hi R_lo + kf_lo R_hi
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                mma_bf16(tm + Lay::T_DV, kdesc(sK, k, kAtom), mdesc(sR, k, S_ATOM), ID_DV, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                mma_bf16(tm + Lay::T_DV, kdesc(sK, k, kAtom), mdesc(sRl, k, S_ATOM), ID_DV, 1u);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                mma_bf16(tm + Lay::T_DV, kdesc(sKl, k, kAtom), mdesc(sR, k, S_ATOM), ID_DV, 1u);
+            mma_commit(mma_bar);
+        }
+        wait_bar(mma_bar, mma_phase);
+        fence_after_sync();
+        {   // dK = dkf * phi'(K), dV -> fp32 staging tiles
+            float v[32], f[32];
+            tmem_ld32(tm + lane + Lay::T_DK + 32 * g, v);
+            dphi_row(sm + Lay::K, row, g, f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(sm + Lay::DK + f32_off(row, 32 * g + 4 * u)) =
+                    make_float4(v[4 * u] * f[4 * u], v[4 * u + 1] * f[4 * u + 1], v[4 * u + 2] * f[4 * u + 2],
+                                v[4 * u + 3] * f[4 * u + 3]);
+            tmem_ld32(tm + lane + Lay::T_DV + 32 * g, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(sm + Lay::DV + f32_off(row, 32 * g + 4 * u)) =
+                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+        sync_tc();
+        if (t == 0) {
+            for (int a = 0; a < 2; ++a) {
+                tma_store_3d(&tmdK, sm + Lay::DK + a * kAtom, 32 * a, c0, bh);
+                tma_store_3d(&tmdV, sm + Lay::DV + a * kAtom, 32 * a, c0, bh);
+            }
+            tma_store_commit();
+            if (c + 1 < nch) load(c0 + L);  // every input tile is consumed
+        }
+    }
+
+cleanup:  // the only early exit follows a copy wait: no copy of this CTA is in flight
+    if (t == 0) tma_store_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
+}
+
 // Spans for a grid of independent (head, span) units: fewest waves x chunks,
 // at most 8 spans per head (every read-out CTA sums all of its head's state
 // partials, so their number stays small), fewest spans on ties.
@@ -432,7 +903,75 @@ inline void nc_spans(int BH, int N, int num_sms, int* spans, int* span_len) {
     *spans = (N + *span_len - 1) / *span_len;
 }
 
+// Spans of the backward's query and key kernels: one CTA per SM.
+inline void ncb_spans(int BH, int N, int num_sms, int* spans, int* span_len) {
+    const int chunks = (N + L - 1) / L;
+    const int s = spans_for(BH, chunks, num_sms);
+    *span_len = ((chunks + s - 1) / s) * L;
+    *spans = (N + *span_len - 1) / *span_len;
+}
+
 }  // namespace tcn
+
+size_t noncausal_backward_tc_f32_scratch(int BH, int N, int num_sms) {
+    int s_spans = 1, q_spans = 1, len = 0;
+    tcn::nc_spans(BH, N, num_sms, &s_spans, &len);
+    tcn::ncb_spans(BH, N, num_sms, &q_spans, &len);
+    return plan::up256(sizeof(float) * static_cast<size_t>(BH) * s_spans * tcn::W) +
+           sizeof(float) * static_cast<size_t>(BH) * q_spans * tcn::W;
+}
+
+cudaError_t noncausal_backward_tc_f32(const LaunchCtx& c, const float* Q, const float* K,
+                                      const float* V, const float* O, const float* G, float* dQ,
+                                      float* dK, float* dV, int BH, int N) {
+    using namespace tcn;
+    auto ka = nc_state_tc_kernel;
+    auto kq = O ? ncb_query_tc_kernel<true> : ncb_query_tc_kernel<false>;
+    auto kk = ncb_key_tc_kernel;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, LayA::BYTES)) ||
+        (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, LayQ::BYTES)) ||
+        (e = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, LayK::BYTES)))
+        return e;
+    for (const void* f : {reinterpret_cast<const void*>(ka), reinterpret_cast<const void*>(kq),
+                          reinterpret_cast<const void*>(kk)})
+        if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared)))
+            return e;
+    NcParams sp;  // the state kernel's parameters (the forward's state pass)
+    sp.N = N;
+    nc_spans(BH, N, c.num_sms, &sp.spans, &sp.span_len);
+    sp.out_spans = sp.out_len = 0;
+    sp.status = c.status_word;
+    NcbParams p;
+    p.N = N;
+    p.s_spans = sp.spans;
+    ncb_spans(BH, N, c.num_sms, &p.q_spans, &p.q_len);
+    p.k_spans = p.q_spans;
+    p.k_len = p.q_len;
+    p.status = c.status_word;
+    char* ws = nullptr;
+    if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), noncausal_backward_tc_f32_scratch(BH, N, c.num_sms))))
+        return e;
+    sp.part = reinterpret_cast<float*>(ws);
+    p.spart = sp.part;
+    p.rpart = reinterpret_cast<float*>(ws + plan::up256(sizeof(float) * static_cast<size_t>(BH) * sp.spans * W));
+    do {
+        CUtensorMap mQ, mK, mV, mO, mG, mdQ, mdK, mdV;
+        if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D)) ||
+            (e = make_map_f32(&mV, V, BH, N, M)) || (e = make_map_f32(&mG, G, BH, N, M)) ||
+            (e = make_map_f32(&mO, O ? O : G, BH, N, M)) || (e = make_map_f32(&mdQ, dQ, BH, N, D)) ||
+            (e = make_map_f32(&mdK, dK, BH, N, D)) || (e = make_map_f32(&mdV, dV, BH, N, M)))
+            break;
+        ka<<<BH * sp.spans, NT, LayA::BYTES, c.stream>>>(mK, mV, sp);
+        kq<<<BH * p.q_spans, NT, LayQ::BYTES, c.stream>>>(mQ, mG, mO, mdQ, p);
+        kk<<<BH * p.k_spans, NT, LayK::BYTES, c.stream>>>(mK, mV, mdK, mdV, p);
+        note_launch(3);
+        e = cudaGetLastError();
+    } while (0);
+    scratch_free(c, ws);
+    return e;
+}
 
 size_t noncausal_forward_tc_f32_scratch(int BH, int N, int num_sms) {
     int spans = 1, len = 0;
