@@ -157,6 +157,20 @@ __device__ __forceinline__ void decay_scan(float* dec, const FwdParams& p, int h
     __syncthreads();
 }
 
+// Row `row` of atom `a` of a K-major 128-row bf16 tile, times f (rounded to
+// bf16), written to the same place in `dst` (which may be `tile`).
+__device__ __forceinline__ void scale_row_atom_to(const uint8_t* tile, uint8_t* dst, int a, int row, float f) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + a * kAtom + swz(row, c));
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = pack_bf16(__uint_as_float(w[k] << 16) * f, __uint_as_float(w[k] & 0xFFFF0000u) * f);
+        *reinterpret_cast<uint4*>(dst + a * kAtom + swz(row, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // Row `row` of a K-major 128-row bf16 tile, atom `a`, times f (rounded to bf16).
 __device__ __forceinline__ void scale_row_atom(uint8_t* tile, int a, int row, float f) {
 #pragma unroll
@@ -178,6 +192,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                      const FwdParams p) {
     using Lay = Layout<D, M, RET>;
     constexpr int DA = Lay::DA, MA = Lay::MA, NE = Lay::NE, W = Lay::W, NT = Lay::THREADS;
+    // retention at D = 64: the output staging tile takes one of the P area's two atoms, so the
+    // other holds a decayed copy of K and the state update need not wait for the P epilogue
+    constexpr bool KCOPY = RET && D == 64 && MA == 1;
     constexpr int HALF = M / Lay::GROUPS;   // columns of a state/output row per warpgroup
     constexpr int PCOLS = L / Lay::GROUPS;  // columns of P per warpgroup
     constexpr uint32_t ID_P = idesc_bf16(128, 128, false, false);
@@ -462,6 +479,21 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncthreads();
         if constexpr (RET) {
             decay_scan(dec, p, h, c0, valid);
+            if constexpr (KCOPY) {  // the decayed K rows into the spare staging atom and the state
+                                    // times 2^A now, so the update can follow P at once
+                const float A = dec[L - 1];
+                scale_row_atom_to(sm + Lay::K, sm + Lay::P + kAtom, 0, row, exp2f(A - dec[row]));
+                if (q < D / 32) {
+                    const float f = exp2f(A);
+                    for (int col = 0; col < NE; col += 16) {
+                        float v[16];
+                        tmem_ld16(tm + lane + Lay::T_S + col, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] *= f;
+                        tmem_st16(tm + lane + Lay::T_S + col, v);
+                    }
+                }
+            }
         } else {
             phi_tile<false, NT>(sm + Lay::Q, DA, valid);
             phi_tile<true, NT>(sm + Lay::K, DA, valid);
@@ -480,6 +512,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             mma_commit(mma_bar);
             if (!RET) mma_state_update(sK, sV, true);  // under the P epilogue; tracked by the next commit
+            if (KCOPY) mma_state_update(smem_u32(sm + Lay::P + kAtom), sV, true);  // decayed K copy
             tma_store_wait_read();           // the staging tile (P area) is free again
         }
         wait_bar(mma_bar, mma_phase);
@@ -519,9 +552,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const float A = dec[L - 1], ai = dec[row];
             for (int a = g; a < DA; a += Lay::GROUPS) {
                 scale_row_atom(sm + Lay::Q, a, row, exp2f(ai));
-                scale_row_atom(sm + Lay::K, a, row, exp2f(A - ai));
+                if (!KCOPY) scale_row_atom(sm + Lay::K, a, row, exp2f(A - ai));
             }
-            if (q < D / 32) {
+            if (!KCOPY && q < D / 32) {
                 const float f = exp2f(A);
                 for (int j0 = g * HALF; j0 < (g + 1) * HALF + (g == 0 ? 16 : 0); j0 += 16) {
                     const int col = j0 < (g + 1) * HALF ? j0 : M;  // then the normaliser block
@@ -538,7 +571,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncthreads();
         fence_after_sync();
         if (t == 0) {
-            if (RET) mma_state_update(sK, sV, true);  // with the decayed K rows
+            if (RET && !KCOPY) mma_state_update(sK, sV, true);  // with the decayed K rows
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)  // O_ext = phi(Q) [S | Z]
                 mma_bf16(tm + Lay::T_O, sdesc(sQ + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
