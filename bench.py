@@ -604,6 +604,76 @@ def run_reference(args):
     return out
 
 
+# Small cases for kernel profiles (ncu): inputs larger than L2 (129 MB) but a few
+# hundred MB on the device, each op run `reps` times after one warm-up call.
+PROFILE_CASES = {
+    "causal_train": "causal forward + backward, B=4 H=16 N=8192 D=M=64 bf16 (the headline step)",
+    "causal_long_small": "causal forward, B=1 H=4 N=65536 D=M=128 bf16 (the long workload's kernel, 4 heads)",
+    "noncausal_f32": "non-causal forward, B=8 H=8 N=4096 D=M=64 fp32",
+    "noncausal_f32_bwd": "non-causal backward, B=8 H=8 N=4096 D=M=64 fp32, Out given",
+    "decode": "decode step, 256 sequences x 16 heads, D=M=64, bf16 q/k/v, fp32 state",
+    "softmax_decode": "softmax KV-cache step, 64 sequences x 16 heads, D=64, 4096-position cache",
+    "retention_gated": "gated retention forward, B=4 H=16 N=8192 D=M=64 bf16",
+    "poly2": "degree-2 polynomial map, causal, B=1 H=16 N=4096 D=32 M=64 bf16",
+}
+
+
+def run_profile(case: str, reps: int):
+    """Runs one path `reps` times (after one warm-up call) for a profiler to capture."""
+    import torch
+    import linear_attention_02_gb300 as la
+    from linear_attention_02_gb300 import synth
+    torch.cuda.set_device(0)
+    dev = "cuda"
+    if case == "causal_train":
+        w = synth.WORKLOADS["causal_train_bf16"]
+        x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, with_grad=True, device=dev)
+        den = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        ck = torch.empty(la.la_causal_ckpt_floats(w.B, w.H, w.N, w.D, w.M), dtype=torch.float32, device=dev)
+
+        def f():
+            O = la.la_forward_causal(x["Q"], x["K"], x["V"], den=den, ckpt=ck)
+            la.la_backward_causal(x["Q"], x["K"], x["V"], x["G"], Out=O, Den=den, Ckpt=ck)
+    elif case == "causal_long_small":
+        x = synth.qkv(1, 4, 65536, 128, 128, "bf16", 1004, 0.5, device=dev)
+        f = lambda: la.la_forward_causal(x["Q"], x["K"], x["V"])
+    elif case in ("noncausal_f32", "noncausal_f32_bwd"):
+        w = synth.WORKLOADS["noncausal_f32"]
+        x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, with_grad=True, device=dev)
+        O = la.la_forward_noncausal(x["Q"], x["K"], x["V"])
+        if case == "noncausal_f32":
+            f = lambda: la.la_forward_noncausal(x["Q"], x["K"], x["V"], out=O)
+        else:
+            f = lambda: la.la_backward_noncausal(x["Q"], x["K"], x["V"], x["G"], Out=O)
+    elif case == "decode":
+        S = torch.randn(256, 16, 64, 64, device=dev)
+        Z = torch.rand(256, 16, 64, device=dev).add_(1.0)
+        s_ = synth.decode_step_qkv(256, 16, 64, 64, "bf16", 1005, 0, device=dev)
+        f = lambda: la.la_decode_step(s_["q"], s_["k"], s_["v"], S, Z)
+    elif case == "softmax_decode":
+        Kc = synth.randn((64, 16, 4096, 64), "bf16", 1007, device=dev)
+        Vc = synth.randn((64, 16, 4096, 64), "bf16", 1008, device=dev)
+        s_ = synth.decode_step_qkv(64, 16, 64, 64, "bf16", 1005, 0, device=dev)
+        f = lambda: la.la_softmax_decode_step(s_["q"], s_["k"], s_["v"], Kc, Vc, 4095)
+    elif case == "retention_gated":
+        w = synth.WORKLOADS["causal_train_bf16"]
+        x = synth.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.scale, device=dev)
+        gates = synth.decays((w.B, w.H, w.N), w.seed + 5, 0.85, 1.0, device=dev)
+        f = lambda: la.la_forward_retention(x["Q"], x["K"], x["V"], gates=gates)
+    elif case == "poly2":
+        x = synth.qkv(1, 16, 4096, 32, 64, "bf16", 1007, device=dev)
+        f = lambda: la.la_forward_poly2(x["Q"], x["K"], x["V"], causal=True)
+    else:
+        raise SystemExit(f"unknown profile case {case}; one of {sorted(PROFILE_CASES)}")
+    f()
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        f()
+    torch.cuda.synchronize()
+    la.la_check_device_status()
+    print(f"profile case {case}: {PROFILE_CASES[case]}, {reps} runs", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,8 +682,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-paths", action="store_true", help="headline step only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
+                    help="run one path on a small case for a profiler, print no JSON line")
+    ap.add_argument("--reps", type=int, default=2, help="runs of the --profile case")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args.profile, args.reps)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -131,17 +131,25 @@ struct FwdParams {
 // log2 of a decay, kept finite: a decay below 2^-64 counts as 2^-64.
 __device__ __forceinline__ float log2_decay(float g) { return fmaxf(log2f(g), -64.f); }
 
-// dec[i] = sum of log2(decay) over tokens c0 .. c0 + i of head h (rows past the
-// head's end add nothing).  Threads 0 .. 127 scan; every thread of the CTA
+// This thread's token (row t < 128) of the chunk at c0 of head h: its decay
+// (1 past the head's end, or for threads t >= 128).  Loaded a chunk ahead of
+// its use, so the load is not on the chunk's critical path.
+__device__ __forceinline__ float row_decay(const FwdParams& p, int h, int c0, int valid) {
+    const int t = threadIdx.x;
+    if (t >= L || t >= valid) return 1.f;
+    return p.gates ? __ldg(p.gates + static_cast<size_t>(h) * p.N + c0 + t)
+                   : (p.gamma_head ? __ldg(p.gamma_head + h % p.H) : 1.f);
+}
+
+// dec[i] = sum of log2(decay) over the chunk's tokens 0 .. i, from each row's
+// decay `gam` (row_decay).  Threads 0 .. 127 scan; every thread of the CTA
 // calls it, and it ends with the scan complete for all of them.
-__device__ __forceinline__ void decay_scan(float* dec, const FwdParams& p, int h, int c0, int valid) {
+__device__ __forceinline__ void decay_scan(float* dec, float gam) {
     const int t = threadIdx.x;
     float* wsum = dec + L;
     float l = 0.f;
     if (t < L) {
-        if (t < valid)
-            l = log2_decay(p.gates ? p.gates[static_cast<size_t>(h) * p.N + c0 + t]
-                                   : (p.gamma_head ? p.gamma_head[h % p.H] : 1.f));
+        l = log2_decay(gam);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float x = __shfl_up_sync(0xffffffffu, l, o);
@@ -251,6 +259,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // thread 0's copies issued on, and waits completed on, each copy barrier (tma_bar doubles
     // as phase 1's first K, V buffer's), so that a CTA ending early drains what is in flight
     uint32_t put0 = 0, put1 = 0, put2 = 0, got0 = 0, got1 = 0, got2 = 0;
+    float gam_next = 1.f;  // retention: this thread's row decay of the next chunk, loaded ahead
 
     auto fail = [&](unsigned code) {
         atomicOr(p.status, code);
@@ -377,6 +386,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (t == 0)
             for (int b = 0; b < KV_BUFS - 1 && b < n1; ++b) load_kv(c_last - b * L, b);
         float run = 0.f;  // retention: log2 decay of the piece's chunks already summed (the later ones)
+        if (RET) gam_next = row_decay(p, h, c_last, min(L, p.N - c_last));
         for (int i1 = 0; i1 < n1; ++i1) {
             const int c0 = c_last - i1 * L;
             const int b = i1 % KV_BUFS;
@@ -395,7 +405,9 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             if (t == 0 && i1 + KV_BUFS - 1 < n1)
                 load_kv(c0 - (KV_BUFS - 1) * L, (i1 + KV_BUFS - 1) % KV_BUFS);
             if constexpr (RET) {  // K rows decayed to the end of the piece
-                decay_scan(dec, p, h, c0, min(L, p.N - c0));
+                const float gam = gam_next;
+                if (i1 + 1 < n1) gam_next = row_decay(p, h, c0 - L, L);
+                decay_scan(dec, gam);
                 const float A = dec[L - 1];
                 const float f = exp2f(run + A - dec[row]);
                 for (int a = g; a < DA; a += Lay::GROUPS) scale_row_atom(sm + k_buf(b), a, row, f);
@@ -471,6 +483,10 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     fence_after_sync();
 
     // ------------------------------------------------- phase 2: outputs
+    if (RET) {  // the first chunk's row decay
+        const int h0 = ur.start / p.CH, c00 = (ur.start - h0 * p.CH) * L;
+        gam_next = row_decay(p, h0, c00, min(L, p.N - c00));
+    }
     for (int gc = ur.start; gc < ur.end; ++gc) {
         const int h = gc / p.CH, cc = gc - h * p.CH;
         const int c0 = cc * L;
@@ -478,7 +494,12 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (t == 0 && !mbar_wait(tma_bar, (got0++) & 1u, kWaitLimit)) fail(kErrWait);
         __syncthreads();
         if constexpr (RET) {
-            decay_scan(dec, p, h, c0, valid);
+            const float gam = gam_next;
+            if (gc + 1 < ur.end) {
+                const int hn = (gc + 1) / p.CH, cn0 = (gc + 1 - hn * p.CH) * L;
+                gam_next = row_decay(p, hn, cn0, min(L, p.N - cn0));
+            }
+            decay_scan(dec, gam);
             if constexpr (KCOPY) {  // the decayed K rows into the spare staging atom and the state
                                     // times 2^A now, so the update can follow P at once
                 const float A = dec[L - 1];
