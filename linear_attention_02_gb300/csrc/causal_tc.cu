@@ -25,12 +25,16 @@
 // one per resident CTA, so a range may end inside a head and the next range
 // continue it.  Phase 1 of a unit whose range stops inside a head accumulates
 // that last piece's aggregate (sum phi(K)^T V | sum phi(K)) and publishes it
-// with a release flag; phase 2 starts its first piece from the carried-in
-// state plus the aggregates of the earlier units of that head (bounded waits
-// on their flags), then runs the chunk loop, restarting the state at every
-// head boundary.  Units are taken from an atomic ticket after TMEM is
+// with a release flag (1).  Phase 2 starts its first piece from the sum of the
+// earlier aggregates of that head (bounded waits on their flags, walking
+// back), and runs the chunk loop,
+// restarting the state at every head boundary.  Units are taken from an atomic ticket after TMEM is
 // allocated, so a CTA only ever waits for CTAs that started (and hold their
-// TMEM) before it.
+// TMEM) before it.  With very many ranges per head (D = 64) the walk is cut short:
+// a piece that starts at its head's start also publishes the head's state at
+// its end (flag 2), and so does every unit once its look-back is done; the
+// walk stops at the first flag 2 it meets, and no unit ever waits for a
+// state, only for aggregates.
 //
 // The same kernel, instantiated with RET, runs linear attention with decay
 // ("retention", "Transformer and Variants" sections 1.3.2 and 1.3.4):
@@ -109,8 +113,11 @@ struct Layout {
 
 struct FwdParams {
     int N, BH, CH, per;    // tokens, heads, chunks per head, chunks per unit
-    float* agg;            // [units][W]
-    unsigned* flags;       // [units], zero before the launch
+    float* agg;            // [units][W] aggregate of each published piece
+    float* incl;           // [units][W] the head's state at the end of each published piece
+    int use_incl;          // publish and use those states (over 128 ranges per head, D = 64)
+    unsigned* flags;       // [units], zero before the launch: 1 = aggregate published,
+                           // 2 = inclusive state published as well
     unsigned* ticket;      // zero before the launch
     const float* S_init;   // [BH][D][M] or null
     const float* Z_init;   // [BH][D] or null
@@ -226,6 +233,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);  // [0] unit, [1] abort
     uint64_t* kv_bar1 = tma_bar + 4;  // phase 1's copies into its second and third K, V buffers
     uint64_t* kv_bar2 = tma_bar + 5;
+    volatile int* lb = reinterpret_cast<volatile int*>(tma_bar + 6);  // the look-back's result
 
     if (t == 0) {
         mbar_init(tma_bar, 1);
@@ -288,10 +296,13 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             mma_bf16(tm + Lay::T_S, sdesc(sk + 2048 * k, kAtom, 1024),
                      sdesc(sv + 2048 * k, kAtom, 1024), ID_S, (accumulate_first || k > 0) ? 1u : 0u);
     };
-    // Starting state of a segment of head h: the carried-in state plus the
-    // published aggregates of units sp0 <= sp < sp1, into TMEM and the bf16
-    // S tile (threads with q < D / 32: state row d = row).
-    auto put_state = [&](int h, int sp0, int sp1) {
+    // Starting state of a segment of head h: the published aggregates of units
+    // sp0 <= sp < sp1, on top of the inclusive state of unit sp0 - 1 when
+    // `from_incl` (else the carried-in state), into TMEM and the bf16 S tile
+    // (threads with q < D / 32: state row d = row).  With RET each term is decayed
+    // by the pieces after it.
+    auto put_state = [&](int h, int sp0, int sp1, bool from_incl) {
+        const float* base = from_incl ? p.incl + static_cast<size_t>(sp0 - 1) * W : nullptr;
         const int d = row;
         for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 16) {
             float v[16];
@@ -312,14 +323,18 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                     f *= exp2f(__ldcg(p.lam + sp));
                 }
-                if (p.S_init)
+                if (base)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = fmaf(f, __ldcg(base + d * M + j0 + i), v[i]);
+                else if (p.S_init)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         v[i] = fmaf(f, p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i], v[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    v[i] = p.S_init ? p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i] : 0.f;
+                    v[i] = base ? __ldcg(base + d * M + j0 + i)
+                                : (p.S_init ? p.S_init[(static_cast<size_t>(h) * D + d) * M + j0 + i] : 0.f);
                 for (int sp = sp0; sp < sp1; ++sp) {
                     const float4* a =
                         reinterpret_cast<const float4*>(p.agg + static_cast<size_t>(sp) * W + d * M + j0);
@@ -343,8 +358,8 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
                            pack_bf16(v[14], v[15]));
         }
-        if (g == 0) {
-            float z = p.Z_init ? p.Z_init[static_cast<size_t>(h) * D + d] : 0.f;
+        if (g == 0) {  // Z (read only without RET, where it is the normaliser state)
+            float z = base ? __ldcg(base + D * M + d) : (p.Z_init ? p.Z_init[static_cast<size_t>(h) * D + d] : 0.f);
             for (int sp = sp0; sp < sp1; ++sp) z += __ldcg(p.agg + static_cast<size_t>(sp) * W + D * M + d);
             float zv[16];
 #pragma unroll
@@ -434,8 +449,13 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
+        // a piece that starts at its head's start knows the head's state at its end now:
+        // the carried-in state (decayed by the piece) plus the aggregate
+        const bool incl_now = p.use_incl && g0 == h * p.CH;
+        const float f_in = RET ? exp2f(run) : 1.f;
         if (q < D / 32) {  // rows d < D of S_ext, this warpgroup's columns
             float* out = p.agg + static_cast<size_t>(unit) * W;
+            float* inc = p.incl + static_cast<size_t>(unit) * W;
             const int d = row;
             for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                 float v[32];
@@ -444,43 +464,101 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 for (int u = 0; u < 8; ++u)
                     reinterpret_cast<float4*>(out + d * M + j0)[u] =
                         make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                if (incl_now) {
+                    if (p.S_init) {
+                        const float* si = p.S_init + (static_cast<size_t>(h) * D + d) * M + j0;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) v[u] = fmaf(f_in, si[u], v[u]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        reinterpret_cast<float4*>(inc + d * M + j0)[u] =
+                            make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                }
             }
             if (g == 0) {
                 float z[16];
                 tmem_ld16(tm + lane + Lay::T_S + M, z);
                 out[D * M + d] = z[0];
+                if (incl_now) inc[D * M + d] = z[0] + (p.Z_init ? f_in * p.Z_init[static_cast<size_t>(h) * D + d] : 0.f);
             }
         }
         if (RET && t == 0) p.lam[unit] = run;
         __threadfence();
         fence_before_sync();
         __syncthreads();
-        if (t == 0 && unit != p.withhold) st_release(p.flags + unit, 1u);
+        if (t == 0 && unit != p.withhold) st_release(p.flags + unit, incl_now ? 2u : 1u);
     }
 
     // phase 2's first copy goes out now, under the look-back (it touches no state tile or TMEM)
     if (t == 0) load(ur.hA, (ur.start - ur.hA * p.CH) * L, true);
 
     // ------------------ look-back: starting state of the first segment
-    if (t == 0 && ur.look) {
-        for (int sp = ur.u_first; sp < unit && !sh[1]; ++sp) {
-            uint32_t n = 0;
-            while (ld_acquire(p.flags + sp) == 0u) {
-                if (++n > p.spin_limit) {
-                    fail(kErrLookback);
+    // Walks back from the unit before this one, waiting for each one's aggregate (flag 1),
+    // and stops at the first whose inclusive state is there already (flag 2), or at the
+    // head's first unit; no unit waits for an inclusive state, so a late one is never worse
+    // off than summing every earlier aggregate.
+    if (t == 0) {
+        int sp0 = unit;  // the aggregates of units sp0 .. unit - 1 are summed
+        int from_incl = 0;
+        if (ur.look) {
+            for (int sp = unit - 1; sp >= ur.u_first && !sh[1]; --sp) {
+                uint32_t n = 0;
+                unsigned fl;
+                while ((fl = ld_acquire(p.flags + sp)) == 0u) {
+                    if (++n > p.spin_limit) {
+                        fail(kErrLookback);
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+                if (fl == 2u) {
+                    sp0 = sp + 1;
+                    from_incl = 1;
                     break;
                 }
-                __nanosleep(256);
+                sp0 = sp;
             }
         }
+        lb[0] = sp0;
+        lb[1] = from_incl;
     }
     __syncthreads();
     if (sh[1]) goto cleanup;
-    if (q < D / 32) put_state(ur.hA, ur.look ? ur.u_first : unit, unit);
+    if (q < D / 32) put_state(ur.hA, lb[0], unit, lb[1] != 0);
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    // A unit that looked back and publishes a piece of the same head now knows the head's
+    // state at its end: its starting state (decayed by its piece) plus its aggregate.
+    if (p.use_incl && ur.look && ur.publish && ur.hA == ur.hB) {
+        if (q < D / 32) {
+            const float* a = p.agg + static_cast<size_t>(unit) * W;
+            float* inc = p.incl + static_cast<size_t>(unit) * W;
+            const float f = RET ? exp2f(__ldcg(p.lam + unit)) : 1.f;
+            const int d = row;
+            for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_S + j0, v);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) v[u] = fmaf(f, v[u], __ldcg(a + d * M + j0 + u));
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    reinterpret_cast<float4*>(inc + d * M + j0)[u] =
+                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
+            if (g == 0) {
+                float z[16];
+                tmem_ld16(tm + lane + Lay::T_S + M, z);
+                inc[D * M + d] = fmaf(f, z[0], __ldcg(a + D * M + d));
+            }
+        }
+        __threadfence();
+        fence_before_sync();
+        __syncthreads();
+        if (t == 0 && unit != p.withhold) st_release(p.flags + unit, 2u);
+    }
 
     // ------------------------------------------------- phase 2: outputs
     if (RET) {  // the first chunk's row decay
@@ -628,7 +706,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         p.Z_final[static_cast<size_t>(h) * D + d] = z[0];
                     }
                 }
-                if (gc + 1 < ur.end) put_state(h + 1, 0, 0);
+                if (gc + 1 < ur.end) put_state(h + 1, 0, 0, false);
             } else {  // S_c -> bf16 copy for the next chunk's O_ext (and a checkpoint)
                 float* ck = p.ckpt && (cc + 1) % kCkptChunks == 0
                                 ? p.ckpt + (static_cast<size_t>(h) * ckpt_slots(p.CH) + (cc + 1) / kCkptChunks) * W
@@ -704,7 +782,8 @@ size_t causal_forward_tc_scratch(int D, int BH, int N, int num_sms) {
     const int per_sm = D == 64 ? Layout<64, 64>::PER_SM : Layout<128, 128>::PER_SM;
     const int chunks = (N + L - 1) / L;
     const size_t units = static_cast<size_t>(plan::tc_units(BH, chunks, per_sm * num_sms));
-    return sizeof(float) * units * plan::state_words(D, D) + sizeof(unsigned) * (units + 1) + 256;
+    // aggregates and inclusive states, flags and the ticket
+    return 2 * sizeof(float) * units * plan::state_words(D, D) + sizeof(unsigned) * (units + 1) + 256;
 }
 
 size_t retention_forward_tc_scratch(int D, int BH, int N, int num_sms) {
@@ -712,8 +791,8 @@ size_t retention_forward_tc_scratch(int D, int BH, int N, int num_sms) {
     const int per_sm = D == 64 ? Layout<64, 64, true>::PER_SM : Layout<128, 128, true>::PER_SM;
     const int chunks = (N + L - 1) / L;
     const size_t units = static_cast<size_t>(plan::tc_units(BH, chunks, per_sm * num_sms));
-    // the causal forward's aggregates and flags, plus one total log2 decay per unit
-    return sizeof(float) * units * (plan::state_words(D, D) + 1) + sizeof(unsigned) * (units + 1) + 256;
+    // the causal forward's aggregates, inclusive states and flags, plus one total log2 decay per unit
+    return sizeof(float) * units * (2 * plan::state_words(D, D) + 1) + sizeof(unsigned) * (units + 1) + 256;
 }
 
 namespace tcf {
@@ -755,9 +834,15 @@ cudaError_t launch_forward(const LaunchCtx& c, const __nv_bfloat16* Q, const __n
     p.CH = chunks;
     p.per = split.per;
     p.agg = reinterpret_cast<float*>(ws);
-    p.flags = reinterpret_cast<unsigned*>(ws + agg_bytes);
+    p.incl = reinterpret_cast<float*>(ws + agg_bytes);
+    // Measured: with many ranges per head a late range's walk over every earlier aggregate
+    // dominates (one 262144-token head at D = 64, 292 ranges: 0.50 -> 0.38 ms with the end
+    // states); with 64 ranges per head the extra publication costs 3% more than it saves, and
+    // at D = 128 (66 KB end states) 4-6%.
+    p.use_incl = D == 64 && chunks / split.per > 128;
+    p.flags = reinterpret_cast<unsigned*>(ws + 2 * agg_bytes);
     p.ticket = p.flags + units;
-    p.lam = RET ? reinterpret_cast<float*>(ws + agg_bytes + flag_bytes) : nullptr;
+    p.lam = RET ? reinterpret_cast<float*>(ws + 2 * agg_bytes + flag_bytes) : nullptr;
     p.withhold = c.withhold_unit;
     p.spin_limit = c.spin_limit ? c.spin_limit : kSpinLimit;
     p.status = c.status_word;

@@ -79,6 +79,8 @@ def test_causal_forward_small(dt, shape):
     (2, 3, 129, 64, 64),      # one full chunk and a single-token tail
     (1, 4, 4096, 64, 64),
     (2, 3, 8300, 64, 64),     # several chunks per range, ranges crossing heads, ragged last chunk
+    (4, 16, 2048, 64, 64),    # four ranges per head: pieces inside heads, look-back over aggregates only
+    (1, 1, 20000, 64, 64),    # 157 one-chunk ranges in one head: the look-back stops at published head states
 ])
 def test_causal_forward_bf16_span_shapes(shape):
     la = _la()

@@ -123,7 +123,7 @@ def test_retention_rejects_both_decays():
 # another, or stop inside a head (its aggregate then carries the piece's total decay)
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("shape", [(8, 40, 300, 64, 64), (1, 2, 5000, 128, 128), (2, 3, 8300, 64, 64),
-                                   (1, 1, 128, 64, 64), (2, 3, 129, 64, 64)])
+                                   (1, 1, 128, 64, 64), (2, 3, 129, 64, 64), (1, 1, 20000, 64, 64)])
 def test_retention_tensor_core_ranges(kind, shape):
     la = _la()
     B, H, N, D, M = shape

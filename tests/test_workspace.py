@@ -22,10 +22,11 @@ def _ws(op, B, H, N, D, M, dt, saved=0, sms=152):
 def test_training_forward_bytes():
     # bf16 D = M = 64: two CTAs per SM -> 304 slots; 64 heads x 64 chunks = 4096
     # chunks cut into ranges of ceil(4096 / 304) = 14 -> 293 units; each unit
-    # publishes one (S | Z) state of 64*64 + 64 floats, plus one flag per unit
-    # and the ticket, plus 256 bytes of slack.
+    # publishes two (S | Z) states of 64*64 + 64 floats (its piece's aggregate and the
+    # head's state at the piece's end), plus one flag per unit and the ticket, plus
+    # 256 bytes of slack.
     units = 293
-    want = 4 * units * (64 * 64 + 64) + 4 * (units + 1) + 256
+    want = 2 * 4 * units * (64 * 64 + 64) + 4 * (units + 1) + 256
     assert _ws("la_forward_causal", 4, 16, 8192, 64, 64, BF16) == want
 
 
