@@ -21,7 +21,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "liblinattn.so")
 
 SOURCES = ["la_api.cu", "ffma_f32.cu", "ffma_bf16.cu", "ncbwd_ffma.cu", "ret_ffma.cu", "poly_ffma.cu", "decode.cu", "softmax_decode.cu", "noalloc.cu",
-           "causal_tc.cu", "causal_bwd_tc.cu", "noncausal_tc.cu", "selftest.cu"]
+           "causal_tc.cu", "causal_bwd_tc.cu", "noncausal_tc.cu", "poly_tc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

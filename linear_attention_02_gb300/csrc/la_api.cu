@@ -293,8 +293,10 @@ size_t workspace_for(const char* op, int BH, int N, int D, int M, la_dtype dt, u
     if (!strcmp(op, "la_backward_noncausal"))
         return !bf16 && D == 64 && M == 64 ? noncausal_backward_tc_f32_scratch(BH, N, sms)
                                            : plan::ffma_noncausal_backward(BH, N, D, M, sms);
-    if (!strcmp(op, "la_forward_poly2"))
-        return D == 32 && (M == 32 || M == 64) ? plan::poly2_scratch(BH, N, M, sms) : SIZE_MAX;
+    if (!strcmp(op, "la_forward_poly2")) {
+        if (D != 32 || (M != 32 && M != 64)) return SIZE_MAX;
+        return bf16 && M == 64 ? plan::poly2_tc_scratch(BH, N) : plan::poly2_scratch(BH, N, M, sms);
+    }
     if (!strcmp(op, "la_forward_retention"))
         return bf16 && D == M && (D == 64 || D == 128) ? retention_forward_tc_scratch(D, BH, N, sms)
                                                        : plan::ffma_retention_forward(BH, N, D, M, sms);
@@ -530,8 +532,8 @@ la_status la_forward_poly2(const void* Q, const void* K, const void* V, void* Ou
     else
         e = M == 32 ? poly2_forward<__nv_bfloat16, 32>(ctx, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
                                                        (const __nv_bfloat16*)V, (__nv_bfloat16*)Out, BH, N, c)
-                    : poly2_forward<__nv_bfloat16, 64>(ctx, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
-                                                       (const __nv_bfloat16*)V, (__nv_bfloat16*)Out, BH, N, c);
+                    : poly2_forward_tc(ctx, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
+                                       (const __nv_bfloat16*)V, (__nv_bfloat16*)Out, BH, N, c);
     return finish(e, fn);
 }
 

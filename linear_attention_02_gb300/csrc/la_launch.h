@@ -122,6 +122,10 @@ template <typename T, int M>
 cudaError_t poly2_forward(const LaunchCtx& c, const T* Q, const T* K, const T* V, T* O, int BH,
                           int N, bool causal);
 
+// The same on the tensor core for bf16 storage and M = 64 (D^2 = 1024 features).
+cudaError_t poly2_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                             const __nv_bfloat16* V, __nv_bfloat16* O, int BH, int N, bool causal);
+
 template <typename T, int D, int M>
 cudaError_t decode_step(const LaunchCtx& c, const T* q, const T* k, const T* v, float* S,
                         float* Z, float* out, int BH);

@@ -109,6 +109,14 @@ inline size_t poly2_scratch(int BH, int N, int M, int num_sms) {
     return up256(agg) + sizeof(float) * static_cast<size_t>(BH) * N * (M + 1);
 }
 
+// Tensor-core degree-2 map (bf16, D = 32, M = 64): four CTAs per head, each
+// owning two 128-feature slices of the D^2 = 1024 features; the only scratch is
+// the fp32 [numerator | normaliser | 15 copies] accumulator [BH][N][M + 16].
+constexpr int kPolyTcGroups = 4;
+inline size_t poly2_tc_scratch(int BH, int N) {
+    return sizeof(float) * static_cast<size_t>(BH) * N * (64 + 16);
+}
+
 // Tensor-core causal kernels: the chunks of all heads cut into equal ranges,
 // one per resident CTA (see tc_common.cuh, split_chunks).
 inline int tc_units(int BH, int chunks_per_head, int slots) {

@@ -41,6 +41,22 @@ def test_poly2_small(causal, dt, shape):
     assert rel_err(O, ref) <= TOL[dt]
 
 
+# bf16 with M = 64 runs the tensor-core kernel: four CTAs per head, each owning two
+# 128-feature slices of the D^2 = 1024 features, partial rows added into an fp32
+# accumulator; one token, a chunk and one token, ragged multi-chunk heads
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 32, 64), (1, 1, 129, 32, 64), (2, 3, 300, 32, 64),
+                                   (1, 2, 2049, 32, 64)])
+def test_poly2_tensor_core(causal, shape):
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=150 + N)
+    O = la.la_forward_poly2(x["Q"].cuda(), x["K"].cuda(), x["V"].cuda(), causal=causal)
+    la.la_check_device_status()
+    ref = oracle.poly_forward_state(x["Q"], x["K"], x["V"], causal)
+    assert rel_err(O, ref) <= TOL["bf16"]
+
+
 def test_poly2_full_bf16():
     # B=4 H=16 N=4096 D=32 M=64, bf16: two heads against the oracle, every head's
     # rows inside the convex hull of the values it sees

@@ -61,6 +61,15 @@ def test_cuda_core_paths_bytes():
     assert _ws("la_forward_causal", 1, 400, 256, 32, 32, F32) == 0
 
 
+def test_poly2_bytes():
+    # bf16, M = 64: the tensor-core path's fp32 [numerator | normaliser | 15 copies]
+    # accumulator, 80 floats per token and head
+    assert _ws("la_forward_poly2", 4, 16, 4096, 32, 64, BF16) == 4 * 64 * 4096 * 80
+    # other shapes on the CUDA cores: span aggregates of the 528 features and the accumulator
+    assert _ws("la_forward_poly2", 1, 2, 1000, 32, 32, F32) > 0
+    assert _ws("la_forward_poly2", 1, 2, 1000, 64, 64, BF16) == _native.SIZE_MAX
+
+
 def test_bad_queries():
     lib = _native.lib
     assert _ws("la_forward_sideways", 1, 1, 8, 64, 64, F32) == _native.SIZE_MAX
