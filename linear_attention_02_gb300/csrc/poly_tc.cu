@@ -130,13 +130,15 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
     }
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);  // the chunk's copies
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);  // the chunk's Q, K copies
     uint64_t* p_bar = tma_bar + 1;                                     // P = Q K^T
     uint64_t* a_bar = tma_bar + 2;  // a slice's products (the second: and P [V | 1])
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tma_bar + 4);
+    uint64_t* v_bar = tma_bar + 5;  // the chunk's V copy
     if (t == 0) {
         mbar_init(tma_bar, 1);
+        mbar_init(v_bar, 1);
         mbar_init(p_bar, 1);
         mbar_init(a_bar, 1);
         fence_mbar_init();
@@ -182,7 +184,7 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     constexpr uint32_t LBO_V = Lay::EXT + 64 - Lay::V;
     const bool intra = p.causal && grp == 0;
     uint32_t p_phase = 0, a_phase = 0;
-    uint32_t put = 0, got = 0;  // thread 0: copies issued and waited for, drained at exit
+    uint32_t put = 0, got = 0, put_v = 0, got_v = 0;  // thread 0: copies issued and waited for
 
     auto fail = [&](unsigned code) {
         atomicOr(p.status, code);
@@ -194,12 +196,18 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         __syncthreads();
         phase ^= 1u;
     };
-    auto load = [&](int c0, bool wq, bool wk, bool wv) {  // thread 0 only
+    // Q and K go out as soon as every thread has read its rows of the chunk before, V once
+    // the chunk before has taken its last product (thread 0 only).
+    auto load_qk = [&](int c0, bool wq, bool wk) {
         ++put;
-        mbar_arrive_expect_tx(tma_bar, (wq ? 8192u : 0u) + (wk ? 8192u : 0u) + (wv ? kAtom : 0u));
+        mbar_arrive_expect_tx(tma_bar, (wq ? 8192u : 0u) + (wk ? 8192u : 0u));
         if (wq) tma_load_3d(sm + Lay::QR, &tmQ, tma_bar, 0, c0, bh);
         if (wk) tma_load_3d(sm + Lay::KR, &tmK, tma_bar, 0, c0, bh);
-        if (wv) tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0, bh);
+    };
+    auto load_v = [&](int c0) {
+        ++put_v;
+        mbar_arrive_expect_tx(v_bar, kAtom);
+        tma_load_3d(sm + Lay::V, &tmV, v_bar, 0, c0, bh);
     };
     // Row t of phi(X) for slice j of this CTA into the tile at `tile`: feature 32 al + b of
     // the slice is x_a x_b with a = 8 grp + 4 j + al (xa holds x_{8 grp} .. x_{8 grp + 7}).
@@ -230,10 +238,9 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         xa[2] = a.z;
         xa[3] = a.w;
     };
-    // The two slices' S (row t = feature) and Z as hi and lo bf16 terms, for the next read-out.
-    auto copy_state = [&]() {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
+    // S (row t = feature) and Z of slice j as hi and lo bf16 terms, for the next read-out.
+    auto copy_slice = [&](int j) {
+        {
             const uint32_t ts = tm + lane + (j ? Lay::T_S1 : Lay::T_S0);
 #pragma unroll
             for (int j0 = 0; j0 < M; j0 += 32) {
@@ -268,7 +275,10 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const bool do_state = p.causal || pass == 0;  // state updates
         const bool do_out = p.causal || pass == 1;    // read-outs
         const bool need_k = do_state || intra, need_v = do_state || intra;
-        if (t == 0) load(0, do_out, need_k, need_v);
+        if (t == 0) {
+            load_qk(0, do_out, need_k);
+            if (need_v) load_v(0);
+        }
         for (int c = 0; c < p.CH; ++c) {
             const int c0 = c * L;
             if (t == 0) {
@@ -292,6 +302,7 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             fence_after_sync();
             if (*abort_flag) goto cleanup;
             if (t == 0) {
+                if (c + 1 < p.CH) load_qk(c0 + L, do_out, need_k);  // every row is read
                 if (intra) {  // P = Q K^T over the 32 real columns
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k)
@@ -306,6 +317,10 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         mma_bf16(tm + Lay::T_O, a, sdesc(sS[0] + 2048 * k, lbo_s[0], 1024), ID_O, k > 0 ? 1u : 0u);
                         mma_bf16(tm + Lay::T_O, a, sdesc(sS[1] + 2048 * k, lbo_s[1], 1024), ID_O, 1u);
                     }
+                if (need_v) {  // V lands under the products above
+                    if (!mbar_wait(v_bar, got_v & 1u, kWaitLimit)) fail(kErrWait);
+                    ++got_v;
+                }
                 if (do_state)
 #pragma unroll
                     for (int k = 0; k < L / 16; ++k)
@@ -344,7 +359,7 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             fence_before_sync();
             __syncthreads();
             fence_after_sync();
-            if (t == 0) {
+            if (t == 0) {  // the second slice (its products touch none of the first slice's tiles)
                 if (do_out)
 #pragma unroll
                     for (int k = 0; k < FS / 16; ++k) {
@@ -364,10 +379,10 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                                     ID_O, 1u);
                 mma_commit(a_bar);
             }
+            if (p.causal) copy_slice(0);  // the first slice's state is final: copied under these products
             wait_bar(a_bar, a_phase);  // every product of the chunk: its input tiles are free
             fence_after_sync();
-            if (t == 0 && c + 1 < p.CH) load(c0 + L, do_out, need_k, need_v);
-            if (p.causal) copy_state();
+            if (t == 0 && need_v && c + 1 < p.CH) load_v(c0 + L);
             if (do_out) {  // the partial [numerator | normaliser] rows, added into the accumulator
                 float* row = reinterpret_cast<float*>(sm + Lay::STG) + NE * t;
 #pragma unroll
@@ -394,9 +409,11 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 tma_reduce_add_3d(&tmAcc, sm + Lay::STG, 0, c0, bh);
                 tma_store_commit();
             }
+            if (p.causal) copy_slice(1);  // while the reduce reads the staged rows out
         }
         if (!p.causal && pass == 0) {  // the totals, for the read-out pass
-            copy_state();
+            copy_slice(0);
+            copy_slice(1);
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
@@ -407,6 +424,7 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 cleanup:
     if (t == 0) {  // copies and reductions still in flight land before the CTA leaves
         for (; got < put; ++got) mbar_wait(tma_bar, got & 1u, kWaitLimit);
+        for (; got_v < put_v; ++got_v) mbar_wait(v_bar, got_v & 1u, kWaitLimit);
         tma_store_wait_all();
     }
     fence_before_sync();
