@@ -664,7 +664,7 @@ PROFILE_CASES = {
     "decode": "decode step, 256 sequences x 16 heads, D=M=64, bf16 q/k/v, fp32 state",
     "softmax_decode": "softmax KV-cache step, 64 sequences x 16 heads, D=64, 4096-position cache",
     "retention_gated": "gated retention forward, B=4 H=16 N=8192 D=M=64 bf16",
-    "poly2": "degree-2 polynomial map, causal, B=1 H=16 N=4096 D=32 M=64 bf16",
+    "poly2": "degree-2 polynomial map, causal, B=4 H=16 N=4096 D=32 M=64 bf16 (the bench workload)",
 }
 
 
@@ -711,7 +711,7 @@ def run_profile(case: str, reps: int):
         gates = synth.decays((w.B, w.H, w.N), w.seed + 5, 0.85, 1.0, device=dev)
         f = lambda: la.la_forward_retention(x["Q"], x["K"], x["V"], gates=gates)
     elif case == "poly2":
-        x = synth.qkv(1, 16, 4096, 32, 64, "bf16", 1007, device=dev)
+        x = synth.qkv(4, 16, 4096, 32, 64, "bf16", 1007, device=dev)
         f = lambda: la.la_forward_poly2(x["Q"], x["K"], x["V"], causal=True)
     else:
         raise SystemExit(f"unknown profile case {case}; one of {sorted(PROFILE_CASES)}")
