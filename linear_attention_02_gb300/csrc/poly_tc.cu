@@ -60,7 +60,7 @@ static_assert(plan::kPolyTcGroups * 2 * FS == D * D, "two slices per CTA cover t
 // after the S tiles and V.  The fp32 partial rows are staged over the phi
 // tiles, which are idle from the chunk's last product to the next chunk.
 struct Lay {
-    static constexpr uint32_t QR = 0;               // raw Q rows [128][32] bf16, no swizzle
+    static constexpr uint32_t QR = 0;               // raw Q rows [128][32] bf16, 64-byte swizzle
     static constexpr uint32_t KR = QR + 8192;       // raw K rows
     static constexpr uint32_t S0 = KR + 8192;       // hi term of S, first slice [128 features][64]
     static constexpr uint32_t S1 = S0 + kAtom;      // of the second
@@ -73,12 +73,12 @@ struct Lay {
     static constexpr uint32_t FK = FQ + 2 * kAtom;  // phi(K) of a slice
     static constexpr uint32_t QP = FK + 2 * kAtom;  // Q, K rows padded to 64 columns (P = Q K^T)
     static constexpr uint32_t KP = QP + kAtom;
-    static constexpr uint32_t STG = FQ;             // fp32 [128][NE] partial rows, dense
+    static constexpr uint32_t STG = FQ;  // fp32 partial rows: three [128][32] boxes, 128-byte swizzle
     static constexpr uint32_t BARS = KP + kAtom;
     static constexpr uint32_t BYTES = BARS + 64;
     // tensor memory: S of the two slices, O_ext, P (packed in place to its first 64 columns)
     static constexpr uint32_t T_S0 = 0, T_S1 = NE, T_O = 2 * NE, T_P = 256, T_COLS = 512;
-    static_assert(STG + L * NE * 4 <= QP && BYTES <= 227 * 1024, "shared memory");
+    static_assert(STG + 3 * kAtom <= QP && BYTES <= 227 * 1024, "shared memory");
     static_assert(T_O + NE <= T_P && T_P + L <= T_COLS, "tensor memory");
 };
 
@@ -90,6 +90,9 @@ struct PolyParams {
 
 // 16-byte chunk c (0 .. 7) of row `row` of the EXT atom, swizzled.
 __device__ __forceinline__ uint32_t ext_off(int row, int c) { return Lay::EXT + swz(row, c); }
+
+// 16-byte chunk c (0 .. 3) of row `row` of a [128][32] bf16 tile with the 64-byte swizzle.
+__device__ __forceinline__ uint32_t swz64(int row, int c) { return row * 64 + ((c ^ ((row >> 1) & 3)) << 4); }
 
 // TMA bulk reduce-add of an fp32 box into global memory (completion: bulk group).
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y,
@@ -223,16 +226,15 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
     };
     auto read_row = [&](uint32_t off, uint32_t (&x2)[16], uint32_t (&xa)[4]) {
-        const uint4* r = reinterpret_cast<const uint4*>(sm + off + 64 * t);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint4 u = r[c];
+            const uint4 u = *reinterpret_cast<const uint4*>(sm + off + swz64(t, c));
             x2[4 * c] = u.x;
             x2[4 * c + 1] = u.y;
             x2[4 * c + 2] = u.z;
             x2[4 * c + 3] = u.w;
         }
-        const uint4 a = r[grp];
+        const uint4 a = *reinterpret_cast<const uint4*>(sm + off + swz64(t, grp));
         xa[0] = a.x;
         xa[1] = a.y;
         xa[2] = a.z;
@@ -383,30 +385,32 @@ poly_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             wait_bar(a_bar, a_phase);  // every product of the chunk: its input tiles are free
             fence_after_sync();
             if (t == 0 && need_v && c + 1 < p.CH) load_v(c0 + L);
-            if (do_out) {  // the partial [numerator | normaliser] rows, added into the accumulator
-                float* row = reinterpret_cast<float*>(sm + Lay::STG) + NE * t;
+            if (do_out) {  // the partial [numerator | normaliser] rows, added into the accumulator:
+                           // columns 32b .. 32b + 31 in box b (box 2: the normaliser block, the
+                           // columns past 80 fall outside the accumulator and are not added)
 #pragma unroll
-                for (int j0 = 0; j0 < M; j0 += 32) {
+                for (int b = 0; b < 2; ++b) {
                     float v[32];
-                    tmem_ld32(tm + lane + Lay::T_O + j0, v);
+                    tmem_ld32(tm + lane + Lay::T_O + 32 * b, v);
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        reinterpret_cast<float4*>(row + j0)[u] =
+                        *reinterpret_cast<float4*>(sm + Lay::STG + b * kAtom + swz(t, u)) =
                             make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
                 }
                 float d[16];
                 tmem_ld16(tm + lane + Lay::T_O + M, d);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    reinterpret_cast<float4*>(row + M)[u] = make_float4(d[4 * u], d[4 * u + 1], d[4 * u + 2],
-                                                                        d[4 * u + 3]);
+                    *reinterpret_cast<float4*>(sm + Lay::STG + 2 * kAtom + swz(t, u)) =
+                        make_float4(d[4 * u], d[4 * u + 1], d[4 * u + 2], d[4 * u + 3]);
             }
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
             fence_after_sync();
             if (do_out && t == 0) {
-                tma_reduce_add_3d(&tmAcc, sm + Lay::STG, 0, c0, bh);
+#pragma unroll
+                for (int b = 0; b < 3; ++b) tma_reduce_add_3d(&tmAcc, sm + Lay::STG + b * kAtom, 32 * b, c0, bh);
                 tma_store_commit();
             }
             if (p.causal) copy_slice(1);  // while the reduce reads the staged rows out
@@ -476,10 +480,9 @@ cudaError_t poly2_forward_tc(const LaunchCtx& c, const __nv_bfloat16* Q, const _
     if (e != cudaSuccess) return e;
     do {
         CUtensorMap mQ, mK, mV, mA;
-        if ((e = make_map_box(&mQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-            (e = make_map_box(&mK, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, D, D, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-            (e = tcf::make_map(&mV, V, BH, N, M)) ||
-            (e = make_map_box(&mA, acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, NE, NE, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        if ((e = make_map_box(&mQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, D, D, CU_TENSOR_MAP_SWIZZLE_64B)) ||
+            (e = make_map_box(&mK, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, D, D, CU_TENSOR_MAP_SWIZZLE_64B)) ||
+            (e = tcf::make_map(&mV, V, BH, N, M)) || (e = tcf::make_map_f32(&mA, acc, BH, N, NE)))
             break;
         if ((e = cudaMemsetAsync(acc, 0, bytes, c.stream)) != cudaSuccess) break;
         if ((e = cudaFuncSetAttribute(poly_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES)))
