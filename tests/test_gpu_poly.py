@@ -57,6 +57,19 @@ def test_poly2_tensor_core(causal, shape):
     assert rel_err(O, ref) <= TOL["bf16"]
 
 
+# inputs off centre and scaled (q, k ~ N(-1, 2^2)): features x_a x_b of either sign and a
+# wide range, normalisers far from 1
+@pytest.mark.parametrize("causal", [True, False])
+def test_poly2_tensor_core_wide_inputs(causal):
+    la = _la()
+    B, H, N, D, M = 1, 2, 700, 32, 64
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=157, scale=2.0, qk_mean=-1.0)
+    O = la.la_forward_poly2(x["Q"].cuda(), x["K"].cuda(), x["V"].cuda(), causal=causal)
+    la.la_check_device_status()
+    ref = oracle.poly_forward_state(x["Q"], x["K"], x["V"], causal)
+    assert rel_err(O, ref) <= TOL["bf16"]
+
+
 def test_poly2_full_bf16():
     # B=4 H=16 N=4096 D=32 M=64, bf16: two heads against the oracle, every head's
     # rows inside the convex hull of the values it sees
