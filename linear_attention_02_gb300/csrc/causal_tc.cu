@@ -138,6 +138,12 @@ struct FwdParams {
 // log2 of a decay, kept finite: a decay below 2^-64 counts as 2^-64.
 __device__ __forceinline__ float log2_decay(float g) { return fmaxf(log2f(g), -64.f); }
 
+// A chunk whose total log2 decay A is at least this has its decays factored into its rows:
+// Q row i times 2^(a_i), K row j times 2^(-a_j) <= 2^100 (inside the range of bf16), so that
+// P = Q K^T comes out as P_ij 2^(a_i - a_j) and the update S += K^T [V | 1] is scaled by 2^A
+// afterwards.  A chunk with a stronger decay takes P's decay element by element.
+constexpr float kFactorMin = -100.f;
+
 // This thread's token (row t < 128) of the chunk at c0 of head h: its decay
 // (1 past the head's end, or for threads t >= 128).  Loaded a chunk ahead of
 // its use, so the load is not on the chunk's critical path.
@@ -268,6 +274,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // as phase 1's first K, V buffer's), so that a CTA ending early drains what is in flight
     uint32_t put0 = 0, put1 = 0, put2 = 0, got0 = 0, got1 = 0, got2 = 0;
     float gam_next = 1.f;  // retention: this thread's row decay of the next chunk, loaded ahead
+    bool fact = false;     // retention: the chunk's decays factor into its Q and K rows
 
     auto fail = [&](unsigned code) {
         atomicOr(p.status, code);
@@ -578,8 +585,15 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 gam_next = row_decay(p, hn, cn0, min(L, p.N - cn0));
             }
             decay_scan(dec, gam);
-            if constexpr (KCOPY) {  // the decayed K rows into the spare staging atom and the state
-                                    // times 2^A now, so the update can follow P at once
+            fact = dec[L - 1] >= kFactorMin;
+            if (fact) {  // Q rows by 2^(a_i), K rows by 2^(-a_i): P comes out decayed
+                const float ai = dec[row];
+                for (int a = g; a < DA; a += Lay::GROUPS) {
+                    scale_row_atom(sm + Lay::Q, a, row, exp2f(ai));
+                    scale_row_atom(sm + Lay::K, a, row, exp2f(-ai));
+                }
+            } else if constexpr (KCOPY) {  // the decayed K rows into the spare staging atom and the
+                                           // state times 2^A now, so the update can follow P at once
                 const float A = dec[L - 1];
                 scale_row_atom_to(sm + Lay::K, sm + Lay::P + kAtom, 0, row, exp2f(A - dec[row]));
                 if (q < D / 32) {
@@ -610,8 +624,8 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                          k > 0 ? 1u : 0u);
             }
             mma_commit(mma_bar);
-            if (!RET) mma_state_update(sK, sV, true);  // under the P epilogue; tracked by the next commit
-            if (KCOPY) mma_state_update(smem_u32(sm + Lay::P + kAtom), sV, true);  // decayed K copy
+            if (!RET || fact) mma_state_update(sK, sV, true);  // under the P epilogue; tracked by the next commit
+            else if (KCOPY) mma_state_update(smem_u32(sm + Lay::P + kAtom), sV, true);  // decayed K copy
             tma_store_wait_read();           // the staging tile (P area) is free again
         }
         wait_bar(mma_bar, mma_phase);
@@ -628,7 +642,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 } else {
                     float v[64];
                     tmem_ld64(tm + lane + Lay::T_P + j0, v);
-                    if constexpr (RET) {  // decay 2^(a_i - a_j) of key j seen from query i
+                    if (RET && !fact) {  // decay 2^(a_i - a_j) of key j seen from query i
                         const float ai = dec[row];
 #pragma unroll
                         for (int u = 0; u < 32; ++u) {
@@ -647,7 +661,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 tmem_st32u(tm + lane + Lay::T_P + g * PCOLS + 32 * jb, pk);
             }
         }
-        if constexpr (RET) {  // P is taken: Q rows by 2^(a_i), K rows by 2^(A - a_j), the state by 2^A
+        if (RET && !fact) {  // P is taken: Q rows by 2^(a_i), K rows by 2^(A - a_j), the state by 2^A
             const float A = dec[L - 1], ai = dec[row];
             for (int a = g; a < DA; a += Lay::GROUPS) {
                 scale_row_atom(sm + Lay::Q, a, row, exp2f(ai));
@@ -670,7 +684,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         __syncthreads();
         fence_after_sync();
         if (t == 0) {
-            if (RET && !KCOPY) mma_state_update(sK, sV, true);  // with the decayed K rows
+            if (RET && !KCOPY && !fact) mma_state_update(sK, sV, true);  // with the decayed K rows
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)  // O_ext = phi(Q) [S | Z]
                 mma_bf16(tm + Lay::T_O, sdesc(sQ + (k >> 2) * kAtom + 32 * (k & 3), 16, 1024),
@@ -689,12 +703,31 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         if (q < D / 32) {
             const int d = row;
+            // factored decays: the state in TMEM is S_{c-1} + (K rows by 2^(-a))^T [V | 1], the
+            // chunk's state 2^A times that; scaled as it is read, and written back for the next chunk
+            const float fA = RET && fact ? exp2f(dec[L - 1]) : 1.f;
+            auto state32 = [&](int j0, float (&v)[32], bool write_back) {
+                tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                if (RET && fact) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) v[u] *= fA;
+                    if (write_back) tmem_st32u(tm + lane + Lay::T_S + j0, reinterpret_cast<const uint32_t(&)[32]>(v));
+                }
+            };
+            auto state_z = [&](float (&z)[16], bool write_back) {
+                tmem_ld16(tm + lane + Lay::T_S + M, z);
+                if (RET && fact) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) z[u] *= fA;
+                    if (write_back) tmem_st16(tm + lane + Lay::T_S + M, z);
+                }
+            };
             if (cc == p.CH - 1) {  // the head ends here: its final state, then the next head's start
                 if (p.S_final) {
                     float* so = p.S_final + (static_cast<size_t>(h) * D + d) * M;
                     for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                         float v[32];
-                        tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                        state32(j0, v, false);
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
                             reinterpret_cast<float4*>(so + j0)[u] =
@@ -702,7 +735,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     }
                     if (g == 0 && p.Z_final) {
                         float z[16];
-                        tmem_ld16(tm + lane + Lay::T_S + M, z);
+                        state_z(z, false);
                         p.Z_final[static_cast<size_t>(h) * D + d] = z[0];
                     }
                 }
@@ -713,7 +746,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                 : nullptr;
                 for (int j0 = g * HALF; j0 < (g + 1) * HALF; j0 += 32) {
                     float v[32];
-                    tmem_ld32(tm + lane + Lay::T_S + j0, v);
+                    state32(j0, v, true);
                     if (ck) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
@@ -727,7 +760,7 @@ causal_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 }
                 if (g == 0) {
                     float z[16];
-                    tmem_ld16(tm + lane + Lay::T_S + M, z);
+                    state_z(z, true);
                     if (ck) ck[D * M + d] = z[0];
                     uint32_t zk[8];
 #pragma unroll

@@ -144,3 +144,26 @@ def test_retention_tensor_core_ranges(kind, shape):
     Ro, Rs = oracle.retention_forward_recurrent(*hs, S0=S0.reshape(B * H, D, M)[idx][None], **okw)
     assert rel_err(O.reshape(B * H, N, M)[idx], Ro[0]) <= TOL["bf16"]
     assert rel_err(S.reshape(B * H, D, M)[idx], Rs[0]) <= TOL["bf16"]
+
+
+# Chunks whose total log2 decay is at least -100 fold their decays into the Q and K rows
+# (P comes out decayed); stronger ones take P's decay element by element.  Gates in
+# [0.25, 1) put about half the chunks on each side of that line; gates near 1e-25
+# are clamped to 2^-64 per token, far past it.
+@pytest.mark.parametrize("gate_range", [(0.25, 1.0), (1e-30, 1e-20)])
+@pytest.mark.parametrize("shape", [(2, 3, 2049, 64, 64), (1, 2, 1000, 128, 128)])
+def test_retention_tensor_core_strong_decays(gate_range, shape):
+    la = _la()
+    B, H, N, D, M = shape
+    x = synth.qkv(B, H, N, D, M, "bf16", seed=160 + N)
+    gates = synth.decays((B, H, N), 161, *gate_range)
+    S0 = torch.randn(B, H, D, M) * 0.1
+    O, S = la.la_forward_retention(x["Q"].cuda(), x["K"].cuda(), x["V"].cuda(), gates=gates.cuda(),
+                                   S_init=S0.cuda(), return_state=True)
+    la.la_check_device_status()
+    idx = list(range(min(B * H, 4)))
+    hs = [x[n].reshape(B * H, N, -1)[idx][None] for n in ("Q", "K", "V")]
+    Ro, Rs = oracle.retention_forward_recurrent(*hs, S0=S0.reshape(B * H, D, M)[idx][None],
+                                                gates=gates.reshape(B * H, N)[idx][None])
+    assert rel_err(O.reshape(B * H, N, M)[idx], Ro[0]) <= TOL["bf16"]
+    assert rel_err(S.reshape(B * H, D, M)[idx], Rs[0]) <= TOL["bf16"]
