@@ -73,6 +73,13 @@ __device__ __forceinline__ uint32_t f32_off(int r, int c) {
     return (c >> 5) * kAtom + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4;
 }
 
+// Two values at once: hi = their bf16 pair (one rounding convert), lo = the bf16 pair of
+// x - hi (hi unpacked by shift and mask); the same bits as split_bf16 on each.
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(x0, x1);
+    lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
     hi = __bfloat162float(h);
@@ -116,11 +123,7 @@ __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
                 v1 = phi_fast(v1);
             }
             if (ZERO_TAIL && r >= valid) v0 = v1 = 0.f;
-            float h0, l0, h1, l1;
-            split_bf16(v0, h0, l0);
-            split_bf16(v1, h1, l1);
-            h[u] = pack_bf16(h0, h1);
-            l[u] = pack_bf16(l0, l1);
+            split_pair(v0, v1, h[u], l[u]);
         }
         *reinterpret_cast<uint4*>(buf + swz(r, j)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(buf + kAtom + swz(r, j)) = make_uint4(l[0], l[1], l[2], l[3]);
@@ -327,13 +330,7 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             }
             uint32_t h[4], l[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float h0, l0, h1, l1;
-                split_bf16(v[2 * u], h0, l0);
-                split_bf16(v[2 * u + 1], h1, l1);
-                h[u] = pack_bf16(h0, h1);
-                l[u] = pack_bf16(l0, l1);
-            }
+            for (int u = 0; u < 4; ++u) split_pair(v[2 * u], v[2 * u + 1], h[u], l[u]);
             *reinterpret_cast<uint4*>(sm + Lay::S + swz(d, j0 >> 3)) = make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4*>(sm + Lay::S + 2 * S_ATOM + swz(d, j0 >> 3)) =
                 make_uint4(l[0], l[1], l[2], l[3]);
@@ -491,13 +488,7 @@ __device__ __forceinline__ void put_state_row(uint8_t* hi, uint8_t* lo, int d, i
     for (int c = 0; c < 4; ++c) {
         uint32_t h[4], l[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float h0, l0, h1, l1;
-            split_bf16(v[8 * c + 2 * u], h0, l0);
-            split_bf16(v[8 * c + 2 * u + 1], h1, l1);
-            h[u] = pack_bf16(h0, h1);
-            l[u] = pack_bf16(l0, l1);
-        }
+        for (int u = 0; u < 4; ++u) split_pair(v[8 * c + 2 * u], v[8 * c + 2 * u + 1], h[u], l[u]);
         *reinterpret_cast<uint4*>(hi + swz(d, 4 * g + c)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(lo + swz(d, 4 * g + c)) = make_uint4(l[0], l[1], l[2], l[3]);
     }
