@@ -90,13 +90,13 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
 // (buf + 16 KB), each one K-major 128-row atom; phi is applied first when PHI,
 // and rows >= valid become 0 when ZERO_TAIL.  Each thread reads its
 // (row, 8-column) groups before any thread writes.
-template <bool PHI, bool ZERO_TAIL>
+template <bool PHI, bool ZERO_TAIL, int NTH = NT>
 __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
-    constexpr int IT = 1024 / NT;  // (row, 8-column) groups per thread
+    constexpr int IT = 1024 / NTH;  // (row, 8-column) groups per thread
     float x[IT][8];
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
-        const int item = threadIdx.x + NT * it;
+        const int item = threadIdx.x + NTH * it;
         const int r = item >> 3, j = item & 7;
         const uint4 a = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j));
         const uint4 b = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j + 4));
@@ -112,7 +112,7 @@ __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
-        const int item = threadIdx.x + NT * it;
+        const int item = threadIdx.x + NTH * it;
         const int r = item >> 3, j = item & 7;
         uint32_t h[4], l[4];
 #pragma unroll
@@ -430,27 +430,41 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t base, int k, uint32_t lbo) {
 // hi | lo), O (fp32 when given, then the gd atoms hi | lo), the state tiles
 // [S_hi | Z_hi | S_lo | Z_lo] and the fp32 dQ staging tile; the gn and gd atoms
 // are 2 kAtom apart, the column stride of the 80-wide g operand.
+// Query side: Q (fp32, then phi(Q) hi | lo, then the fp32 dQ staging tile), G (fp32,
+// then gn hi | lo), one EXT atom holding gd's hi term in 16-byte chunks 0-1 and its lo
+// term in 2-3 (the second N / K atom of [gn | gd] for either term, through the
+// descriptors' strides), and [S | Z] hi | lo.  112 KB: two CTAs of one warpgroup share an
+// SM.  O, when given, is read by each row's thread from global memory (it only enters gd).
 struct LayQ {
-    static constexpr uint32_t Q = 0, G = 2 * kAtom, O = 4 * kAtom, S = 6 * kAtom, OUT = 8 * kAtom;
-    static constexpr uint32_t GSTEP = O - G;
-    static constexpr uint32_t BARS = 10 * kAtom;
-    static constexpr uint32_t XCH = BARS + 64;  // [2][128] fp32 partial row sums
-    static constexpr uint32_t BYTES = XCH + 1024;
+    static constexpr uint32_t Q = 0, G = 2 * kAtom, EXT = 4 * kAtom, S = 5 * kAtom;
+    static constexpr uint32_t OUT = Q;
+    static constexpr uint32_t GSTEP = EXT - G;               // gn hi -> gd hi
+    static constexpr uint32_t GSTEP_LO = EXT + 32 - (G + kAtom);  // gn lo -> gd lo
+    static constexpr uint32_t BARS = 7 * kAtom;
+    static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_O = 0, T_DQ = 80, T_R = 144, T_COLS = 256;
 };
+constexpr int NTQ = 128;  // query-side threads: one per tile row
+static_assert(2 * (LayQ::BYTES + 1024) <= 233472u, "two query-side CTAs per SM");
 // key-side kernel shared memory: K (fp32, then phi(K) hi | lo), V (fp32, then
 // hi | lo), the ones atom (2 kAtom after V_hi: the column stride of [V_hi | 1]),
 // the tiles [R_hi | r_hi | R_lo | r_lo] and the fp32 dK and dV staging tiles.
+// Key side: the fp32 dK, dV rows are staged over the K, V tiles they come from, once
+// the products have read them, so that a CTA takes 112 KB and two CTAs of one
+// warpgroup share an SM (the key side's chunks are independent of each other).
 struct LayK {
     static constexpr uint32_t K = 0, V = 2 * kAtom, ONES = 4 * kAtom, R = 5 * kAtom;
-    static constexpr uint32_t DK = 7 * kAtom, DV = 9 * kAtom;
-    static constexpr uint32_t BARS = 11 * kAtom;
+    static constexpr uint32_t DK = K, DV = V;
+    static constexpr uint32_t BARS = 7 * kAtom;
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_DK = 0, T_DV = 64, T_COLS = 128;
 };
+constexpr int NTK = 128;  // key-side threads: one per tile row
+static_assert(2 * (LayK::BYTES + 1024) <= 233472u, "two key-side CTAs per SM");
 static_assert(LayQ::BYTES <= 227 * 1024 && LayK::BYTES <= 227 * 1024, "shared memory");
 
 struct NcbParams {
+    const float* O;       // the forward's output [BH][N][M] (query side, when given)
     int N;
     int s_spans;          // state partials per head (the state kernel's spans)
     int q_spans, q_len;   // query-side spans (the (R | r) partials' layout)
@@ -522,10 +536,9 @@ __device__ __forceinline__ void dphi_row(const uint8_t* hi, int r, int g, float 
 }
 
 template <bool HAS_O>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTQ, 2)
 ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
-                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmdQ,
-                    const NcbParams p) {
+                    const __grid_constant__ CUtensorMap tmdQ, const NcbParams p) {
     using Lay = LayQ;
     extern __shared__ __align__(1024) uint8_t sm[];
     const int t = threadIdx.x, warp = t >> 5;
@@ -537,7 +550,6 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     uint64_t* mma_bar = tma_bar + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
     volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
-    float* xch = reinterpret_cast<float*>(sm + Lay::XCH);
     if (t == 0) {
         mbar_init(tma_bar, 1);
         mbar_init(mma_bar, 1);
@@ -557,7 +569,7 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int bh = unit / p.q_spans, s = unit - bh * p.q_spans;
     const int n0 = s * p.q_len, n1 = min(p.N, n0 + p.q_len);
     const int nch = (n1 - n0 + L - 1) / L;
-    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
+    const int q = warp;  // TMEM lane quarter; one warpgroup: each thread takes its whole row
     const int row = 32 * q + (t & 31);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sQ = smem_u32(sm + Lay::Q), sG = smem_u32(sm + Lay::G), sS = smem_u32(sm + Lay::S);
@@ -573,16 +585,16 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         phase ^= 1u;
     };
     auto load = [&](int c0) {  // thread 0 only
-        mbar_arrive_expect_tx(tma_bar, (HAS_O ? 6 : 4) * kAtom);
+        mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
         for (int a = 0; a < 2; ++a) {
             tma_load_3d(sm + Lay::Q + a * kAtom, &tmQ, tma_bar, 32 * a, c0, bh);
             tma_load_3d(sm + Lay::G + a * kAtom, &tmG, tma_bar, 32 * a, c0, bh);
-            if (HAS_O) tma_load_3d(sm + Lay::O + a * kAtom, &tmO, tma_bar, 32 * a, c0, bh);
         }
     };
     if (t == 0) load(n0);
 
-    if (q < D / 32) {  // [S | Z] of the head, split: row d, this warpgroup's 32 columns
+    if (q < D / 32) {  // [S | Z] of the head, split: row d, both 32-column halves
+      for (int g = 0; g < 2; ++g) {
         float v[32];
         const float z = sum_partials(p.spart + static_cast<size_t>(bh) * p.s_spans * W, p.s_spans, row, g, v);
         put_state_row(sm + Lay::S, sm + Lay::S + 2 * S_ATOM, row, g, v);
@@ -595,15 +607,15 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 *reinterpret_cast<uint4*>(sm + Lay::S + 3 * S_ATOM + swz(row, c)) = make_uint4(pl, pl, pl, pl);
             }
         }
+      }
     }
 
     for (int c = 0; c < nch; ++c) {
         const int c0 = n0 + c * L;
         const int valid = min(L, n1 - c0);
         wait_bar(tma_bar, tma_phase);
-        split_tile<true, false>(sm + Lay::Q, L);  // phi(Q) hi | lo (rows past N are 0: phi(0) = 1
-                                                  // there, but their g rows are 0)
-        if (t == 0) tma_store_wait_read();        // the dQ staging tile is free again
+        split_tile<true, false, NTQ>(sm + Lay::Q, L);  // phi(Q) hi | lo (rows past N are 0: phi(0) = 1
+                                                       // there, but their g rows are 0)
         sync_tc();
         if (sh[1]) goto cleanup;
         if (t == 0) {  // O_ext = qf [S | Z]
@@ -621,21 +633,32 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                          ID_O, 1u);
             mma_commit(mma_bar);
         }
-        float gv[32], ov[32];
+        float gv[2][32], go = 0.f;
+        if (HAS_O && row < valid) {  // G . O of this row: O from global memory, G from the tile
+            const float4* orow = reinterpret_cast<const float4*>(p.O + (static_cast<size_t>(bh) * p.N + c0 + row) * M);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {  // this thread's 32 columns of G (and O) from the fp32 tiles
-            const float4 a = *reinterpret_cast<const float4*>(sm + Lay::G + f32_off(row, 32 * g + 4 * u));
-            gv[4 * u] = a.x;
-            gv[4 * u + 1] = a.y;
-            gv[4 * u + 2] = a.z;
-            gv[4 * u + 3] = a.w;
-            if (HAS_O) {
-                const float4 b = *reinterpret_cast<const float4*>(sm + Lay::O + f32_off(row, 32 * g + 4 * u));
-                ov[4 * u] = b.x;
-                ov[4 * u + 1] = b.y;
-                ov[4 * u + 2] = b.z;
-                ov[4 * u + 3] = b.w;
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 a = *reinterpret_cast<const float4*>(sm + Lay::G + f32_off(row, 32 * h + 4 * u));
+                    const float4 b = __ldg(orow + 8 * h + u);
+                    gv[h][4 * u] = a.x;
+                    gv[h][4 * u + 1] = a.y;
+                    gv[h][4 * u + 2] = a.z;
+                    gv[h][4 * u + 3] = a.w;
+                    go = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, go))));
+                }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 a = *reinterpret_cast<const float4*>(sm + Lay::G + f32_off(row, 32 * h + 4 * u));
+                    gv[h][4 * u] = a.x;
+                    gv[h][4 * u + 1] = a.y;
+                    gv[h][4 * u + 2] = a.z;
+                    gv[h][4 * u + 3] = a.w;
+                }
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
@@ -646,22 +669,30 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             den = dz[0];
         }
         const float inv = row < valid ? 1.f / den : 0.f;
-        if (!HAS_O) {  // O = num / den
-            tmem_ld32(tm + lane + Lay::T_O + 32 * g, ov);
+        if (!HAS_O) {  // O = num / den, and G . O
 #pragma unroll
-            for (int u = 0; u < 32; ++u) ov[u] *= inv;
+            for (int h = 0; h < 2; ++h) {
+                float ov[32];
+                tmem_ld32(tm + lane + Lay::T_O + 32 * h, ov);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) go = fmaf(gv[h][u], ov[u] * inv, go);
+            }
         }
-        float go = 0.f;
+        const float gd = -go * inv;
+        __syncthreads();  // every G row is read: the tile takes g from here on
+        {   // gn = G / den, split, into the G tile's atoms; gd's two terms into the EXT atom
 #pragma unroll
-        for (int u = 0; u < 32; ++u) go = fmaf(gv[u], ov[u], go);
-        xch[g * 128 + row] = go;
-        __syncthreads();  // every G and O row is read: the tiles take g from here on
-        const float gd = -(xch[row] + xch[128 + row]) * inv;
-        {   // gn = G / den, split, into the G tile's atoms
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) gv[u] *= inv;
-            put_state_row(sm + Lay::G, sm + Lay::G + kAtom, row, g, gv);
-            if (g == 0) put_ext_row(sm + Lay::O, sm + Lay::O + kAtom, row, gd);
+                for (int u = 0; u < 32; ++u) gv[h][u] *= inv;
+                put_state_row(sm + Lay::G, sm + Lay::G + kAtom, row, h, gv[h]);
+            }
+            float gh, gl;
+            split_bf16(gd, gh, gl);
+            *reinterpret_cast<uint4*>(sm + Lay::EXT + swz(row, 0)) = make_uint4(pack_bf16(gh, 0.f), 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + Lay::EXT + swz(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + Lay::EXT + swz(row, 2)) = make_uint4(pack_bf16(gl, 0.f), 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + Lay::EXT + swz(row, 3)) = make_uint4(0u, 0u, 0u, 0u);
         }
         sync_tc();
         if (t == 0) {
@@ -675,7 +706,7 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mma_bf16(tm + Lay::T_DQ, kdesc(sG, k, Lay::GSTEP), kdesc(sS + 2 * S_ATOM, k, S_ATOM), ID_DQ, 1u);
 #pragma unroll
             for (int k = 0; k < NE / 16; ++k)
-                mma_bf16(tm + Lay::T_DQ, kdesc(sGl, k, Lay::GSTEP), kdesc(sS, k, S_ATOM), ID_DQ, 1u);
+                mma_bf16(tm + Lay::T_DQ, kdesc(sGl, k, Lay::GSTEP_LO), kdesc(sS, k, S_ATOM), ID_DQ, 1u);
             // [R | r] += qf^T g (the D = 64 rows pad to 128 through the A operand's atom stride)
 #pragma unroll
             for (int k = 0; k < L / 16; ++k)
@@ -683,7 +714,7 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                          (c > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
             for (int k = 0; k < L / 16; ++k)
-                mma_bf16(tm + Lay::T_R, mdesc(sQ, k, kAtom), mdesc(sGl, k, Lay::GSTEP), ID_S, 1u);
+                mma_bf16(tm + Lay::T_R, mdesc(sQ, k, kAtom), mdesc(sGl, k, Lay::GSTEP_LO), ID_S, 1u);
 #pragma unroll
             for (int k = 0; k < L / 16; ++k)
                 mma_bf16(tm + Lay::T_R, mdesc(sQ + kAtom, k, kAtom), mdesc(sG, k, Lay::GSTEP), ID_S, 1u);
@@ -691,37 +722,48 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        {   // dQ = dqf * phi'(Q) -> fp32 staging tile
-            float v[32], f[32];
-            tmem_ld32(tm + lane + Lay::T_DQ + 32 * g, v);
-            dphi_row(sm + Lay::Q, row, g, f);
+        {   // dQ = dqf * phi'(Q) -> fp32 staging tile over the Q tile: phi'(Q) of the whole row
+            // is read before any thread writes over it
+            float f[2][32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<float4*>(sm + Lay::OUT + f32_off(row, 32 * g + 4 * u)) =
-                    make_float4(v[4 * u] * f[4 * u], v[4 * u + 1] * f[4 * u + 1], v[4 * u + 2] * f[4 * u + 2],
-                                v[4 * u + 3] * f[4 * u + 3]);
+            for (int h = 0; h < 2; ++h) dphi_row(sm + Lay::Q, row, h, f[h]);
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_DQ + 32 * h, v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<float4*>(sm + Lay::OUT + f32_off(row, 32 * h + 4 * u)) =
+                        make_float4(v[4 * u] * f[h][4 * u], v[4 * u + 1] * f[h][4 * u + 1],
+                                    v[4 * u + 2] * f[h][4 * u + 2], v[4 * u + 3] * f[h][4 * u + 3]);
+            }
         }
         sync_tc();
         if (t == 0) {
             tma_store_3d(&tmdQ, sm + Lay::OUT, 0, c0, bh);
             tma_store_3d(&tmdQ, sm + Lay::OUT + kAtom, 32, c0, bh);
             tma_store_commit();
-            if (c + 1 < nch) load(c0 + L);  // every input tile is consumed
+            if (c + 1 < nch) {  // the staged rows are read out of the Q tile first
+                tma_store_wait_read();
+                load(c0 + L);
+            }
         }
     }
     if (q < D / 32) {  // publish this span's [R | r]
         float* out = p.rpart + (static_cast<size_t>(bh) * p.q_spans + s) * W;
-        float v[32];
-        tmem_ld32(tm + lane + Lay::T_R + 32 * g, v);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            reinterpret_cast<float4*>(out + row * M + 32 * g)[u] =
-                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        if (g == 0) {
-            float z[16];
-            tmem_ld16(tm + lane + Lay::T_R + M, z);
-            out[D * M + row] = z[0];
+        for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tm + lane + Lay::T_R + 32 * h, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                reinterpret_cast<float4*>(out + row * M + 32 * h)[u] =
+                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         }
+        float z[16];
+        tmem_ld16(tm + lane + Lay::T_R + M, z);
+        out[D * M + row] = z[0];
     }
 
 cleanup:  // the only early exit follows a copy wait: no copy of this CTA is in flight
@@ -731,7 +773,7 @@ cleanup:  // the only early exit follows a copy wait: no copy of this CTA is in 
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTK, 2)
 ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                   const NcbParams p) {
@@ -756,7 +798,7 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         tmem_alloc(tmem_slot, Lay::T_COLS);
         tmem_relinquish();
     }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += NT)
+    for (int i = t; i < static_cast<int>(kAtom / 16); i += NTK)
         reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
             make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_before_sync();
@@ -768,7 +810,7 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int bh = unit / p.k_spans, s = unit - bh * p.k_spans;
     const int n0 = s * p.k_len, n1 = min(p.N, n0 + p.k_len);
     const int nch = (n1 - n0 + L - 1) / L;
-    const int q = warp & 3, g = warp >> 2;
+    const int q = warp;  // one warpgroup: every thread takes both 32-column halves of its row
     const int row = 32 * q + (t & 31);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sR = smem_u32(sm + Lay::R);
@@ -794,18 +836,21 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     if (t == 0) load(n0);
 
     if (q < D / 32) {  // [R | r] of the head (the query side's partials), split
-        float v[32];
-        const float r = sum_partials(p.rpart + static_cast<size_t>(bh) * p.q_spans * W, p.q_spans, row, g, v);
-        put_state_row(sm + Lay::R, sm + Lay::R + 2 * S_ATOM, row, g, v);
-        if (g == 0) put_ext_row(sm + Lay::R + S_ATOM, sm + Lay::R + 3 * S_ATOM, row, r);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            float v[32];
+            const float r =
+                sum_partials(p.rpart + static_cast<size_t>(bh) * p.q_spans * W, p.q_spans, row, g, v);
+            put_state_row(sm + Lay::R, sm + Lay::R + 2 * S_ATOM, row, g, v);
+            if (g == 0) put_ext_row(sm + Lay::R + S_ATOM, sm + Lay::R + 3 * S_ATOM, row, r);
+        }
     }
 
     for (int c = 0; c < nch; ++c) {
         const int c0 = n0 + c * L;
         wait_bar(tma_bar, tma_phase);
-        split_tile<true, false>(sm + Lay::K, L);   // phi(K) hi | lo
-        split_tile<false, false>(sm + Lay::V, L);  // V hi | lo
-        if (t == 0) tma_store_wait_read();         // the staging tiles are free again
+        split_tile<true, false, NTK>(sm + Lay::K, L);   // phi(K) hi | lo
+        split_tile<false, false, NTK>(sm + Lay::V, L);  // V hi | lo
         sync_tc();
         if (sh[1]) goto cleanup;
         if (t == 0) {
@@ -834,20 +879,27 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        {   // dK = dkf * phi'(K), dV -> fp32 staging tiles
-            float v[32], f[32];
-            tmem_ld32(tm + lane + Lay::T_DK + 32 * g, v);
-            dphi_row(sm + Lay::K, row, g, f);
+        {   // dK = dkf * phi'(K), dV -> fp32 staging tiles over the K, V tiles: phi'(K) of the
+            // whole row is read from the K tile before any thread writes over it
+            float f[2][32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<float4*>(sm + Lay::DK + f32_off(row, 32 * g + 4 * u)) =
-                    make_float4(v[4 * u] * f[4 * u], v[4 * u + 1] * f[4 * u + 1], v[4 * u + 2] * f[4 * u + 2],
-                                v[4 * u + 3] * f[4 * u + 3]);
-            tmem_ld32(tm + lane + Lay::T_DV + 32 * g, v);
+            for (int g = 0; g < 2; ++g) dphi_row(sm + Lay::K, row, g, f[g]);
+            __syncthreads();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<float4*>(sm + Lay::DV + f32_off(row, 32 * g + 4 * u)) =
-                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            for (int g = 0; g < 2; ++g) {
+                float v[32];
+                tmem_ld32(tm + lane + Lay::T_DK + 32 * g, v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<float4*>(sm + Lay::DK + f32_off(row, 32 * g + 4 * u)) =
+                        make_float4(v[4 * u] * f[g][4 * u], v[4 * u + 1] * f[g][4 * u + 1],
+                                    v[4 * u + 2] * f[g][4 * u + 2], v[4 * u + 3] * f[g][4 * u + 3]);
+                tmem_ld32(tm + lane + Lay::T_DV + 32 * g, v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<float4*>(sm + Lay::DV + f32_off(row, 32 * g + 4 * u)) =
+                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
         }
         sync_tc();
         if (t == 0) {
@@ -856,7 +908,10 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 tma_store_3d(&tmdV, sm + Lay::DV + a * kAtom, 32 * a, c0, bh);
             }
             tma_store_commit();
-            if (c + 1 < nch) load(c0 + L);  // every input tile is consumed
+            if (c + 1 < nch) {  // the staged rows are read out of the input tiles first
+                tma_store_wait_read();
+                load(c0 + L);
+            }
         }
     }
 
@@ -894,10 +949,10 @@ inline void nc_spans(int BH, int N, int num_sms, int* spans, int* span_len) {
     *spans = (N + *span_len - 1) / *span_len;
 }
 
-// Spans of the backward's query and key kernels: one CTA per SM.
+// Spans of the backward's query and key kernels: two CTAs per SM.
 inline void ncb_spans(int BH, int N, int num_sms, int* spans, int* span_len) {
     const int chunks = (N + L - 1) / L;
-    const int s = spans_for(BH, chunks, num_sms);
+    const int s = spans_for(BH, chunks, 2 * num_sms);
     *span_len = ((chunks + s - 1) / s) * L;
     *spans = (N + *span_len - 1) / *span_len;
 }
@@ -940,6 +995,7 @@ cudaError_t noncausal_backward_tc_f32(const LaunchCtx& c, const float* Q, const 
     ncb_spans(BH, N, c.num_sms, &p.q_spans, &p.q_len);
     p.k_spans = p.q_spans;
     p.k_len = p.q_len;
+    p.O = O;
     p.status = c.status_word;
     char* ws = nullptr;
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&ws), noncausal_backward_tc_f32_scratch(BH, N, c.num_sms))))
@@ -948,15 +1004,15 @@ cudaError_t noncausal_backward_tc_f32(const LaunchCtx& c, const float* Q, const 
     p.spart = sp.part;
     p.rpart = reinterpret_cast<float*>(ws + plan::up256(sizeof(float) * static_cast<size_t>(BH) * sp.spans * W));
     do {
-        CUtensorMap mQ, mK, mV, mO, mG, mdQ, mdK, mdV;
+        CUtensorMap mQ, mK, mV, mG, mdQ, mdK, mdV;
         if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D)) ||
             (e = make_map_f32(&mV, V, BH, N, M)) || (e = make_map_f32(&mG, G, BH, N, M)) ||
-            (e = make_map_f32(&mO, O ? O : G, BH, N, M)) || (e = make_map_f32(&mdQ, dQ, BH, N, D)) ||
-            (e = make_map_f32(&mdK, dK, BH, N, D)) || (e = make_map_f32(&mdV, dV, BH, N, M)))
+            (e = make_map_f32(&mdQ, dQ, BH, N, D)) || (e = make_map_f32(&mdK, dK, BH, N, D)) ||
+            (e = make_map_f32(&mdV, dV, BH, N, M)))
             break;
         ka<<<BH * sp.spans, NT, LayA::BYTES, c.stream>>>(mK, mV, sp);
-        kq<<<BH * p.q_spans, NT, LayQ::BYTES, c.stream>>>(mQ, mG, mO, mdQ, p);
-        kk<<<BH * p.k_spans, NT, LayK::BYTES, c.stream>>>(mK, mV, mdK, mdV, p);
+        kq<<<BH * p.q_spans, NTQ, LayQ::BYTES, c.stream>>>(mQ, mG, mdQ, p);
+        kk<<<BH * p.k_spans, NTK, LayK::BYTES, c.stream>>>(mK, mV, mdK, mdV, p);
         note_launch(3);
         e = cudaGetLastError();
     } while (0);

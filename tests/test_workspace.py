@@ -124,11 +124,11 @@ def test_peak_pool_use_matches_report(dt, shape):
 
 def test_noncausal_backward_bytes():
     # fp32 D = M = 64 on the tensor cores: the forward's state partials (4 spans per head
-    # at two CTAs per SM) plus the query side's (R | r) partials: one CTA per SM, 32 chunks
-    # per head cut into 7 spans of 5 chunks (448 CTAs, 3 waves of 152: the fewest waves x
-    # chunks), 64 heads
+    # at two CTAs per SM) plus the query side's (R | r) partials, also two CTAs per SM: 32
+    # chunks per head cut into 4 spans of 8 chunks (256 CTAs, one wave of 304 slots: the
+    # fewest waves x chunks, fewest spans on a tie with 8 spans of 4), 64 heads
     up = lambda x: (x + 255) // 256 * 256
     W = 64 * 64 + 64
-    assert _ws("la_backward_noncausal", 8, 8, 4096, 64, 64, F32) == up(4 * 64 * 4 * W) + 4 * 64 * 7 * W
+    assert _ws("la_backward_noncausal", 8, 8, 4096, 64, 64, F32) == up(4 * 64 * 4 * W) + 4 * 64 * 4 * W
     # other shapes on the CUDA cores: state and (R | r) partials and totals
     assert _ws("la_backward_noncausal", 1, 2, 1000, 32, 64, BF16) > 0
