@@ -13,7 +13,7 @@
 // Layout: a head's cache rows are contiguous, K_cache [BH][T_max][D],
 // V_cache [BH][T_max][M] (M = D).  Each CTA takes a range of positions of one
 // head; a lane group of LR lanes holds one row (16 bytes a lane) and a warp
-// works on 32 / LR rows at a time, four rows per lane group in flight.  Scores
+// works on 32 / LR rows at a time, eight rows per lane group in flight.  Scores
 // are kept in base 2 (q pre-scaled by log2(e) / sqrt(D)), and each lane group
 // keeps a running maximum, a running sum of weights and its slice of the
 // weighted value sum (the online form of the max-subtracted softmax).  The
@@ -32,7 +32,7 @@ namespace la {
 namespace {
 
 constexpr int kSdThreads = 256;
-constexpr int kSdUnroll = 4;
+constexpr int kSdUnroll = 8;
 
 template <typename T, int D>
 struct SdShape {
