@@ -8,17 +8,21 @@
 // fp32 operands run on the bf16 tensor path split in two: x = hi + lo with
 // hi = bf16(x) and lo = bf16(x - hi), and a product a b is taken as
 // a_hi b_hi + a_hi b_lo + a_lo b_hi (the dropped a_lo b_lo and the rounding of
-// the lo parts are about 2^-17 of |a b|), accumulated in fp32 in TMEM.  The
-// ones block appended to V carries the normaliser through the same products.
+// the lo parts are about 2^-17 of |a b|), accumulated in fp32 in TMEM.  In the
+// read-out and the backward, a Z block appended to S (or a ones block to V)
+// carries the normaliser through the same products.
 //
-//   state kernel   one CTA per (head, span): TMA loads fp32 K, V tiles of 128
-//                  tokens; phi and the split are done in place (the fp32 tile
-//                  becomes its hi and lo bf16 tiles); the MMAs accumulate
-//                  [S | Z] for the span, published as fp32 partials;
+//   state kernel   one CTA per (head, span): TMA loads fp32 K, V tiles of 64
+//                  tokens into a ring of three slots; phi and the split are
+//                  done in place (the fp32 tile becomes its hi and lo bf16
+//                  tiles); the MMAs accumulate S for the span and the CUDA
+//                  cores sum Z; [S | Z] is published as fp32 partials;
 //   read-out kernel one CTA per (head, span): sums the partials of the head,
 //                  splits [S | Z] into bf16 hi and lo state tiles, then per
-//                  chunk loads fp32 Q, applies phi and the split, takes the
-//                  three products into TMEM and stores num / den as fp32.
+//                  chunk loads fp32 Q, applies phi and the split (into an
+//                  operand tile, so that the next chunk's copy lands under
+//                  this chunk's products), takes the three products into TMEM
+//                  and stores num / den as fp32.
 // Each input is read once from HBM and the output written once.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -38,24 +42,33 @@ constexpr int D = 64, M = 64, NE = M + 16, W = D * M + D;
 constexpr int NT = 256;  // two warpgroups; two CTAs share an SM
 constexpr uint32_t S_ATOM = D * 128;  // 64 state rows x 128 bytes
 
-constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);   // kf^T [V | 1]
+constexpr uint32_t ID_S = idesc_bf16(128, NE, true, true);   // MN-major x MN-major, N = M + 16
 constexpr uint32_t ID_O = idesc_bf16(128, NE, false, true);  // qf [S | Z]
 
-// state kernel shared memory: K tile (fp32, then hi | lo bf16), V tile (fp32,
-// then hi | lo bf16) followed by a ones atom and a zeros atom, so that
-// [V_hi | 1] and [V_lo | 0] are operands with a 32 KB atom stride.
+// state kernel shared memory: a ring of three 64-token stages, each an fp32 K
+// tile and an fp32 V tile of two 8 KB atoms (32 columns of 64 rows); after the
+// split in place each tile is its hi atom followed by its lo atom.
+constexpr int LS = 64;                  // tokens per state-kernel stage
+constexpr int NSTG = 3;                 // stages in the ring
+constexpr uint32_t kAtomS = LS * 128;   // one 64-row atom column
+constexpr uint32_t ID_SV = idesc_bf16(128, M, true, true);  // kf^T V, MN-major x MN-major
 struct LayA {
-    static constexpr uint32_t K = 0, V = 2 * kAtom, ONES = 4 * kAtom, ZEROS = 5 * kAtom;
-    static constexpr uint32_t BARS = 6 * kAtom;
-    static constexpr uint32_t BYTES = BARS + 64;
-    static constexpr uint32_t T_COLS = 128;
+    static constexpr uint32_t STAGE = 4 * kAtomS;  // K then V
+    static constexpr uint32_t V = 2 * kAtomS;      // V within a stage
+    static constexpr uint32_t BARS = NSTG * STAGE;  // copy, split and product barriers, TMEM slot, flags
+    static constexpr uint32_t BYTES = BARS + 128;
+    static constexpr uint32_t T_COLS = 64;
 };
+constexpr int NTS = NT + 32;  // state kernel: eight split warps and one issuing warp
+static_assert(LayA::BYTES <= 113 * 1024, "two CTAs per SM");
 
-// read-out kernel shared memory: Q tile (fp32, then hi | lo bf16), state tiles
-// [S_hi | Z_hi] and [S_lo | Z_lo] (MN-major, 64 rows, 8 KB atoms) and the fp32
-// output staging tile.
+// read-out kernel shared memory: the fp32 Q tile (the copy's landing place),
+// the operand tile (Q's hi | lo bf16 atoms, then the fp32 output staging), and
+// the state tiles [S_hi | Z_hi] and [S_lo | Z_lo] (MN-major, 64 rows, 8 KB
+// atoms).  The split reads Q into registers and writes the operand tile, so
+// the next chunk's copy can land while this chunk is multiplied and stored.
 struct LayB {
-    static constexpr uint32_t Q = 0, S = 2 * kAtom, OUT = 4 * kAtom;
+    static constexpr uint32_t Q = 0, S = 2 * kAtom, OP = 4 * kAtom;
     static constexpr uint32_t BARS = 6 * kAtom;
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_COLS = 128;
@@ -68,9 +81,10 @@ struct NcParams {
     unsigned* status;
 };
 
-// Byte offset of fp32 element (r, c), c < 64, in a tile of two 32-column atoms.
-__device__ __forceinline__ uint32_t f32_off(int r, int c) {
-    return (c >> 5) * kAtom + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4;
+// Byte offset of fp32 element (r, c), c < 64, in a tile of two 32-column atoms
+// of `atom` bytes each.
+__device__ __forceinline__ uint32_t f32_off(int r, int c, uint32_t atom = kAtom) {
+    return (c >> 5) * atom + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4;
 }
 
 // Two values at once: hi = their bf16 pair (one rounding convert), lo = the bf16 pair of
@@ -88,8 +102,11 @@ __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
 
 // In place: the fp32 [128 x 64] tile at `buf` becomes bf16 hi (buf) and lo
 // (buf + 16 KB), each one K-major 128-row atom; phi is applied first when PHI,
-// and rows >= valid become 0 when ZERO_TAIL.  Each thread reads its
-// (row, 8-column) groups before any thread writes.
+// and rows >= valid become 0 when ZERO_TAIL.  Thread t takes the 8-column
+// group t % 8 of rows t / 8 + (NTH / 8) i, so the eight threads of a row are
+// one warp and the hi and lo words written over a row's fp32 values are that
+// row's: the warp reads all of its rows before it writes, with no block-wide
+// barrier.
 template <bool PHI, bool ZERO_TAIL, int NTH = NT>
 __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
     constexpr int IT = 1024 / NTH;  // (row, 8-column) groups per thread
@@ -109,7 +126,7 @@ __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
         x[it][6] = __uint_as_float(b.z);
         x[it][7] = __uint_as_float(b.w);
     }
-    __syncthreads();
+    __syncwarp();  // a row's reads and writes are all this warp's
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
         const int item = threadIdx.x + NTH * it;
@@ -130,6 +147,58 @@ __device__ __forceinline__ void split_tile(uint8_t* buf, int valid) {
     }
 }
 
+// split_tile on one 64-row stage, by the NT threads 0 .. NT - 1: the fp32
+// [64 x 64] tile at `buf` becomes bf16 hi (buf) and lo (buf + 8 KB), phi applied
+// first when PHI.  Thread t takes the 8-column group t % 8 of rows t / 8 and
+// t / 8 + NT / 8, so the eight threads of a row are one warp, and the hi and lo
+// words written over a row's fp32 values are that row's: no thread outside
+// the warp reads them, and the warp needs no block-wide barrier.  With ZSUM, rows >=
+// valid become 0 and each thread adds its values to z: the same 8 columns,
+// 8 (t % 8) on, in every row it takes.
+template <bool PHI, bool ZSUM>
+__device__ __forceinline__ void split_stage(uint8_t* buf, int valid, float (&z)[8]) {
+    constexpr int IT = LS * 8 / NT;  // rows per thread
+    const int j = threadIdx.x & 7;
+    float x[IT][8];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int r = (threadIdx.x >> 3) + (NT / 8) * it;
+        const uint4 a = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j, kAtomS));
+        const uint4 b = *reinterpret_cast<const uint4*>(buf + f32_off(r, 8 * j + 4, kAtomS));
+        x[it][0] = __uint_as_float(a.x);
+        x[it][1] = __uint_as_float(a.y);
+        x[it][2] = __uint_as_float(a.z);
+        x[it][3] = __uint_as_float(a.w);
+        x[it][4] = __uint_as_float(b.x);
+        x[it][5] = __uint_as_float(b.y);
+        x[it][6] = __uint_as_float(b.z);
+        x[it][7] = __uint_as_float(b.w);
+    }
+    __syncwarp();  // a row's reads and writes are all this warp's
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int r = (threadIdx.x >> 3) + (NT / 8) * it;
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float v0 = x[it][2 * u], v1 = x[it][2 * u + 1];
+            if (PHI) {
+                v0 = phi_fast(v0);
+                v1 = phi_fast(v1);
+            }
+            if (ZSUM) {
+                v0 = r < valid ? v0 : 0.f;
+                v1 = r < valid ? v1 : 0.f;
+                z[2 * u] += v0;
+                z[2 * u + 1] += v1;
+            }
+            split_pair(v0, v1, h[u], l[u]);
+        }
+        *reinterpret_cast<uint4*>(buf + swz(r, j)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(buf + kAtomS + swz(r, j)) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
 __device__ __forceinline__ void sync_tc() {
     fence_proxy_async();
     fence_before_sync();
@@ -138,8 +207,18 @@ __device__ __forceinline__ void sync_tc() {
 }
 
 // ------------------------------------------------------------ state kernel
+//
+// The span's 64-token stages go through a ring of three slots.  Eight warps
+// split each stage in place (phi(K) and K, V into hi and lo), each on its own
+// rows with no block-wide barrier, and hand it over through the slot's split
+// barrier (one arrival per thread); a ninth warp issues the copies and the
+// products (S = kf^T V as hi hi + hi lo + lo hi, N = 64) and refills a slot
+// with the stage three ahead as soon as the products that read it are done,
+// so the split warps wait neither for copies in steady state nor for the
+// products.  Z is the sum of the phi(K) rows, added up in fp32 on the CUDA
+// cores during the split.
 
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(NTS, 2)
 nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const NcParams p) {
     using Lay = LayA;
@@ -149,24 +228,23 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (t == 0) atomicOr(p.status, kErrAlign);
         return;
     }
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + Lay::BARS);
-    uint64_t* mma_bar = tma_bar + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 2);
-    volatile int* sh = reinterpret_cast<volatile int*>(tma_bar + 3);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::BARS);  // [NSTG] copy landed
+    uint64_t* done = full + NSTG;                                   // [NSTG] split written
+    uint64_t* mmab = full + 2 * NSTG;                               // [NSTG] products done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3 * NSTG);
+    volatile int* sh = reinterpret_cast<volatile int*>(full + 3 * NSTG + 1);
     if (t == 0) {
-        mbar_init(tma_bar, 1);
-        mbar_init(mma_bar, 1);
+        for (int b = 0; b < NSTG; ++b) {
+            mbar_init(full + b, 1);
+            mbar_init(done + b, NT);
+            mbar_init(mmab + b, 1);
+        }
         fence_mbar_init();
         sh[1] = 0;
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, Lay::T_COLS);
         tmem_relinquish();
-    }
-    for (int i = t; i < static_cast<int>(kAtom / 16); i += NT) {
-        reinterpret_cast<uint4*>(sm + Lay::ONES)[i] =
-            make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        reinterpret_cast<uint4*>(sm + Lay::ZEROS)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_before_sync();
     __syncthreads();
@@ -176,72 +254,124 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     const int unit = blockIdx.x;
     const int bh = unit / p.spans, s = unit - bh * p.spans;
     const int n0 = s * p.span_len, n1 = min(p.N, n0 + p.span_len);
-    const int nch = (n1 - n0 + L - 1) / L;
-    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
+    const int nst = max(0, (n1 - n0 + LS - 1) / LS);
+    const int q = warp & 3, g = (warp >> 2) & 1;  // TMEM lane quarter, column half (split warps)
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V);
-    uint32_t tma_phase = 0, mma_phase = 0;
+    float z[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) z[u] = 0.f;
 
     auto fail = [&](unsigned code) {
         atomicOr(p.status, code);
         sh[1] = 1;
     };
-    auto wait_bar = [&](uint64_t* bar, uint32_t& phase) {
-        if (t == 0 && !mbar_wait(bar, phase, kWaitLimit)) fail(kErrWait);
-        __syncthreads();
-        phase ^= 1u;
-    };
-    auto load = [&](int c0) {
-        mbar_arrive_expect_tx(tma_bar, 4 * kAtom);
-        tma_load_3d(sm + Lay::K, &tmK, tma_bar, 0, c0, bh);
-        tma_load_3d(sm + Lay::K + kAtom, &tmK, tma_bar, 32, c0, bh);
-        tma_load_3d(sm + Lay::V, &tmV, tma_bar, 0, c0, bh);
-        tma_load_3d(sm + Lay::V + kAtom, &tmV, tma_bar, 32, c0, bh);
-    };
 
-    if (t == 0) load(n0);
-    for (int c = 0; c < nch; ++c) {
-        const int c0 = n0 + c * L;
-        const int valid = min(L, n1 - c0);
-        wait_bar(tma_bar, tma_phase);
-        split_tile<true, true>(sm + Lay::K, valid);
-        split_tile<false, false>(sm + Lay::V, valid);
-        sync_tc();
-        if (sh[1]) goto cleanup;
-        if (t == 0) {
-            // K_hi^T [V_hi | 1] + K_hi^T [V_lo | 0] + K_lo^T [V_hi | 1]; the D = 64
-            // rows pad to 128 through the A operand's atom stride (rows never read)
+    if (warp == NT / 32) {
+        if (t == NT) {  // the issuing thread; a slot's barriers see stage st with parity (st / NSTG) & 1
+            int loaded = 0, issued = 0;
+            auto load = [&](int st) {
+                uint8_t* buf = sm + (st % NSTG) * Lay::STAGE;
+                uint64_t* bar = full + st % NSTG;
+                const int y = n0 + st * LS;
+                mbar_arrive_expect_tx(bar, Lay::STAGE);
+                tma_load_3d(buf, &tmK, bar, 0, y, bh);
+                tma_load_3d(buf + kAtomS, &tmK, bar, 32, y, bh);
+                tma_load_3d(buf + Lay::V, &tmV, bar, 0, y, bh);
+                tma_load_3d(buf + Lay::V + kAtomS, &tmV, bar, 32, y, bh);
+                ++loaded;
+            };
+            for (int st = 0; st < min(NSTG, nst); ++st) load(st);
+            for (int c = 0; c < nst; ++c) {
+                const int w = mbar_wait_or(done + c % NSTG, (c / NSTG) & 1u, kWaitLimit, sh + 1);
+                if (w) {
+                    if (w == 2) fail(kErrWait);
+                    break;
+                }
+                fence_after_sync();
+                // K_hi^T V_hi + K_hi^T V_lo + K_lo^T V_hi; the D = 64 rows of kf^T pad to the
+                // MMA's 128 through the A operand's atom stride (accumulator lanes never read)
+                const uint32_t sK = smem_u32(sm + (c % NSTG) * Lay::STAGE), sV = sK + Lay::V;
 #pragma unroll
-            for (int k = 0; k < L / 16; ++k)
-                mma_bf16(tm, sdesc(sK + 2048 * k, kAtom, 1024), sdesc(sV + 2048 * k, 2 * kAtom, 1024),
-                         ID_S, (c > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < LS / 16; ++k)
+                    mma_bf16(tm, sdesc(sK + 2048 * k, kAtomS, 1024), sdesc(sV + 2048 * k, kAtomS, 1024),
+                             ID_SV, (c > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
-            for (int k = 0; k < L / 16; ++k)
-                mma_bf16(tm, sdesc(sK + 2048 * k, kAtom, 1024),
-                         sdesc(sV + kAtom + 2048 * k, 2 * kAtom, 1024), ID_S, 1u);
+                for (int k = 0; k < LS / 16; ++k)
+                    mma_bf16(tm, sdesc(sK + 2048 * k, kAtomS, 1024),
+                             sdesc(sV + kAtomS + 2048 * k, kAtomS, 1024), ID_SV, 1u);
 #pragma unroll
-            for (int k = 0; k < L / 16; ++k)
-                mma_bf16(tm, sdesc(sK + kAtom + 2048 * k, kAtom, 1024),
-                         sdesc(sV + 2048 * k, 2 * kAtom, 1024), ID_S, 1u);
-            mma_commit(mma_bar);
+                for (int k = 0; k < LS / 16; ++k)
+                    mma_bf16(tm, sdesc(sK + kAtomS + 2048 * k, kAtomS, 1024),
+                             sdesc(sV + 2048 * k, kAtomS, 1024), ID_SV, 1u);
+                mma_commit(mmab + c % NSTG);
+                ++issued;
+                if (c >= 1 && c - 1 + NSTG < nst) {  // stage c - 1's slot, once its products are done
+                    const int pv = c - 1;
+                    if (!mbar_wait(mmab + pv % NSTG, (pv / NSTG) & 1u, kWaitLimit)) {
+                        fail(kErrWait);
+                        break;
+                    }
+                    load(pv + NSTG);
+                }
+            }
+            // the last commit covers every product before it; then every copy still in flight
+            // (only the last one into each slot can be: the earlier ones were split)
+            if (issued > 0 &&
+                !mbar_wait(mmab + (issued - 1) % NSTG, ((issued - 1) / NSTG) & 1u, kWaitLimit))
+                fail(kErrWait);
+            for (int st = max(0, loaded - NSTG); st < loaded; ++st)
+                mbar_wait(full + st % NSTG, (st / NSTG) & 1u, kWaitLimit);
         }
-        wait_bar(mma_bar, mma_phase);
-        fence_after_sync();
-        if (t == 0 && c + 1 < nch) load(c0 + L);
-    }
-    if (q < D / 32) {  // publish the span's [S | Z]: row d < D, this warpgroup's 32 columns
-        float* out = p.part + static_cast<size_t>(unit) * W;
-        const int d = 32 * q + (t & 31);
-        float v[32];
-        tmem_ld32(tm + lane + 32 * g, v);
+        __syncwarp();
+    } else {
+        for (int c = 0; c < nst; ++c) {  // every split thread waits for the copy itself
+            uint8_t* buf = sm + (c % NSTG) * Lay::STAGE;
+            const int w = mbar_wait_or(full + c % NSTG, (c / NSTG) & 1u, kWaitLimit, sh + 1);
+            if (w) {
+                if (w == 2) fail(kErrWait);
+                break;
+            }
+            const int valid = min(LS, n1 - (n0 + c * LS));
+            split_stage<true, true>(buf, valid, z);
+            split_stage<false, false>(buf + Lay::V, valid, z);
+            fence_proxy_async();
+            mbar_arrive(done + c % NSTG);
+        }
+        // Z: the threads of an 8-column group are the lanes l, l ^ 8, l ^ 16, l ^ 24 of every warp
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            reinterpret_cast<float4*>(out + d * M + 32 * g)[u] =
-                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        if (g == 0) {
-            float z[16];
-            tmem_ld16(tm + lane + M, z);
-            out[D * M + d] = z[0];
+        for (int u = 0; u < 8; ++u) {
+            z[u] += __shfl_xor_sync(0xffffffffu, z[u], 8);
+            z[u] += __shfl_xor_sync(0xffffffffu, z[u], 16);
+        }
+    }
+    __syncthreads();  // every product is done (or the CTA gives up): slot 0 takes the warps' Z sums
+    if (sh[1]) goto cleanup;
+    fence_after_sync();
+    {
+        float* zw = reinterpret_cast<float*>(sm);  // [NT / 32][D]
+        if (warp < NT / 32 && (t & 31) < 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) zw[warp * D + 8 * (t & 31) + u] = z[u];
+        }
+        __syncthreads();
+        float* out = p.part + static_cast<size_t>(unit) * W;
+        if (warp < NT / 32 && q < D / 32) {  // publish the span's S: row d < D, 32 columns
+            const int d = 32 * q + (t & 31);
+            float v[32];
+            tmem_ld32(tm + lane + 32 * g, v);
+            if (nst == 0)
+#pragma unroll
+                for (int u = 0; u < 32; ++u) v[u] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                reinterpret_cast<float4*>(out + d * M + 32 * g)[u] =
+                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+        if (t < D) {
+            float zz = 0.f;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) zz += zw[w * D + t];
+            out[D * M + t] = zz;
         }
     }
 
@@ -288,7 +418,7 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int nch = (n1 - n0 + L - 1) / L;
     const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter, warpgroup (column half)
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t sQ = smem_u32(sm + Lay::Q), sS = smem_u32(sm + Lay::S);
+    const uint32_t sQ = smem_u32(sm + Lay::OP), sS = smem_u32(sm + Lay::S);  // sQ: the operand tile
     uint32_t tma_phase = 0, mma_phase = 0;
 
     auto fail = [&](unsigned code) {
@@ -300,10 +430,14 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         __syncthreads();
         phase ^= 1u;
     };
+    bool in_flight = false;  // thread 0: a Q copy not yet waited for, and its phase
+    uint32_t ld_phase = 0;
     auto load = [&](int c0) {
         mbar_arrive_expect_tx(tma_bar, 2 * kAtom);
         tma_load_3d(sm + Lay::Q, &tmQ, tma_bar, 0, c0, bh);
         tma_load_3d(sm + Lay::Q + kAtom, &tmQ, tma_bar, 32, c0, bh);
+        in_flight = true;
+        ld_phase = tma_phase;
     };
     if (t == 0) load(n0);
 
@@ -352,10 +486,42 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int c = 0; c < nch; ++c) {
         const int c0 = n0 + c * L;
         wait_bar(tma_bar, tma_phase);
-        split_tile<true, false>(sm + Lay::Q, L);
-        if (t == 0) tma_store_wait_read();  // the staging tile is free again
-        sync_tc();
         if (sh[1]) goto cleanup;
+        if (t == 0) in_flight = false;
+        {   // phi(Q) split into the operand tile: this thread's (row, 8-column) groups into
+            // registers, the Q tile handed back to the next copy, then the hi | lo words
+            constexpr int IT = 1024 / NT;
+            float x[IT][8];
+#pragma unroll
+            for (int it = 0; it < IT; ++it) {
+                const int r = (t >> 3) + (NT / 8) * it, j = t & 7;
+                const uint4 a = *reinterpret_cast<const uint4*>(sm + Lay::Q + f32_off(r, 8 * j));
+                const uint4 b = *reinterpret_cast<const uint4*>(sm + Lay::Q + f32_off(r, 8 * j + 4));
+                x[it][0] = __uint_as_float(a.x);
+                x[it][1] = __uint_as_float(a.y);
+                x[it][2] = __uint_as_float(a.z);
+                x[it][3] = __uint_as_float(a.w);
+                x[it][4] = __uint_as_float(b.x);
+                x[it][5] = __uint_as_float(b.y);
+                x[it][6] = __uint_as_float(b.z);
+                x[it][7] = __uint_as_float(b.w);
+            }
+            if (t == 0) tma_store_wait_read();  // the last chunk's output has left the operand tile
+            __syncthreads();                    // every Q read is done
+            if (t == 0 && c + 1 < nch) load(c0 + L);
+#pragma unroll
+            for (int it = 0; it < IT; ++it) {
+                const int r = (t >> 3) + (NT / 8) * it, j = t & 7;
+                uint32_t hh[4], ll[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    split_pair(phi_fast(x[it][2 * u]), phi_fast(x[it][2 * u + 1]), hh[u], ll[u]);
+                *reinterpret_cast<uint4*>(sm + Lay::OP + swz(r, j)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                *reinterpret_cast<uint4*>(sm + Lay::OP + kAtom + swz(r, j)) =
+                    make_uint4(ll[0], ll[1], ll[2], ll[3]);
+            }
+        }
+        sync_tc();
         if (t == 0) {
             // Q_hi [S_hi | Z_hi] + Q_hi [S_lo | Z_lo] + Q_lo [S_hi | Z_hi]
 #pragma unroll
@@ -374,8 +540,8 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        if (t == 0 && c + 1 < nch) load(c0 + L);  // the Q tile is consumed
-        {   // V' = num / den, this warpgroup's 32 columns, fp32 into the swizzled staging tile
+        if (sh[1]) goto cleanup;
+        {   // V' = num / den, this warpgroup's 32 columns, fp32 over the consumed operand tile
             const int i = 32 * q + (t & 31);
             float dz[16];
             tmem_ld16(tm + lane + M, dz);
@@ -384,20 +550,23 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             tmem_ld32(tm + lane + 32 * g, v);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<float4*>(sm + Lay::OUT + f32_off(i, 32 * g + 4 * u)) =
+                *reinterpret_cast<float4*>(sm + Lay::OP + f32_off(i, 32 * g + 4 * u)) =
                     make_float4(v[4 * u] * inv, v[4 * u + 1] * inv, v[4 * u + 2] * inv,
                                 v[4 * u + 3] * inv);
         }
         sync_tc();
         if (t == 0) {
-            tma_store_3d(&tmO, sm + Lay::OUT, 0, c0, bh);
-            tma_store_3d(&tmO, sm + Lay::OUT + kAtom, 32, c0, bh);
+            tma_store_3d(&tmO, sm + Lay::OP, 0, c0, bh);
+            tma_store_3d(&tmO, sm + Lay::OP + kAtom, 32, c0, bh);
             tma_store_commit();
         }
     }
 
 cleanup:
-    if (t == 0) tma_store_wait_all();
+    if (t == 0) {  // a copy still in flight after an early exit lands before the CTA leaves
+        if (in_flight) mbar_wait(tma_bar, ld_phase, kWaitLimit);
+        tma_store_wait_all();
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
@@ -1004,13 +1173,14 @@ cudaError_t noncausal_backward_tc_f32(const LaunchCtx& c, const float* Q, const 
     p.spart = sp.part;
     p.rpart = reinterpret_cast<float*>(ws + plan::up256(sizeof(float) * static_cast<size_t>(BH) * sp.spans * W));
     do {
-        CUtensorMap mQ, mK, mV, mG, mdQ, mdK, mdV;
+        CUtensorMap mQ, mK, mV, mG, mdQ, mdK, mdV, mKs, mVs;
         if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D)) ||
             (e = make_map_f32(&mV, V, BH, N, M)) || (e = make_map_f32(&mG, G, BH, N, M)) ||
             (e = make_map_f32(&mdQ, dQ, BH, N, D)) || (e = make_map_f32(&mdK, dK, BH, N, D)) ||
-            (e = make_map_f32(&mdV, dV, BH, N, M)))
+            (e = make_map_f32(&mdV, dV, BH, N, M)) || (e = make_map_f32(&mKs, K, BH, N, D, LS)) ||
+            (e = make_map_f32(&mVs, V, BH, N, M, LS)))
             break;
-        ka<<<BH * sp.spans, NT, LayA::BYTES, c.stream>>>(mK, mV, sp);
+        ka<<<BH * sp.spans, NTS, LayA::BYTES, c.stream>>>(mKs, mVs, sp);
         kq<<<BH * p.q_spans, NTQ, LayQ::BYTES, c.stream>>>(mQ, mG, mdQ, p);
         kk<<<BH * p.k_spans, NTK, LayK::BYTES, c.stream>>>(mK, mV, mdK, mdV, p);
         note_launch(3);
@@ -1052,10 +1222,10 @@ cudaError_t noncausal_forward_tc_f32(const LaunchCtx& c, const float* Q, const f
     if ((e = scratch_alloc(c, reinterpret_cast<void**>(&p.part), part_bytes)) != cudaSuccess) return e;
     do {
         CUtensorMap mQ, mK, mV, mO;
-        if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D)) ||
-            (e = make_map_f32(&mV, V, BH, N, M)) || (e = make_map_f32(&mO, O, BH, N, M)))
+        if ((e = make_map_f32(&mQ, Q, BH, N, D)) || (e = make_map_f32(&mK, K, BH, N, D, LS)) ||
+            (e = make_map_f32(&mV, V, BH, N, M, LS)) || (e = make_map_f32(&mO, O, BH, N, M)))
             break;
-        ka<<<BH * p.spans, NT, LayA::BYTES, c.stream>>>(mK, mV, p);
+        ka<<<BH * p.spans, NTS, LayA::BYTES, c.stream>>>(mK, mV, p);
         kb<<<BH * p.out_spans, NT, LayB::BYTES, c.stream>>>(mQ, mO, p);
         note_launch(2);
         e = cudaGetLastError();

@@ -250,15 +250,15 @@ inline cudaError_t make_map(CUtensorMap* m, const void* base, int BH, int N, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 3-D map over a [BH][N][C] fp32 tensor with a {32, 128, 1} box (128 bytes of
+// 3-D map over a [BH][N][C] fp32 tensor with a {32, rows, 1} box (128 bytes of
 // a row per box) and the 128-byte swizzle.
-inline cudaError_t make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int C) {
+inline cudaError_t make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int C, int rows = L) {
     EncodeTiled enc = encoder();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 4, static_cast<cuuint64_t>(N) * C * 4};
-    cuuint32_t box[3] = {32, static_cast<cuuint32_t>(L), 1};
+    cuuint32_t box[3] = {32, static_cast<cuuint32_t>(rows), 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

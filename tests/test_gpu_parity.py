@@ -233,6 +233,10 @@ def test_noncausal_small(dt, shape):
     (2, 3, 129, 64, 64),      # one chunk and a one-token tail
     (8, 40, 300, 64, 64),     # more heads than resident CTAs
     (1, 2, 4097, 64, 64),     # many spans per head, ragged tail
+    (1, 1, 64, 64, 64),       # one 64-token stage
+    (1, 1, 65, 64, 64),       # a one-token second stage
+    (1, 2, 192, 64, 64),      # fewer stages than ring slots
+    (2, 1, 448, 64, 64),      # more stages than ring slots: slots refilled
 ])
 def test_noncausal_f32_tensor_core_shapes(shape):
     # fp32 at D = M = 64 runs on the tensor cores with operands split into two bf16 terms
