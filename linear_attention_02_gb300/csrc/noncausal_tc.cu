@@ -619,8 +619,8 @@ static_assert(2 * (LayQ::BYTES + 1024) <= 233472u, "two query-side CTAs per SM")
 // hi | lo), the ones atom (2 kAtom after V_hi: the column stride of [V_hi | 1]),
 // the tiles [R_hi | r_hi | R_lo | r_lo] and the fp32 dK and dV staging tiles.
 // Key side: the fp32 dK, dV rows are staged over the K, V tiles they come from, once
-// the products have read them, so that a CTA takes 112 KB and two CTAs of one
-// warpgroup share an SM (the key side's chunks are independent of each other).
+// the products have read them, so that a CTA takes 112 KB and two CTAs of two
+// warpgroups share an SM (the key side's chunks are independent of each other).
 struct LayK {
     static constexpr uint32_t K = 0, V = 2 * kAtom, ONES = 4 * kAtom, R = 5 * kAtom;
     static constexpr uint32_t DK = K, DV = V;
@@ -628,7 +628,7 @@ struct LayK {
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_DK = 0, T_DV = 64, T_COLS = 128;
 };
-constexpr int NTK = 128;  // key-side threads: one per tile row
+constexpr int NTK = 256;  // key-side threads: two per tile row (one per 32-column half)
 static_assert(2 * (LayK::BYTES + 1024) <= 233472u, "two key-side CTAs per SM");
 static_assert(LayQ::BYTES <= 227 * 1024 && LayK::BYTES <= 227 * 1024, "shared memory");
 
@@ -979,7 +979,7 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int bh = unit / p.k_spans, s = unit - bh * p.k_spans;
     const int n0 = s * p.k_len, n1 = min(p.N, n0 + p.k_len);
     const int nch = (n1 - n0 + L - 1) / L;
-    const int q = warp;  // one warpgroup: every thread takes both 32-column halves of its row
+    const int q = warp & 3, g = warp >> 2;  // TMEM lane quarter; the row's 32-column half
     const int row = 32 * q + (t & 31);
     const uint32_t lane = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t sK = smem_u32(sm + Lay::K), sV = smem_u32(sm + Lay::V), sR = smem_u32(sm + Lay::R);
@@ -1004,15 +1004,11 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     };
     if (t == 0) load(n0);
 
-    if (q < D / 32) {  // [R | r] of the head (the query side's partials), split
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            float v[32];
-            const float r =
-                sum_partials(p.rpart + static_cast<size_t>(bh) * p.q_spans * W, p.q_spans, row, g, v);
-            put_state_row(sm + Lay::R, sm + Lay::R + 2 * S_ATOM, row, g, v);
-            if (g == 0) put_ext_row(sm + Lay::R + S_ATOM, sm + Lay::R + 3 * S_ATOM, row, r);
-        }
+    if (q < D / 32) {  // [R | r] of the head (the query side's partials), split: this half
+        float v[32];
+        const float r = sum_partials(p.rpart + static_cast<size_t>(bh) * p.q_spans * W, p.q_spans, row, g, v);
+        put_state_row(sm + Lay::R, sm + Lay::R + 2 * S_ATOM, row, g, v);
+        if (g == 0) put_ext_row(sm + Lay::R + S_ATOM, sm + Lay::R + 3 * S_ATOM, row, r);
     }
 
     for (int c = 0; c < nch; ++c) {
@@ -1048,27 +1044,22 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         wait_bar(mma_bar, mma_phase);
         fence_after_sync();
-        {   // dK = dkf * phi'(K), dV -> fp32 staging tiles over the K, V tiles: phi'(K) of the
-            // whole row is read from the K tile before any thread writes over it
-            float f[2][32];
-#pragma unroll
-            for (int g = 0; g < 2; ++g) dphi_row(sm + Lay::K, row, g, f[g]);
+        {   // dK = dkf * phi'(K), dV -> fp32 staging tiles over the K, V tiles, this thread's
+            // half row: phi'(K) is read from the K tile before any thread writes over it
+            float f[32], v[32];
+            dphi_row(sm + Lay::K, row, g, f);
             __syncthreads();
+            tmem_ld32(tm + lane + Lay::T_DK + 32 * g, v);
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                float v[32];
-                tmem_ld32(tm + lane + Lay::T_DK + 32 * g, v);
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(sm + Lay::DK + f32_off(row, 32 * g + 4 * u)) =
+                    make_float4(v[4 * u] * f[4 * u], v[4 * u + 1] * f[4 * u + 1], v[4 * u + 2] * f[4 * u + 2],
+                                v[4 * u + 3] * f[4 * u + 3]);
+            tmem_ld32(tm + lane + Lay::T_DV + 32 * g, v);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<float4*>(sm + Lay::DK + f32_off(row, 32 * g + 4 * u)) =
-                        make_float4(v[4 * u] * f[g][4 * u], v[4 * u + 1] * f[g][4 * u + 1],
-                                    v[4 * u + 2] * f[g][4 * u + 2], v[4 * u + 3] * f[g][4 * u + 3]);
-                tmem_ld32(tm + lane + Lay::T_DV + 32 * g, v);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<float4*>(sm + Lay::DV + f32_off(row, 32 * g + 4 * u)) =
-                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-            }
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(sm + Lay::DV + f32_off(row, 32 * g + 4 * u)) =
+                    make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         }
         sync_tc();
         if (t == 0) {
