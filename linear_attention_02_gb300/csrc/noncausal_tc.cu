@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "la_launch.h"
 #include "la_plan.h"
@@ -73,6 +74,18 @@ struct LayB {
     static constexpr uint32_t BYTES = BARS + 64;
     static constexpr uint32_t T_COLS = 128;
 };
+
+// Programmatic dependent launch.  launch_dependents: this CTA lets the next
+// kernel in the stream (launched with programmatic stream serialization) start
+// its CTAs; dependency_wait: blocks until the preceding kernel in the stream
+// has completed and its memory is visible (a no-op when this kernel was not
+// launched that way).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 struct NcParams {
     int N, spans, span_len;   // state-kernel spans (the partials' layout)
@@ -250,6 +263,7 @@ nc_state_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = *tmem_slot;
+    pdl_launch_dependents();  // the read-out's CTAs may take free slots and start their copies
 
     const int unit = blockIdx.x;
     const int bh = unit / p.spans, s = unit - bh * p.spans;
@@ -440,6 +454,7 @@ nc_out_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         ld_phase = tma_phase;
     };
     if (t == 0) load(n0);
+    pdl_dependency_wait();  // the state kernel's partials are complete (Q does not depend on it)
 
     if (q < D / 32) {  // [S | Z] of the head, split into hi and lo MN-major tiles: row d, this
                        // warpgroup's 32 columns (and Z for the first)
@@ -761,6 +776,8 @@ ncb_query_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     };
     if (t == 0) load(n0);
+    pdl_launch_dependents();  // the key side's CTAs may take free slots and start their copies
+    pdl_dependency_wait();    // the state pass's partials are complete (Q, G do not depend on it)
 
     if (q < D / 32) {  // [S | Z] of the head, split: row d, both 32-column halves
       for (int g = 0; g < 2; ++g) {
@@ -1003,6 +1020,7 @@ ncb_key_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
     };
     if (t == 0) load(n0);
+    pdl_dependency_wait();  // the query side's partials are complete (K, V do not depend on it)
 
     if (q < D / 32) {  // [R | r] of the head (the query side's partials), split: this half
         float v[32];
@@ -1080,6 +1098,27 @@ cleanup:  // the only early exit follows a copy wait: no copy of this CTA is in 
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, Lay::T_COLS);
+}
+
+// Launches `kern` so that it may start while the kernel before it in `stream`
+// finishes (programmatic stream serialization); the kernel waits for that
+// kernel's results itself (pdl_dependency_wait) and only reads inputs that do
+// not depend on it before then.  Its CTAs start only after every CTA of the
+// kernel before it has started, so none of them can hold a slot it needs.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), int grid, int block, uint32_t smem,
+                             cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Spans for a grid of independent (head, span) units: fewest waves x chunks,
@@ -1172,8 +1211,11 @@ cudaError_t noncausal_backward_tc_f32(const LaunchCtx& c, const float* Q, const 
             (e = make_map_f32(&mVs, V, BH, N, M, LS)))
             break;
         ka<<<BH * sp.spans, NTS, LayA::BYTES, c.stream>>>(mKs, mVs, sp);
-        kq<<<BH * p.q_spans, NTQ, LayQ::BYTES, c.stream>>>(mQ, mG, mdQ, p);
-        kk<<<BH * p.k_spans, NTK, LayK::BYTES, c.stream>>>(mK, mV, mdK, mdV, p);
+        // the query and key sides start under the tail of the kernel before them
+        // (programmatic dependent launch) and wait for its partials in-kernel
+        if ((e = launch_dependent(kq, BH * p.q_spans, NTQ, LayQ::BYTES, c.stream, mQ, mG, mdQ, p)) ||
+            (e = launch_dependent(kk, BH * p.k_spans, NTK, LayK::BYTES, c.stream, mK, mV, mdK, mdV, p)))
+            break;
         note_launch(3);
         e = cudaGetLastError();
     } while (0);
@@ -1217,7 +1259,9 @@ cudaError_t noncausal_forward_tc_f32(const LaunchCtx& c, const float* Q, const f
             (e = make_map_f32(&mV, V, BH, N, M, LS)) || (e = make_map_f32(&mO, O, BH, N, M)))
             break;
         ka<<<BH * p.spans, NTS, LayA::BYTES, c.stream>>>(mK, mV, p);
-        kb<<<BH * p.out_spans, NT, LayB::BYTES, c.stream>>>(mQ, mO, p);
+        // the read-out starts under the state kernel's tail (programmatic dependent launch):
+        // its prologue and first Q copy overlap, and it waits for the partials in-kernel
+        if ((e = launch_dependent(kb, BH * p.out_spans, NT, LayB::BYTES, c.stream, mQ, mO, p))) break;
         note_launch(2);
         e = cudaGetLastError();
     } while (0);
