@@ -118,6 +118,11 @@ la_status la_backward_causal(const void* Q, const void* K, const void* V, const 
  * ("Transformers are RNNs", section 二, eq. linear and the matrix form
  * (phi(Q)phi(K)^T)V = phi(Q)(phi(K)^T V)).
  *   Q, K [B][H][N][D]; V [B][H][N][M] dtype (read);  Out [B][H][N][M] dtype (written).
+ * The call's kernels run in `stream` after the caller's earlier work there.
+ * On the fp32 D = M = 64 path the read-out kernel is launched as a
+ * programmatic dependent of the state kernel (it starts under that kernel's
+ * tail and waits for its partials itself); the chain stays inside the call,
+ * and a CUDA graph that captures the call keeps it.
  */
 la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void* Out,
                                int B, int H, int N, int D, int M, la_dtype dtype,
@@ -137,7 +142,9 @@ la_status la_forward_noncausal(const void* Q, const void* K, const void* V, void
  *   Out  [B][H][N][M] dtype, nullable               (read) the forward's output;
  *        recomputed when NULL
  *   dQ, dK [B][H][N][D]; dV [B][H][N][M] dtype      (written)
- * Outputs may not alias inputs or each other.
+ * Outputs may not alias inputs or each other.  On the fp32 D = M = 64 path
+ * the call's three kernels are chained by programmatic dependent launch, as
+ * in la_forward_noncausal; ordering with the caller's work is unchanged.
  */
 la_status la_backward_noncausal(const void* Q, const void* K, const void* V, const void* Out,
                                 const void* dOut, void* dQ, void* dK, void* dV,
